@@ -1,0 +1,424 @@
+"""Benchmark: bf16 GEMM + fused epilogue throughput (TFLOP/s) on GB300.
+
+One step = one call of the hot path on one batch of synthetic input: by default
+the MLP-forward linear layer D = GELU_tanh(X W^T + bias) with X[8192,4096],
+W[14336,4096], bias[14336] (X ~ N(0,1), W and bias ~ N(0,0.02), bf16, fp32
+accumulation).  `--workload llama_ffn` times the Llama-FFN fusion instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  `value` is the device-timed throughput of the
+whole job (all ranks; inputs resident in HBM); `e2e` is the same metric with the
+host->device copy of the inputs from pinned memory and the device->host copy of
+D inside the timed region; `roofline` relates the kernel's achieved TFLOP/s to
+the measured dense bf16 peak; `cpu_baseline` is the CPU oracle timed on a
+bounded sample of the same workload.  `--impl reference` times that oracle as
+the reference arm.  Under torchrun each rank runs its own replica (the workload
+has no exchange step): weak scaling, no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16 GEMM+epilogue TFLOP/s and % of GB300 dense bf16 peak, per shape"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1000 * 1000
+
+WORKLOADS = {
+    "mlp_gelu": dict(M=8192, N=14336, K=4096, kind="linear", act="gelu_tanh", bias=True,
+                     name="mlp_gelu_8192x14336x4096"),
+    "llama_ffn": dict(M=8192, N=14336, K=4096, kind="ffn", act="silu*", bias=False,
+                      name="llama_ffn_8192x14336x4096"),
+}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(dist, x: float, device=None) -> float:
+    """Max of a float over ranks (identity on one rank)."""
+    if dist is None:
+        return x
+    import torch
+    dev = device if (device is not None and dist.get_backend() == "nccl") else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_replicas(per_rank_units: float, local_seconds: float, dist, device=None):
+    """Whole-job throughput of N independent replicas: all units / the slowest rank's time."""
+    world = dist.get_world_size() if dist is not None else 1
+    slowest = reduce_max(dist, local_seconds, device)
+    return per_rank_units * world / slowest, slowest
+
+
+# ------------------------------------------------------------------ peaks, clocks, traffic
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background (read-only queries)."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t_marks = []
+        self.out_path = os.path.join("/tmp", f"gbgemm_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.out_path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self):
+        self.t_marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.out_path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[6:10]))
+                except Exception:
+                    continue
+        os.unlink(self.out_path)
+        if not rows:
+            return None
+        t0, t1 = (self.t_marks[0], self.t_marks[-1]) if len(self.t_marks) >= 2 else (0, 1e30)
+        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0] or rows
+        sm = sorted(r[1] for r in inside)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4]) if v.lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": "timed region (+-1 s) at 100 ms sampling"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_bf16_gemm_persistent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ workloads
+
+def make_inputs(wl: dict, device):
+    from dense_bf16_gemm_persistent_gb300 import inputs
+    if wl["kind"] == "ffn":
+        return inputs.llama_ffn(device=device, M=wl["M"], N=wl["N"], K=wl["K"])
+    return inputs.mlp_gelu(device=device, M=wl["M"], N=wl["N"], K=wl["K"])
+
+
+def flops_per_step(wl: dict) -> float:
+    per = 2.0 * wl["M"] * wl["N"] * wl["K"]
+    return 2 * per if wl["kind"] == "ffn" else per
+
+
+def step_fn(wl: dict, t: dict, out):
+    import dense_bf16_gemm_persistent_gb300 as gb
+    if wl["kind"] == "ffn":
+        return lambda: gb.ffn_gated(t["X"], t["W1"], t["W3"], out=out)
+    return lambda: gb.linear(t["A"], t["B"], t["bias"], None, act=t["act"], out=out)
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+
+def oracle_sample_run(wl: dict, rows: int, seed: int = 0):
+    """Run the CPU oracle on `rows` full output rows of the workload (CPU-generated
+    inputs of the same recipe, only the rows needed).  Returns (seconds, flops, threads)."""
+    import numpy as np
+    import oracle
+    from dense_bf16_gemm_persistent_gb300 import inputs
+    K, N = wl["K"], wl["N"]
+    if wl["kind"] == "ffn":
+        X = inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed))
+        W1 = inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02))
+        W3 = inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 2, std=0.02))
+        t0 = time.perf_counter()
+        oracle.ffn_gated(X, W1, W3)
+        dt = time.perf_counter() - t0
+        return dt, 4.0 * rows * N * K, oracle.num_threads()
+    A = inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed))
+    B = inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02))
+    bias = inputs.to_bits(inputs.randn_bf16((N,), seed=seed + 2, std=0.02))
+    t0 = time.perf_counter()
+    oracle.linear(A, B, bias, None, "gelu_tanh")
+    dt = time.perf_counter() - t0
+    _ = np
+    return dt, 2.0 * rows * N * K, oracle.num_threads()
+
+
+def calibrate_rows(wl: dict, target_s: float) -> int:
+    """Rows of output the oracle computes in about target_s seconds."""
+    dt, _, _ = oracle_sample_run(wl, 2)
+    rows = max(2, int(2 * target_s / max(dt, 1e-3)))
+    return min(rows, wl["M"])
+
+
+def cpu_baseline(wl: dict, target_s: float = 12.0) -> dict:
+    rows = calibrate_rows(wl, target_s)
+    dt, fl, threads = oracle_sample_run(wl, rows)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{rows} full output rows ({rows}x{wl['N']} entries, K={wl['K']}) of {wl['name']}, "
+                      f"{dt:.1f} s on {threads} host threads"}
+
+
+def run_reference(args, wl: dict):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    rows = calibrate_rows(wl, args.ref_step_s)
+    for _ in range(args.warmup):
+        oracle_sample_run(wl, rows)
+    t0 = time.perf_counter()
+    total_fl = 0.0
+    threads = 1
+    for _ in range(args.steps):
+        _, fl, threads = oracle_sample_run(wl, rows)
+        total_fl += fl
+    dt = time.perf_counter() - t0
+    value = total_fl / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"each step: {rows} full output rows ({rows}x{wl['N']}, K={wl['K']}) "
+                                       f"of {wl['name']} on {threads} host threads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl: dict) -> dict:
+    ws = 2 * (wl["M"] * wl["K"] + wl["N"] * wl["K"] * (2 if wl["kind"] == "ffn" else 1) + wl["M"] * wl["N"])
+    return {"workload": wl["name"], "M": wl["M"], "N": wl["N"], "K": wl["K"],
+            "epilogue": "gelu_tanh(acc + bias)" if wl["kind"] == "linear" else "silu(acc1) * acc3",
+            "l2": f"no flush: inputs+output {ws / 1e6:.0f} MB > 129 MB L2"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, wl: dict):
+    import torch
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    import dense_bf16_gemm_persistent_gb300 as gb
+    gb.lib()
+
+    t = make_inputs(wl, device)
+    out = torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16, device=device)
+    step = step_fn(wl, t, out)
+    stream = torch.cuda.current_stream(device)
+    fl = flops_per_step(wl)
+
+    # pre-warm (clocks to steady state) + W warm-up steps, all untimed
+    sampler = ClockSampler(local)
+    t_end = time.time() + args.prewarm_s
+    step()
+    torch.cuda.synchronize()
+    while time.time() < t_end:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    gb.device_status()
+
+    # timed region: K steps, one event per launch boundary on the launching stream
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    sampler.mark()
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    barrier(dist, device)
+    local_ms = evs[0].elapsed_time(evs[-1])
+    launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    gb.device_status()
+    clocks = sampler.stop()
+    value, slowest_s = aggregate_replicas(fl * args.steps / 1e12, local_ms / 1e3, dist, device)
+
+    # end to end through the public API: pinned host inputs -> device -> kernel -> host
+    e2e = None
+    if not args.skip_e2e:
+        names = ["X", "W1", "W3"] if wl["kind"] == "ffn" else ["A", "B", "bias"]
+        host = {k: t[k].cpu().pin_memory() for k in names}
+        dev_in = {k: torch.empty_like(t[k]) for k in names}
+        host_out = torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16).pin_memory()
+        tin = dict(dev_in)
+        tin["act"] = t.get("act")
+        e2e_step = step_fn(wl, tin, out)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = host_out.numel() * host_out.element_size()
+
+        def full_step():
+            for k in names:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            e2e_step()
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            full_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, args.steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist, device)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            full_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        gb.device_status()
+        e2e_val, _ = aggregate_replicas(fl * n_e2e / 1e12, e0.elapsed_time(e1) / 1e3, dist, device)
+        e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    achieved = fl / (avg_launch_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = recorded_traffic(wl["name"])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": slowest_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(wl),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
+                     "kernel": "gb::gemm_persistent_kernel", "avg_launch_ms": avg_launch_ms,
+                     "flops_per_launch": fl},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "plan": gb.last_plan(),
+    }
+    if not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_s)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mlp_gelu")
+    ap.add_argument("--prewarm-s", type=float, default=1.0, help="untimed seconds of steps before warm-up")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of CPU-oracle work")
+    ap.add_argument("--ref-step-s", type=float, default=4.0, help="reference arm: seconds per step")
+    args = ap.parse_args(argv)
+    if args.warmup < 0 or args.steps < 1:
+        ap.error("--steps >= 1 and --warmup >= 0")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,155 @@
+"""Python binding of gbgemm: persistent tcgen05 bf16 GEMM with a fused epilogue (GB300, sm_103a).
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+library ``libgbgemm.so`` through its C ABI (``include/gbgemm.h``); there is no
+fallback of any kind, and every call raises if the library is missing.
+
+    linear(A, B, bias=None, R=None, act="none")  ->  bf16(act(A @ B.T + bias) + R)
+    ffn_gated(X, W1, W3)                         ->  bf16(silu(X @ W1.T) * (X @ W3.T))
+
+Tensors are torch CUDA bf16 tensors, 2-D with a contiguous last dimension
+(bias: contiguous 1-D).  Work is enqueued on ``torch.cuda.current_stream()``
+unless a stream is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbgemm.so")
+
+ACT = {"none": 0, "gelu_tanh": 1, "silu": 2, "relu": 3}
+STATUS = {0: "GB_OK", 1: "GB_ERR_INVALID_ARG", 2: "GB_ERR_UNSUPPORTED", 3: "GB_ERR_CUDA", 4: "GB_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GBError(RuntimeError):
+    """A non-OK gb_status_t, with the library's message."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgbgemm.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"the CUDA library {LIB_PATH} is not built; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, p, st = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        L.gb_gemm_linear.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64, p]
+        L.gb_gemm_ffn_gated.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p]
+        L.gb_get_device_status.argtypes = [p]
+        L.gb_last_error.argtypes = []
+        L.gb_last_error.restype = ctypes.c_char_p
+        L.gb_set_config.argtypes = [ctypes.c_char_p]
+        L.gb_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        L.gb_set_fault_injection.argtypes = [ctypes.c_int]
+        L.gb_last_plan.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+        L.gb_version.argtypes = []
+        L.gb_version.restype = ctypes.c_char_p
+        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_get_device_status", "gb_set_config",
+                     "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan"):
+            getattr(L, name).restype = st
+        _lib = L
+        return L
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise GBError(status, lib().gb_last_error().decode(errors="replace"))
+
+
+def _mat(t: torch.Tensor | None, name: str, rows: int | None = None, cols: int | None = None):
+    """(pointer, leading dimension in elements) of a 2-D bf16 CUDA tensor."""
+    if t is None:
+        return None, 0
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA bfloat16 tensor, got {t.dtype} on {t.device}")
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name}: expected a 2-D tensor with a contiguous last dimension")
+    if rows is not None and t.shape[0] != rows or cols is not None and t.shape[1] != cols:
+        raise ValueError(f"{name}: shape {tuple(t.shape)} does not match ({rows}, {cols})")
+    ld = t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+    return t.data_ptr(), ld
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def linear(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = None, R: torch.Tensor | None = None,
+           act: str = "none", out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = bf16(act(A @ B.T + bias) + R) on the GPU (A [M,K], B [N,K], bias [N], R [M,N])."""
+    M, K = A.shape
+    N = B.shape[0]
+    if act not in ACT:
+        raise ValueError(f"act must be one of {sorted(ACT)}")
+    pa, lda = _mat(A, "A", M, K)
+    pb, ldb = _mat(B, "B", N, K)
+    pr, ldr = _mat(R, "R", M, N)
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.shape != (N,) or (N > 1 and bias.stride(0) != 1):
+            raise ValueError("bias: expected a contiguous CUDA bfloat16 tensor of shape (N,)")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    pd, ldd = _mat(out, "out", M, N)
+    _check(lib().gb_gemm_linear(pa, lda, pb, ldb, bias.data_ptr() if bias is not None else None, pr, ldr,
+                                ACT[act], pd, ldd, M, N, K, _stream(stream)))
+    return out
+
+
+def ffn_gated(X: torch.Tensor, W1: torch.Tensor, W3: torch.Tensor, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """D = bf16(silu(X @ W1.T) * (X @ W3.T)) on the GPU (X [M,K], W1/W3 [N,K])."""
+    M, K = X.shape
+    N = W1.shape[0]
+    px, ldx = _mat(X, "X", M, K)
+    p1, ld1 = _mat(W1, "W1", N, K)
+    p3, ld3 = _mat(W3, "W3", N, K)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    pd, ldd = _mat(out, "out", M, N)
+    _check(lib().gb_gemm_ffn_gated(px, ldx, p1, ld1, p3, ld3, pd, ldd, M, N, K, _stream(stream)))
+    return out
+
+
+def device_status(stream=None) -> None:
+    """Synchronise the stream and raise GBError if a kernel recorded a device-side fault."""
+    _check(lib().gb_get_device_status(_stream(stream)))
+
+
+def set_config(spec: str | None = None) -> None:
+    """Override the tile heuristic ("bn=128,grid=8,persistent=0,group=4,zigzag=1"); None restores it."""
+    _check(lib().gb_set_config(spec.encode() if spec else None))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().gb_set_wait_timeout_ns(int(ns)))
+
+
+def set_fault_injection(mode: int) -> None:
+    _check(lib().gb_set_fault_injection(int(mode)))
+
+
+def last_plan() -> str:
+    buf = ctypes.create_string_buffer(512)
+    _check(lib().gb_last_plan(buf, len(buf)))
+    return buf.value.decode()
+
+
+def version() -> str:
+    return lib().gb_version().decode()

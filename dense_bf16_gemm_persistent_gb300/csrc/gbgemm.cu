@@ -1,0 +1,435 @@
+// C ABI of the library: argument validation, tile planning, TMA descriptor
+// cache and kernel launch.  The device code lives in gemm_kernel.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cinttypes>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <list>
+#include <mutex>
+#include <string>
+
+#include "../../include/gbgemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using gb::GemmParams;
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;  // TMA coordinates are signed 32-bit
+constexpr int64_t kMaxLd = (int64_t(1) << 39) - 1;   // TMA strides are below 2^40 bytes
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+
+thread_local std::string t_error;
+thread_local std::string t_plan;
+
+gb_status_t fail(gb_status_t s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return s;
+}
+
+gb_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(GB_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// ---------------------------------------------------------------- configuration override
+
+struct Config {
+    int bn = 0;          // 0 = heuristic
+    int grid = 0;        // 0 = one CTA per SM
+    int persistent = 1;  // 0 = one tile per CTA
+    int group = 0;       // 0 = heuristic
+    int zigzag = -1;     // -1 = heuristic
+};
+
+std::mutex g_cfg_mu;
+Config g_cfg;
+uint64_t g_timeout_ns = kDefaultTimeoutNs;
+int g_inject = 0;
+
+Config current_config(uint64_t* timeout, int* inject) {
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    *timeout = g_timeout_ns;
+    *inject = g_inject;
+    return g_cfg;
+}
+
+// ---------------------------------------------------------------- device properties
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+    size_t smem_optin = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+gb_status_t device_info(int* dev_out, DeviceInfo* info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GB_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int v = 0;
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+        if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+        if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
+        d.smem_optin = static_cast<size_t>(v);
+        d.ready = true;
+    }
+    if (d.major != 10 || d.minor != 3)
+        return fail(GB_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, d.major,
+                    d.minor);
+    *dev_out = dev;
+    *info = d;
+    return GB_OK;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct TmapKey {
+    const void* base;
+    uint64_t inner, outer, stride_bytes;
+    uint32_t box_inner, box_outer;
+    int swizzle;
+    bool operator==(const TmapKey& o) const {
+        return base == o.base && inner == o.inner && outer == o.outer && stride_bytes == o.stride_bytes &&
+               box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle;
+    }
+};
+
+std::mutex g_tmap_mu;
+std::list<std::pair<TmapKey, CUtensorMap>> g_tmap_cache;  // most recent first
+constexpr size_t kTmapCacheSize = 128;
+
+// A 2-D bf16 tensor map: `outer` rows of `inner` elements, rows `stride_bytes` apart.
+gb_status_t make_tmap(CUtensorMap* out, const void* base, uint64_t inner, uint64_t outer, uint64_t stride_bytes,
+                      uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    const TmapKey key{base, inner, outer, stride_bytes, box_inner, box_outer, static_cast<int>(swizzle)};
+    {
+        std::lock_guard<std::mutex> lk(g_tmap_mu);
+        for (auto it = g_tmap_cache.begin(); it != g_tmap_cache.end(); ++it) {
+            if (it->first == key) {
+                *out = it->second;
+                if (it != g_tmap_cache.begin()) g_tmap_cache.splice(g_tmap_cache.begin(), g_tmap_cache, it);
+                return GB_OK;
+            }
+        }
+    }
+    auto fn = encode_fn();
+    if (!fn) return fail(GB_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap m;
+    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GB_ERR_CUDA,
+                    "cuTensorMapEncodeTiled failed (%d) for base=%p dims=(%" PRIu64 ",%" PRIu64 ") stride=%" PRIu64
+                    " box=(%u,%u)",
+                    static_cast<int>(r), base, inner, outer, stride_bytes, box_inner, box_outer);
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    g_tmap_cache.emplace_front(key, m);
+    if (g_tmap_cache.size() > kTmapCacheSize) g_tmap_cache.pop_back();
+    *out = m;
+    return GB_OK;
+}
+
+// ---------------------------------------------------------------- kernels and launch
+
+template <int BN, int NUM_B, int STAGES>
+gb_status_t launch(const GemmParams& p, int grid, int dev, const DeviceInfo& info, cudaStream_t stream) {
+    using S = gb::KernelShape<BN, NUM_B, STAGES>;
+    auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES>;
+    static bool attr_set[64] = {};
+    static std::mutex mu;
+    if (S::kSmemBytes > info.smem_optin)
+        return fail(GB_ERR_UNSUPPORTED, "kernel needs %u bytes of shared memory, device allows %zu", S::kSmemBytes,
+                    info.smem_optin);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            attr_set[dev] = true;
+        }
+    }
+    kern<<<grid, gb::kThreads, S::kSmemBytes, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return GB_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Problem {
+    const void* a;
+    int64_t lda;
+    const void* b0;
+    int64_t ldb0;
+    const void* b1;
+    int64_t ldb1;
+    const void* bias;
+    const void* r;
+    int64_t ldr;
+    int act;
+    void* d;
+    int64_t ldd;
+    int64_t m, n, k;
+    bool ffn;
+};
+
+gb_status_t validate(const Problem& pr) {
+    const char* an = pr.ffn ? "X" : "A";
+    const char* bn = pr.ffn ? "W1" : "B";
+    if (pr.m < 0 || pr.n < 0 || pr.k < 0)
+        return fail(GB_ERR_INVALID_ARG, "negative size M=%" PRId64 " N=%" PRId64 " K=%" PRId64, pr.m, pr.n, pr.k);
+    if (pr.act < GB_ACT_NONE || pr.act > GB_ACT_RELU) return fail(GB_ERR_INVALID_ARG, "unknown activation %d", pr.act);
+    if (pr.m > kMaxDim || pr.n > kMaxDim || pr.k > kMaxDim)
+        return fail(GB_ERR_UNSUPPORTED, "sizes must be below 2^31 (M=%" PRId64 " N=%" PRId64 " K=%" PRId64 ")", pr.m,
+                    pr.n, pr.k);
+    if (pr.m == 0 || pr.n == 0) return GB_OK;
+    if (!pr.d) return fail(GB_ERR_INVALID_ARG, "D is null");
+    if (pr.ldd < pr.n) return fail(GB_ERR_INVALID_ARG, "ldd=%" PRId64 " < N=%" PRId64, pr.ldd, pr.n);
+    if (pr.r && pr.ldr < pr.n) return fail(GB_ERR_INVALID_ARG, "ldr=%" PRId64 " < N=%" PRId64, pr.ldr, pr.n);
+    if (pr.k > 0) {
+        if (!pr.a) return fail(GB_ERR_INVALID_ARG, "%s is null", an);
+        if (!pr.b0) return fail(GB_ERR_INVALID_ARG, "%s is null", bn);
+        if (pr.ffn && !pr.b1) return fail(GB_ERR_INVALID_ARG, "W3 is null");
+        if (pr.lda < pr.k) return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < K=%" PRId64, pr.ffn ? "x" : "a", pr.lda, pr.k);
+        if (pr.ldb0 < pr.k)
+            return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < K=%" PRId64, pr.ffn ? "w1" : "b", pr.ldb0, pr.k);
+        if (pr.ffn && pr.ldb1 < pr.k) return fail(GB_ERR_INVALID_ARG, "ldw3=%" PRId64 " < K=%" PRId64, pr.ldb1, pr.k);
+        if (!aligned16(pr.a) || !aligned16(pr.b0) || (pr.ffn && !aligned16(pr.b1)))
+            return fail(GB_ERR_UNSUPPORTED, "operand base addresses must be 16-byte aligned for TMA");
+        if (pr.lda % 8 || pr.ldb0 % 8 || (pr.ffn && pr.ldb1 % 8))
+            return fail(GB_ERR_UNSUPPORTED, "operand leading dimensions must be multiples of 8 elements for TMA");
+        if (pr.lda > kMaxLd || pr.ldb0 > kMaxLd || (pr.ffn && pr.ldb1 > kMaxLd))
+            return fail(GB_ERR_UNSUPPORTED, "operand leading dimension too large for TMA");
+    }
+    if (!aligned2(pr.d) || (pr.r && !aligned2(pr.r)) || (pr.bias && !aligned2(pr.bias)))
+        return fail(GB_ERR_UNSUPPORTED, "D, R and bias must be 2-byte aligned");
+    if (pr.ldd > kMaxLd || (pr.r && pr.ldr > kMaxLd)) return fail(GB_ERR_UNSUPPORTED, "leading dimension too large");
+    return GB_OK;
+}
+
+gb_status_t run(const Problem& pr, void* stream_ptr) {
+    gb_status_t st = validate(pr);
+    if (st != GB_OK) return st;
+    if (pr.m == 0 || pr.n == 0) {
+        t_plan = "empty (no launch)";
+        return GB_OK;
+    }
+    int dev = 0;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != GB_OK) return st;
+    uint64_t timeout_ns;
+    int inject;
+    const Config cfg = current_config(&timeout_ns, &inject);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    // Tile width: the FFN kernel holds two 128-column accumulators per buffer;
+    // the linear kernel uses 256 columns unless N fits in 128.
+    int bn = pr.ffn ? 128 : (cfg.bn ? cfg.bn : (pr.n <= 128 ? 128 : 256));
+    if (pr.ffn && cfg.bn && cfg.bn != 128) return fail(GB_ERR_UNSUPPORTED, "the FFN kernel supports bn=128 only");
+
+    GemmParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.m = static_cast<int32_t>(pr.m);
+    prm.n = static_cast<int32_t>(pr.n);
+    prm.k = static_cast<int32_t>(pr.k);
+    prm.num_m_blocks = static_cast<int32_t>(cdiv(pr.m, gb::kBM));
+    prm.num_n_blocks = static_cast<int32_t>(cdiv(pr.n, bn));
+    prm.num_k_blocks = static_cast<int32_t>(cdiv(pr.k, gb::kBK));
+    const int64_t tiles = static_cast<int64_t>(prm.num_m_blocks) * prm.num_n_blocks;
+    if (tiles > kMaxDim) return fail(GB_ERR_UNSUPPORTED, "too many tiles");
+    prm.num_tiles = static_cast<int32_t>(tiles);
+    int group = cfg.group ? cfg.group : 16;
+    if (group > prm.num_m_blocks) group = prm.num_m_blocks;
+    prm.group_m = group < 1 ? 1 : group;
+    prm.zigzag = cfg.zigzag >= 0 ? cfg.zigzag : (prm.num_k_blocks >= 256 ? 1 : 0);
+    prm.act = pr.ffn ? GB_ACT_NONE : pr.act;
+    prm.bias = static_cast<const uint16_t*>(pr.bias);
+    prm.r = static_cast<const uint16_t*>(pr.r);
+    prm.d = static_cast<uint16_t*>(pr.d);
+    prm.ldr = pr.ldr;
+    prm.ldd = pr.ldd;
+    prm.timeout_ns = timeout_ns;
+    prm.inject = inject;
+    uint32_t flags = 0;
+    if (!pr.ffn && pr.bias) flags |= gb::kFlagBias | (aligned16(pr.bias) ? gb::kFlagBiasVec : 0u);
+    if (!pr.ffn && pr.r) flags |= gb::kFlagResidual | ((aligned16(pr.r) && pr.ldr % 8 == 0) ? gb::kFlagRVec : 0u);
+    const bool d_tma = aligned16(pr.d) && pr.ldd % 8 == 0;
+    if (d_tma) flags |= gb::kFlagDTma;
+    prm.flags = flags;
+
+    if (pr.k > 0) {
+        if ((st = make_tmap(&prm.tm_a, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            GB_OK)
+            return st;
+        if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.k, pr.n, pr.ldb0 * 2, gb::kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            GB_OK)
+            return st;
+        if (pr.ffn &&
+            (st = make_tmap(&prm.tm_b1, pr.b1, pr.k, pr.n, pr.ldb1 * 2, gb::kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+                GB_OK)
+            return st;
+    }
+    if (d_tma &&
+        (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
+        return st;
+
+    int grid = cfg.persistent ? info.sms : prm.num_tiles;
+    if (cfg.grid > 0 && cfg.grid < grid) grid = cfg.grid;
+    if (grid > prm.num_tiles) grid = prm.num_tiles;
+
+    char plan[256];
+    snprintf(plan, sizeof plan,
+             "kernel=%s bm=%d bn=%d bk=%d stages=%d grid=%d tiles=%d k_blocks=%d group=%d zigzag=%d d_store=%s "
+             "r_load=%s",
+             pr.ffn ? "ffn_gated" : "linear", gb::kBM, bn, gb::kBK, (pr.ffn || bn == 256) ? 4 : 6, grid, prm.num_tiles, prm.num_k_blocks,
+             prm.group_m, prm.zigzag, d_tma ? "tma" : "st.global",
+             pr.r ? ((flags & gb::kFlagRVec) ? "ld.v4" : "ld.b16") : "none");
+    t_plan = plan;
+
+    if (pr.ffn) return launch<128, 2, 4>(prm, grid, dev, info, stream);
+    if (bn == 256) return launch<256, 1, 4>(prm, grid, dev, info, stream);
+    if (bn == 128) return launch<128, 1, 6>(prm, grid, dev, info, stream);
+    return fail(GB_ERR_UNSUPPORTED, "unsupported tile width bn=%d (128 or 256)", bn);
+}
+
+bool parse_int(const char* s, size_t n, long* out) {
+    std::string t(s, n);
+    char* end = nullptr;
+    long v = strtol(t.c_str(), &end, 10);
+    if (t.empty() || *end) return false;
+    *out = v;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+gb_status_t gb_gemm_linear(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, const void* R,
+                           int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
+    t_error.clear();
+    Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false};
+    return run(pr, stream);
+}
+
+gb_status_t gb_gemm_ffn_gated(const void* X, int64_t ldx, const void* W1, int64_t ldw1, const void* W3, int64_t ldw3,
+                              void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
+    t_error.clear();
+    Problem pr{X, ldx, W1, ldw1, W3, ldw3, nullptr, nullptr, 0, GB_ACT_NONE, D, ldd, M, N, K, true};
+    return run(pr, stream);
+}
+
+gb_status_t gb_get_device_status(void* stream) {
+    t_error.clear();
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, gb::g_gb_status, sizeof v)) != cudaSuccess)
+        return cuda_fail(e, "reading the device status word");
+    if (v == 0) return GB_OK;
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpyToSymbol(gb::g_gb_status, &zero, sizeof zero)) != cudaSuccess)
+        return cuda_fail(e, "clearing the device status word");
+    const uint32_t code = v & 0xffu, role = (v >> 8) & 0xffu, where = v >> 16;
+    static const char* roles[] = {"?", "producer", "mma", "epilogue"};
+    return fail(static_cast<gb_status_t>(code), "device pipeline wait timed out (role=%s, where=0x%x)",
+                roles[role < 4 ? role : 0], where);
+}
+
+const char* gb_last_error(void) { return t_error.c_str(); }
+
+gb_status_t gb_set_config(const char* spec) {
+    Config c;
+    if (spec && *spec) {
+        const char* s = spec;
+        while (*s) {
+            const char* comma = strchr(s, ',');
+            size_t len = comma ? static_cast<size_t>(comma - s) : strlen(s);
+            const char* eq = static_cast<const char*>(memchr(s, '=', len));
+            if (!eq) return fail(GB_ERR_INVALID_ARG, "config item without '=': %.*s", static_cast<int>(len), s);
+            std::string key(s, static_cast<size_t>(eq - s));
+            long v = 0;
+            if (!parse_int(eq + 1, len - static_cast<size_t>(eq + 1 - s), &v))
+                return fail(GB_ERR_INVALID_ARG, "bad value for %s", key.c_str());
+            if (key == "bn" && (v == 128 || v == 256)) c.bn = static_cast<int>(v);
+            else if (key == "grid" && v >= 0 && v <= 1000000) c.grid = static_cast<int>(v);
+            else if (key == "persistent" && (v == 0 || v == 1)) c.persistent = static_cast<int>(v);
+            else if (key == "group" && v >= 1 && v <= 1000000) c.group = static_cast<int>(v);
+            else if (key == "zigzag" && v >= -1 && v <= 1) c.zigzag = static_cast<int>(v);
+            else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
+            s += len;
+            if (*s == ',') ++s;
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    g_cfg = c;
+    return GB_OK;
+}
+
+gb_status_t gb_set_wait_timeout_ns(uint64_t ns) {
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    g_timeout_ns = ns ? ns : kDefaultTimeoutNs;
+    return GB_OK;
+}
+
+gb_status_t gb_last_plan(char* buf, size_t len) {
+    if (!buf) return fail(GB_ERR_INVALID_ARG, "buf is null");
+    if (len == 0) return GB_OK;
+    snprintf(buf, len, "%s", t_plan.c_str());
+    return GB_OK;
+}
+
+gb_status_t gb_set_fault_injection(int mode) {
+    if (mode != gb::kInjectNone && mode != gb::kInjectSkipFirstStage)
+        return fail(GB_ERR_INVALID_ARG, "unknown fault-injection mode %d", mode);
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    g_inject = mode;
+    return GB_OK;
+}
+
+const char* gb_version(void) { return "0.1.0"; }
+
+}  // extern "C"

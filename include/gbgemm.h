@@ -1,0 +1,166 @@
+/*
+ * gbgemm -- persistent, warp-specialised bf16 GEMM with a fused epilogue for
+ * GB300 (sm_103a): TMA -> shared-memory ring -> tcgen05.mma into TMEM ->
+ * epilogue -> TMA store.  C ABI; plain pointers and sizes only.
+ *
+ * Operations (the problem statement of "Implement persistent matmul
+ * scheduling", NVIDIA/Fuser PR #3812, and "Translate MmaOp patterns properly
+ * on Hopper", NVIDIA/Fuser PR #4072: MatmulOp = A.B, LinearOp = linear layer
+ * with bias, tensors in the EPILOGUE_INPUT role, the Llama-FFN horizontal
+ * fusion; "Automate performant Hopper matmul", NVIDIA/Fuser issue #3819,
+ * section "Epilogue"):
+ *
+ *   gb_gemm_linear    D[m,n] = bf16( act( sum_k A[m,k] B[n,k] + bias[n] ) + R[m,n] )
+ *   gb_gemm_ffn_gated D[m,n] = bf16( silu( sum_k X[m,k] W1[n,k] ) * sum_k X[m,k] W3[n,k] )
+ *
+ * Arithmetic: bf16 operands, fp32 accumulation in tensor memory, fp32
+ * epilogue, one round-to-nearest-even to bf16.  The accumulation order inside
+ * the tensor core is not the sequential k order, so results agree with a
+ * sequential fp32 sum up to rounding.
+ *
+ * Layouts.  Every matrix is row-major bf16 (passed as raw 16-bit storage) with
+ * a leading dimension given in ELEMENTS.  A is [M,K] and B is [N,K]: both
+ * operands are K-major ("TN"), as a linear layer stores its weight.  bias is a
+ * contiguous [N] vector.  R and D are [M,N].
+ *
+ * Ownership.  All pointers are DEVICE pointers owned by the caller and must
+ * stay valid until the work queued on `stream` has finished.  The library
+ * allocates no device memory: it keeps only a host-side cache of TMA
+ * descriptors and a per-device 32-bit status word in its own static device
+ * memory.
+ *
+ * Synchronisation.  Calls only validate, plan and enqueue on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream) and return at once.
+ *
+ * Aliasing.  D must not overlap A, B, X, W1, W3 or bias.  D == R (same pointer
+ * and leading dimension) is allowed: every element of R is read before the same
+ * element of D is written, by the same thread.
+ *
+ * Errors.  Every call returns a gb_status_t; nothing aborts or throws.
+ * gb_last_error() gives a message for the last non-OK status on the calling
+ * thread.  Faults that can only be seen on the device (a pipeline wait that
+ * ran out of time) are recorded in the device status word and reported by
+ * gb_get_device_status().
+ *
+ * Limits.  0 <= M, N, K < 2^31; leading dimensions >= the row length.
+ * A, B, X, W1, W3: base address 16-byte aligned and leading dimension a
+ * multiple of 8 elements (TMA requires 16-byte aligned rows), else
+ * GB_ERR_UNSUPPORTED.  D, R, bias: any 2-byte aligned address and leading
+ * dimension; when D (or R) is 16-byte aligned with a leading dimension that is
+ * a multiple of 8, it moves by TMA, otherwise by predicated plain loads and
+ * stores.  M == 0 or N == 0 is a no-op.  K == 0 gives D = act(bias) + R.
+ */
+#ifndef GBGEMM_H
+#define GBGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GB_API __attribute__((visibility("default")))
+#else
+#define GB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GB_OK = 0,
+    GB_ERR_INVALID_ARG = 1,  /* a null pointer, a negative size, a too-small leading dimension */
+    GB_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels handle (alignment, size) */
+    GB_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (message in gb_last_error) */
+    GB_ERR_TIMEOUT = 4       /* a device pipeline wait ran out of time (gb_get_device_status) */
+} gb_status_t;
+
+typedef enum {
+    GB_ACT_NONE = 0,
+    GB_ACT_GELU_TANH = 1,    /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+    GB_ACT_SILU = 2,         /* x / (1 + exp(-x)) */
+    GB_ACT_RELU = 3          /* max(x, 0) */
+} gb_act_t;
+
+/*
+ * D = bf16( act(A . B^T + bias) + R ).
+ * Matmul / linear layer with its fused epilogue ("Automate performant Hopper
+ * matmul", sections "Persistent matmul" and "Epilogue"; the EPILOGUE_INPUT
+ * role in "Translate MmaOp patterns properly on Hopper").
+ *   A    [M,K], leading dimension lda (elements)        required if M,K > 0
+ *   B    [N,K], leading dimension ldb                   required if N,K > 0
+ *   bias [N] or NULL (no bias)
+ *   R    [M,N] with leading dimension ldr, or NULL (no epilogue input)
+ *   act  a gb_act_t value
+ *   D    [M,N] with leading dimension ldd               required if M,N > 0
+ *   stream  cudaStream_t to enqueue on
+ * Returns GB_OK once the work is enqueued.
+ */
+GB_API gb_status_t gb_gemm_linear(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* bias, const void* R, int64_t ldr, int act,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                           void* stream);
+
+/*
+ * D = bf16( silu(X . W1^T) * (X . W3^T) ): the Llama-FFN horizontal fusion,
+ * two products sharing the X operand, both fp32-accumulated before the
+ * epilogue ("Translate MmaOp patterns properly on Hopper", commit "Fix llama
+ * ffn horizontal fusion on Ampere").
+ *   X  [M,K] (ldx), W1 [N,K] (ldw1), W3 [N,K] (ldw3), D [M,N] (ldd).
+ */
+GB_API gb_status_t gb_gemm_ffn_gated(const void* X, int64_t ldx, const void* W1, int64_t ldw1,
+                              const void* W3, int64_t ldw3, void* D, int64_t ldd,
+                              int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * GB_OK if no kernel recorded a fault since the last call; GB_ERR_TIMEOUT if a
+ * pipeline wait ran out of time (the kernel then stopped early and its output
+ * is undefined); GB_ERR_CUDA if the synchronisation itself failed.
+ * gb_last_error() then names the role and stage that gave up.
+ */
+GB_API gb_status_t gb_get_device_status(void* stream);
+
+/* Message for the last non-OK status returned on the calling thread ("" if none).
+ * The pointer stays valid until the next gbgemm call on the same thread. */
+GB_API const char* gb_last_error(void);
+
+/*
+ * Tile-configuration override, the analogue of a heuristic plugin.  `spec` is
+ * a comma-separated list of key=value pairs, or NULL / "" to restore the
+ * built-in heuristic.  Keys: bn (linear tile width: 128 or 256), grid (maximum
+ * number of CTAs; 0 = one per SM), persistent (0 = one tile per CTA),
+ * group (tile-swizzle group size along M, >= 1), zigzag (0, 1, or -1 = auto).
+ * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
+ */
+GB_API gb_status_t gb_set_config(const char* spec);
+
+/*
+ * Upper bound, in nanoseconds, on every pipeline wait inside the kernels
+ * (default 4e9, i.e. 4 s; 0 restores the default).  A wait that runs out
+ * records GB_ERR_TIMEOUT in the device status word and the kernel returns.
+ */
+GB_API gb_status_t gb_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook for the failure path (process-wide).  mode 0: off (default).
+ * mode 1: the producer never issues its first pipeline stage, so the MMA
+ * role's wait on that stage runs out after the wait limit; every role then
+ * stops, drains what it has in flight, frees TMEM and returns, and
+ * gb_get_device_status() reports GB_ERR_TIMEOUT.  The output is undefined.
+ * Nothing faults or hangs.  Returns GB_ERR_INVALID_ARG for other modes.
+ */
+GB_API gb_status_t gb_set_fault_injection(int mode);
+
+/* Writes a one-line description of the last plan chosen on this thread
+ * (tile shape, stages, grid, swizzle, store path) into buf (NUL-terminated,
+ * truncated to len). Returns GB_OK, or GB_ERR_INVALID_ARG for a null buf. */
+GB_API gb_status_t gb_last_plan(char* buf, size_t len);
+
+/* Library version as "major.minor.patch". */
+GB_API const char* gb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBGEMM_H */

@@ -1,0 +1,125 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol the header
+declares, and rejects invalid arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbgemm.h")
+
+GB_OK, GB_ERR_INVALID_ARG, GB_ERR_UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dense_bf16_gemm_persistent_gb300 import _build
+    _build.build()
+    import dense_bf16_gemm_persistent_gb300 as gb
+    return gb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gb_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_get_device_status", "gb_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in gbgemm.h but not exported"
+
+
+def test_version(L):
+    assert re.fullmatch(r"\d+\.\d+\.\d+", L.gb_version().decode())
+
+
+# Fake, never-dereferenced device addresses: validation rejects the call first.
+P16 = 0x10000      # 16-byte aligned
+P2 = 0x10002       # 2-byte aligned only
+P1 = 0x10001       # odd
+
+
+def lin(L, A=P16, lda=64, B=P16, ldb=64, bias=None, R=None, ldr=0, act=0, D=P16, ldd=32, M=16, N=32, K=64):
+    return L.gb_gemm_linear(A, lda, B, ldb, bias, R, ldr, act, D, ldd, M, N, K, None)
+
+
+@pytest.mark.parametrize("kwargs,status,needle", [
+    (dict(A=None), GB_ERR_INVALID_ARG, "A is null"),
+    (dict(B=None), GB_ERR_INVALID_ARG, "B is null"),
+    (dict(D=None), GB_ERR_INVALID_ARG, "D is null"),
+    (dict(M=-1), GB_ERR_INVALID_ARG, "negative"),
+    (dict(K=-5), GB_ERR_INVALID_ARG, "negative"),
+    (dict(lda=32), GB_ERR_INVALID_ARG, "lda"),
+    (dict(ldb=8), GB_ERR_INVALID_ARG, "ldb"),
+    (dict(ldd=31), GB_ERR_INVALID_ARG, "ldd"),
+    (dict(R=P16, ldr=16), GB_ERR_INVALID_ARG, "ldr"),
+    (dict(act=7), GB_ERR_INVALID_ARG, "activation"),
+    (dict(act=-1), GB_ERR_INVALID_ARG, "activation"),
+    (dict(A=P2), GB_ERR_UNSUPPORTED, "16-byte"),
+    (dict(B=P2), GB_ERR_UNSUPPORTED, "16-byte"),
+    (dict(lda=68, K=60), GB_ERR_UNSUPPORTED, "multiples of 8"),
+    (dict(D=P1), GB_ERR_UNSUPPORTED, "2-byte"),
+    (dict(bias=P1), GB_ERR_UNSUPPORTED, "2-byte"),
+    (dict(M=1 << 31), GB_ERR_UNSUPPORTED, "2^31"),
+    (dict(K=1 << 31, lda=1 << 31, ldb=1 << 31), GB_ERR_UNSUPPORTED, "2^31"),
+])
+def test_linear_rejects(L, kwargs, status, needle):
+    assert lin(L, **kwargs) == status
+    assert needle in L.gb_last_error().decode()
+
+
+def test_empty_problem_is_a_noop(L):
+    # M == 0 or N == 0: nothing to compute, no device call, GB_OK even with null pointers
+    assert L.gb_gemm_linear(None, 0, None, 0, None, None, 0, 0, None, 0, 0, 5, 7, None) == GB_OK
+    assert L.gb_gemm_linear(None, 0, None, 0, None, None, 0, 0, None, 0, 5, 0, 7, None) == GB_OK
+    assert L.gb_gemm_ffn_gated(None, 0, None, 0, None, 0, None, 0, 0, 4, 4, None) == GB_OK
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((None, 64, P16, 64, P16, 64, P16, 32, 16, 32, 64), "X is null"),
+    ((P16, 64, None, 64, P16, 64, P16, 32, 16, 32, 64), "W1 is null"),
+    ((P16, 64, P16, 64, None, 64, P16, 32, 16, 32, 64), "W3 is null"),
+    ((P16, 64, P16, 64, P16, 32, P16, 32, 16, 32, 64), "ldw3"),
+    ((P16, 64, P16, 64, P2, 64, P16, 32, 16, 32, 64), "16-byte"),
+])
+def test_ffn_rejects(L, args, needle):
+    assert L.gb_gemm_ffn_gated(*args, None) != GB_OK
+    assert needle in L.gb_last_error().decode()
+
+
+def test_config_parser(L):
+    assert L.gb_set_config(b"bn=128,grid=4,persistent=0,group=8,zigzag=1") == GB_OK
+    assert L.gb_set_config(None) == GB_OK
+    assert L.gb_set_config(b"") == GB_OK
+    for bad in (b"bn=96", b"nope=1", b"grid", b"group=0", b"zigzag=2", b"bn=12x"):
+        assert L.gb_set_config(bad) == GB_ERR_INVALID_ARG, bad
+    assert L.gb_set_config(None) == GB_OK
+
+
+def test_misc_entry_points(L):
+    assert L.gb_set_wait_timeout_ns(1000) == GB_OK
+    assert L.gb_set_wait_timeout_ns(0) == GB_OK
+    assert L.gb_set_fault_injection(9) == GB_ERR_INVALID_ARG
+    assert L.gb_set_fault_injection(0) == GB_OK
+    assert L.gb_last_plan(None, 10) == GB_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(64)
+    assert L.gb_last_plan(buf, 64) == GB_OK
+
+
+def test_kernels_have_no_stack_frame_or_spills(L):
+    """Every kernel compiles with 0 bytes of stack frame and no spills (ptxas -v)."""
+    from dense_bf16_gemm_persistent_gb300 import _build
+    log = open(os.path.join(_build.LOG_DIR, "ptxas.log")).read()
+    entries = re.findall(r"Compiling entry function '(\w+)'", log)
+    props = re.findall(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", log)
+    assert entries and len(props) >= len(entries)
+    for e, (stack, st, ld) in zip(entries, props):
+        assert (int(stack), int(st), int(ld)) == (0, 0, 0), e

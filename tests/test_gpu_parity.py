@@ -1,0 +1,236 @@
+"""CUDA path vs the CPU oracle on sizes the oracle finishes in seconds: every
+output element is compared.  Shapes span several tiles and ragged tails; the
+epilogue variants, store paths, the configuration overrides and the edge cases
+(K = 0, M or N = 0, one row, D aliasing R) are all covered."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_bf16_gemm_persistent_gb300 as gb
+from dense_bf16_gemm_persistent_gb300 import inputs
+from tests.gpu_util import assert_bitexact, assert_close, bits, int_tensor
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _reset_config():
+    gb.set_config(None)
+    yield
+    gb.set_config(None)
+    gb.device_status()
+
+
+def run_linear(A, B, bias=None, R=None, act="none", **kw):
+    d = gb.linear(A.to(DEV), B.to(DEV), None if bias is None else bias.to(DEV),
+                  None if R is None else R.to(DEV), act=act, **kw)
+    gb.device_status()
+    return bits(d)
+
+
+def ref_linear(A, B, bias=None, R=None, act="none"):
+    return oracle.linear(bits(A), bits(B), None if bias is None else bits(bias),
+                         None if R is None else bits(R), act)
+
+
+def test_plain_256x384x512():
+    """The plain-matmul workload: A[256,512], B[384,512] ~ N(0,1), seed 0, no epilogue."""
+    w = inputs.plain()
+    assert_close(run_linear(w["A"], w["B"]), ref_linear(w["A"], w["B"]), "plain")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (300, 700, 520), (1, 1, 8), (129, 257, 72),
+                                   (127, 255, 4096), (513, 96, 1000)])
+def test_integer_inputs_bit_exact(M, N, K):
+    """Small-integer operands: every partial sum is exact in fp32 in any order, so the
+    GPU must reproduce the oracle bit for bit."""
+    A = int_tensor((M, K), 1)
+    B = int_tensor((N, K), 2)
+    bias = int_tensor((N,), 3, -4, 4)
+    R = int_tensor((M, N), 4, -4, 4)
+    assert_bitexact(run_linear(A, B), ref_linear(A, B), "no epilogue")
+    assert_bitexact(run_linear(A, B, bias, R, "relu"), ref_linear(A, B, bias, R, "relu"), "bias+relu+R")
+
+
+def test_index_pattern_exact():
+    """D[m,n] = m + 16 n (exact): catches swapped rows/columns and tile-placement errors."""
+    M, N, K = 300, 260, 64
+    a = torch.zeros(M, K)
+    a[:, 0] = torch.arange(M) % 128
+    a[:, 1] = 1
+    b = torch.zeros(N, K)
+    b[:, 0] = 1
+    b[:, 1] = 16 * (torch.arange(N) % 16)
+    A, B = a.to(torch.bfloat16), b.to(torch.bfloat16)
+    want = ((torch.arange(M) % 128)[:, None] + 16 * (torch.arange(N) % 16)[None, :]).float().to(torch.bfloat16)
+    assert_bitexact(run_linear(A, B), bits(want), "index pattern")
+
+
+@pytest.mark.parametrize("M", [1, 127, 128, 129, 255, 257])
+@pytest.mark.parametrize("N", [1, 96, 128, 129, 256, 257, 520])
+@pytest.mark.parametrize("K", [8, 64, 200])
+def test_tile_edges(M, N, K):
+    A = inputs.randn_bf16((M, K), seed=M * 7 + N)
+    B = inputs.randn_bf16((N, K), seed=N * 11 + K, std=1.0 / np.sqrt(K))
+    assert_close(run_linear(A, B), ref_linear(A, B), f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("act", ["none", "gelu_tanh", "silu", "relu"])
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("with_r", [False, True])
+def test_epilogue_variants(act, with_bias, with_r):
+    M, N, K = 333, 777, 320
+    A = inputs.randn_bf16((M, K), seed=20)
+    B = inputs.randn_bf16((N, K), seed=21, std=0.1)
+    bias = inputs.randn_bf16((N,), seed=22, std=0.5) if with_bias else None
+    R = inputs.randn_bf16((M, N), seed=23) if with_r else None
+    assert_close(run_linear(A, B, bias, R, act), ref_linear(A, B, bias, R, act), f"{act} {with_bias} {with_r}")
+
+
+def test_unaligned_d_and_r_use_plain_loads_and_stores():
+    """N = 4099: rows of D and R are 8198 bytes apart (not a multiple of 16), so the
+    kernel takes the predicated st.global / scalar-load path."""
+    M, N, K = 200, 4099, 128
+    A = inputs.randn_bf16((M, K), seed=30)
+    B = inputs.randn_bf16((N, K), seed=31, std=1.0 / np.sqrt(K))
+    R = inputs.randn_bf16((M, N), seed=32)
+    got = run_linear(A, B, None, R)
+    assert "d_store=st.global" in gb.last_plan()
+    assert_close(got, ref_linear(A, B, None, R), "N=4099")
+
+
+def test_strided_views_and_offset_d():
+    """Operands with leading dimension > K, and D / R as column slices of bigger buffers."""
+    M, N, K = 190, 300, 136
+    Abig = inputs.randn_bf16((M, K + 40), seed=40)
+    Bbig = inputs.randn_bf16((N, K + 24), seed=41, std=0.1)
+    A, B = Abig[:, 8:8 + K], Bbig[:, 16:16 + K]
+    Rbig = inputs.randn_bf16((M, N + 13), seed=42)
+    R = Rbig[:, 5:5 + N]
+    Dbig = torch.zeros((M, N + 9), dtype=torch.bfloat16, device=DEV)
+    D = Dbig[:, 3:3 + N]
+    gb.linear(A.to(DEV), B.to(DEV), None, R.to(DEV), act="silu", out=D)
+    gb.device_status()
+    assert_close(bits(D), oracle.linear(bits(A.contiguous()), bits(B.contiguous()), None, bits(R.contiguous()),
+                                        "silu"), "strided")
+    # columns outside the view are untouched
+    assert torch.all(Dbig[:, :3] == 0) and torch.all(Dbig[:, 3 + N:] == 0)
+
+
+def test_d_aliases_r():
+    M, N, K = 260, 384, 96
+    A = inputs.randn_bf16((M, K), seed=50)
+    B = inputs.randn_bf16((N, K), seed=51, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=52)
+    ref = ref_linear(A, B, None, R, "gelu_tanh")
+    RD = R.to(DEV).clone()
+    gb.linear(A.to(DEV), B.to(DEV), None, RD, act="gelu_tanh", out=RD)
+    gb.device_status()
+    assert_close(bits(RD), ref, "D == R")
+
+
+def test_k_zero_gives_epilogue_of_zero():
+    M, N = 150, 270
+    A = torch.zeros((M, 0), dtype=torch.bfloat16)
+    B = torch.zeros((N, 0), dtype=torch.bfloat16)
+    bias = inputs.randn_bf16((N,), seed=60)
+    R = inputs.randn_bf16((M, N), seed=61)
+    d = gb.linear(torch.empty((M, 0), dtype=torch.bfloat16, device=DEV),
+                  torch.empty((N, 0), dtype=torch.bfloat16, device=DEV), bias.to(DEV), R.to(DEV), act="gelu_tanh")
+    gb.device_status()
+    assert_close(bits(d), oracle.linear(bits(A), bits(B), bits(bias), bits(R), "gelu_tanh"), "K=0")
+
+
+def test_empty_outputs():
+    A = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    B = torch.empty((32, 64), dtype=torch.bfloat16, device=DEV)
+    assert gb.linear(A, B).shape == (0, 32)
+    assert gb.linear(B, A).shape == (32, 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 500, 200), (1, 7, 8), (257, 129, 1000)])
+def test_ffn_gated(M, N, K):
+    X = inputs.randn_bf16((M, K), seed=70)
+    W1 = inputs.randn_bf16((N, K), seed=71, std=1.0 / np.sqrt(K))
+    W3 = inputs.randn_bf16((N, K), seed=72, std=1.0 / np.sqrt(K))
+    d = gb.ffn_gated(X.to(DEV), W1.to(DEV), W3.to(DEV))
+    gb.device_status()
+    assert_close(bits(d), oracle.ffn_gated(bits(X), bits(W1), bits(W3)), f"ffn {M}x{N}x{K}")
+
+
+def test_ffn_integer_bit_exact_when_gate_is_relu_like():
+    """With W1 chosen so that X.W1^T is a large positive or zero integer, silu is x or 0
+    exactly in fp32, and the product with an integer X.W3^T is exact."""
+    M, N, K = 130, 140, 64
+    X = int_tensor((M, K), 80, 0, 1)
+    W1 = torch.zeros((N, K))
+    W1[:, 0] = 200.0
+    W1[::3, 0] = 0.0                 # every third column: X.W1^T = 0 -> silu = 0
+    X[:, 0] = 1                      # so X.W1^T = 200 (silu(200) == 200 in fp32) or 0
+    W3 = int_tensor((N, K), 81, -2, 2)
+    W1b = W1.to(torch.bfloat16)
+    d = gb.ffn_gated(X.to(DEV), W1b.to(DEV), W3.to(DEV))
+    gb.device_status()
+    assert_bitexact(bits(d), oracle.ffn_gated(bits(X), bits(W1b), bits(W3)), "ffn exact")
+
+
+@pytest.mark.parametrize("spec", ["bn=128", "bn=256", "persistent=0", "grid=3", "grid=1", "group=1",
+                                  "group=3,grid=5", "bn=128,grid=7,group=2"])
+def test_config_overrides_give_identical_bits(spec):
+    """Tile size, grid, swizzle and persistence change which CTA computes a tile but not
+    the per-element accumulation order within the tile: identical bits."""
+    M, N, K = 700, 900, 256
+    A = inputs.randn_bf16((M, K), seed=90)
+    B = inputs.randn_bf16((N, K), seed=91, std=0.1)
+    bias = inputs.randn_bf16((N,), seed=92, std=0.1)
+    base = run_linear(A, B, bias, None, "gelu_tanh")
+    gb.set_config(spec)
+    got = run_linear(A, B, bias, None, "gelu_tanh")
+    assert_bitexact(got, base, spec)
+    assert_close(got, ref_linear(A, B, bias, None, "gelu_tanh"), spec)
+
+
+@pytest.mark.parametrize("spec", ["zigzag=1,grid=4", "zigzag=1,grid=1", "zigzag=0,grid=4"])
+def test_zigzag(spec):
+    """Reversing K changes the accumulation order: within tolerance on random inputs,
+    bit-exact on integer inputs."""
+    M, N, K = 520, 600, 640
+    gb.set_config(spec)
+    A = inputs.randn_bf16((M, K), seed=93)
+    B = inputs.randn_bf16((N, K), seed=94, std=1.0 / np.sqrt(K))
+    assert_close(run_linear(A, B), ref_linear(A, B), spec)
+    Ai, Bi = int_tensor((M, K), 95), int_tensor((N, K), 96)
+    assert_bitexact(run_linear(Ai, Bi), ref_linear(Ai, Bi), spec)
+
+
+def test_golden_fixtures():
+    from tests import golden
+    for name in golden.FIXTURES:
+        g = golden.load(name)
+        t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(DEV) for k, v in g.items()}
+        if "X" in g:
+            d = gb.ffn_gated(t["X"], t["W1"], t["W3"])
+        else:
+            act = "gelu_tanh" if "gelu" in name else ("silu" if "silu" in name else "none")
+            d = gb.linear(t["A"], t["B"], t.get("bias"), t.get("R"), act=act)
+        gb.device_status()
+        assert_close(bits(d), g["D"], name)
+
+
+def test_repeated_calls_and_streams():
+    """Back-to-back launches on a side stream reuse cached descriptors and stay correct."""
+    M, N, K = 384, 512, 192
+    A = inputs.randn_bf16((M, K), seed=100)
+    B = inputs.randn_bf16((N, K), seed=101, std=0.1)
+    ref = ref_linear(A, B, None, None, "relu")
+    s = torch.cuda.Stream()
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        outs = [gb.linear(Ad, Bd, act="relu") for _ in range(5)]
+    gb.device_status(s)
+    for o in outs:
+        assert_close(bits(o), ref, "repeat")
