@@ -204,41 +204,43 @@ def step_fn(wl: dict, t: dict, out):
 
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
 
-def oracle_sample_run(wl: dict, rows: int, seed: int = 0):
-    """Run the CPU oracle on `rows` full output rows of the workload (CPU-generated
-    inputs of the same recipe, only the rows needed).  Returns (seconds, flops, threads)."""
-    import numpy as np
-    import oracle
+def oracle_sample_inputs(wl: dict, rows: int, seed: int = 0) -> dict:
+    """CPU-generated inputs (same recipe as the GPU run) for `rows` output rows."""
     from dense_bf16_gemm_persistent_gb300 import inputs
     K, N = wl["K"], wl["N"]
     if wl["kind"] == "ffn":
-        X = inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed))
-        W1 = inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02))
-        W3 = inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 2, std=0.02))
+        return {"X": inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed)),
+                "W1": inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02)),
+                "W3": inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 2, std=0.02))}
+    return {"A": inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed)),
+            "B": inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02)),
+            "bias": inputs.to_bits(inputs.randn_bf16((N,), seed=seed + 2, std=0.02))}
+
+
+def oracle_sample_run(wl: dict, h: dict, rows: int):
+    """Run the CPU oracle on the first `rows` output rows.  Returns (seconds, flops, threads)."""
+    import oracle
+    K, N = wl["K"], wl["N"]
+    if wl["kind"] == "ffn":
         t0 = time.perf_counter()
-        oracle.ffn_gated(X, W1, W3)
-        dt = time.perf_counter() - t0
-        return dt, 4.0 * rows * N * K, oracle.num_threads()
-    A = inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed))
-    B = inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02))
-    bias = inputs.to_bits(inputs.randn_bf16((N,), seed=seed + 2, std=0.02))
+        oracle.ffn_gated(h["X"][:rows], h["W1"], h["W3"])
+        return time.perf_counter() - t0, 4.0 * rows * N * K, oracle.num_threads()
     t0 = time.perf_counter()
-    oracle.linear(A, B, bias, None, "gelu_tanh")
-    dt = time.perf_counter() - t0
-    _ = np
-    return dt, 2.0 * rows * N * K, oracle.num_threads()
+    oracle.linear(h["A"][:rows], h["B"], h["bias"], None, "gelu_tanh")
+    return time.perf_counter() - t0, 2.0 * rows * N * K, oracle.num_threads()
 
 
-def calibrate_rows(wl: dict, target_s: float) -> int:
-    """Rows of output the oracle computes in about target_s seconds."""
-    dt, _, _ = oracle_sample_run(wl, 2)
-    rows = max(2, int(2 * target_s / max(dt, 1e-3)))
-    return min(rows, wl["M"])
+def calibrate_rows(wl: dict, target_s: float) -> tuple[int, dict]:
+    """Rows of output the oracle computes in about target_s seconds, and their inputs."""
+    h = oracle_sample_inputs(wl, 4)
+    dt, _, _ = oracle_sample_run(wl, h, 4)
+    rows = min(max(4, int(4 * target_s / max(dt, 1e-3))), wl["M"])
+    return rows, oracle_sample_inputs(wl, rows)
 
 
 def cpu_baseline(wl: dict, target_s: float = 12.0) -> dict:
-    rows = calibrate_rows(wl, target_s)
-    dt, fl, threads = oracle_sample_run(wl, rows)
+    rows, h = calibrate_rows(wl, target_s)
+    dt, fl, threads = oracle_sample_run(wl, h, rows)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{rows} full output rows ({rows}x{wl['N']} entries, K={wl['K']}) of {wl['name']}, "
                       f"{dt:.1f} s on {threads} host threads"}
@@ -248,19 +250,17 @@ def run_reference(args, wl: dict):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    rows = calibrate_rows(wl, args.ref_step_s)
+    rows, h = calibrate_rows(wl, args.ref_step_s)
     for _ in range(args.warmup):
-        oracle_sample_run(wl, rows)
-    t0 = time.perf_counter()
-    total_fl = 0.0
-    threads = 1
+        oracle_sample_run(wl, h, rows)
+    total_s, total_fl, threads = 0.0, 0.0, 1
     for _ in range(args.steps):
-        _, fl, threads = oracle_sample_run(wl, rows)
+        dt, fl, threads = oracle_sample_run(wl, h, rows)
+        total_s += dt
         total_fl += fl
-    dt = time.perf_counter() - t0
-    value = total_fl / dt / 1e12
+    value = total_fl / total_s / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": config_of(wl),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",

@@ -128,20 +128,20 @@ def sample_indices(M: int, N: int, *, seed: int = 1234, rows: int = 256, cols: i
                    tile_m: int = 128, tile_n: int = 256) -> tuple[np.ndarray, np.ndarray]:
     """Rows and columns of a sampled output grid (|rows| * |cols| entries, 65536 by default).
 
-    The grid always holds the first and last row/column and the first and last
-    row/column of every tile boundary that fits; the rest are drawn uniformly
-    without replacement from ``numpy.random.default_rng(seed)``.  Returned sorted."""
+    The grid always holds the first and last row/column and both sides of up to
+    rows/8 (cols/8) tile boundaries spread evenly over the range; the rest are drawn
+    uniformly without replacement from ``numpy.random.default_rng(seed)``.  Sorted."""
     rng = np.random.default_rng(seed)
 
     def pick(extent: int, want: int, tile: int) -> np.ndarray:
         if extent <= want:
             return np.arange(extent, dtype=np.int64)
-        special = {0, extent - 1}
-        for b in range(tile, extent, tile):
-            if len(special) + 2 > want // 2:
-                break
-            special.update((b - 1, b))
-        special = np.array(sorted(special), dtype=np.int64)
+        # first/last index, plus both sides of tile boundaries spread evenly over the range
+        bounds = np.arange(tile, extent, tile, dtype=np.int64)
+        nb = min(bounds.size, want // 8)
+        if nb:
+            bounds = bounds[np.linspace(0, bounds.size - 1, nb).round().astype(np.int64)]
+        special = np.unique(np.concatenate([[0, extent - 1], bounds - 1, bounds]))
         rest = np.setdiff1d(np.arange(extent, dtype=np.int64), special)
         extra = rng.choice(rest, size=want - special.size, replace=False)
         return np.sort(np.concatenate([special, extra]))

@@ -53,15 +53,17 @@ enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_GELU_TANH = 1, ORACLE_ACT_SILU = 2, ORACL
 /* ---- bf16 <-> binary32 / binary64 conversions -------------------------------- */
 
 /* A bf16 value is the upper 16 bits of an IEEE binary32 value. */
-float oracle_bf16_to_f32(uint16_t h) {
+static inline float bf16_to_f32(uint16_t h) {
     uint32_t u = (uint32_t)h << 16;
     float f;
     memcpy(&f, &u, sizeof f);
     return f;
 }
 
+float oracle_bf16_to_f32(uint16_t h) { return bf16_to_f32(h); }
+
 /* Round a binary32 value to bf16, nearest with ties to even. */
-uint16_t oracle_f32_to_bf16(float f) {
+static inline uint16_t f32_to_bf16(float f) {
     uint32_t u;
     memcpy(&u, &f, sizeof u);
     if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays NaN */
@@ -69,6 +71,8 @@ uint16_t oracle_f32_to_bf16(float f) {
     u += 0x7fffu + lsb;
     return (uint16_t)(u >> 16);
 }
+
+uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16(f); }
 
 /* Round a binary64 value straight to bf16 (nearest, ties to even), with no
  * intermediate rounding to binary32.  bf16 keeps 8 significant bits; below the
@@ -92,7 +96,7 @@ uint16_t oracle_f64_to_bf16(double x) {
 
 /* ---- activations ------------------------------------------------------------- */
 
-float oracle_act_f32(int act, float x) {
+static inline float act_f32(int act, float x) {
     switch (act) {
     case ORACLE_ACT_NONE: return x;
     case ORACLE_ACT_GELU_TANH: {
@@ -107,7 +111,7 @@ float oracle_act_f32(int act, float x) {
     }
 }
 
-double oracle_act_f64(int act, double x) {
+static inline double act_f64(int act, double x) {
     switch (act) {
     case ORACLE_ACT_NONE: return x;
     case ORACLE_ACT_GELU_TANH: {
@@ -121,16 +125,19 @@ double oracle_act_f64(int act, double x) {
     }
 }
 
+float oracle_act_f32(int act, float x) { return act_f32(act, x); }
+double oracle_act_f64(int act, double x) { return act_f64(act, x); }
+
 void oracle_act_f32_array(int act, const float* x, float* y, int64_t n) {
-    for (int64_t i = 0; i < n; ++i) y[i] = oracle_act_f32(act, x[i]);
+    for (int64_t i = 0; i < n; ++i) y[i] = act_f32(act, x[i]);
 }
 
 void oracle_act_f64_array(int act, const double* x, double* y, int64_t n) {
-    for (int64_t i = 0; i < n; ++i) y[i] = oracle_act_f64(act, x[i]);
+    for (int64_t i = 0; i < n; ++i) y[i] = act_f64(act, x[i]);
 }
 
 void oracle_f32_to_bf16_array(const float* x, uint16_t* y, int64_t n) {
-    for (int64_t i = 0; i < n; ++i) y[i] = oracle_f32_to_bf16(x[i]);
+    for (int64_t i = 0; i < n; ++i) y[i] = f32_to_bf16(x[i]);
 }
 
 void oracle_f64_to_bf16_array(const double* x, uint16_t* y, int64_t n) {
@@ -142,7 +149,7 @@ void oracle_f64_to_bf16_array(const double* x, uint16_t* y, int64_t n) {
 static float dot_f32(const uint16_t* a, const uint16_t* b, int64_t K) {
     float acc = 0.0f;
     for (int64_t k = 0; k < K; ++k) {
-        float p = oracle_bf16_to_f32(a[k]) * oracle_bf16_to_f32(b[k]);
+        float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k]);
         acc = acc + p;
     }
     return acc;
@@ -151,7 +158,7 @@ static float dot_f32(const uint16_t* a, const uint16_t* b, int64_t K) {
 static double dot_f64(const uint16_t* a, const uint16_t* b, int64_t K) {
     double acc = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double p = (double)oracle_bf16_to_f32(a[k]) * (double)oracle_bf16_to_f32(b[k]);
+        double p = (double)bf16_to_f32(a[k]) * (double)bf16_to_f32(b[k]);
         acc = acc + p;
     }
     return acc;
@@ -175,10 +182,10 @@ void oracle_linear_f32(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             float v = dot_f32(A + m * lda, B + n * ldb, K);
-            if (bias) v = v + oracle_bf16_to_f32(bias[n]);
-            v = oracle_act_f32(act, v);
-            if (R) v = v + oracle_bf16_to_f32(R[m * ldr + n]);
-            D[m * ldd + n] = oracle_f32_to_bf16(v);
+            if (bias) v = v + bf16_to_f32(bias[n]);
+            v = act_f32(act, v);
+            if (R) v = v + bf16_to_f32(R[m * ldr + n]);
+            D[m * ldd + n] = f32_to_bf16(v);
         }
     }
 }
@@ -190,9 +197,9 @@ void oracle_linear_f64(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double v = dot_f64(A + m * lda, B + n * ldb, K);
-            if (bias) v = v + (double)oracle_bf16_to_f32(bias[n]);
-            v = oracle_act_f64(act, v);
-            if (R) v = v + (double)oracle_bf16_to_f32(R[m * ldr + n]);
+            if (bias) v = v + (double)bf16_to_f32(bias[n]);
+            v = act_f64(act, v);
+            if (R) v = v + (double)bf16_to_f32(R[m * ldr + n]);
             Y[m * ldy + n] = v;
         }
     }
@@ -208,8 +215,8 @@ void oracle_ffn_f32(const uint16_t* X, int64_t ldx, const uint16_t* W1, int64_t 
         for (int64_t n = 0; n < N; ++n) {
             float a1 = dot_f32(X + m * ldx, W1 + n * ldw1, K);
             float a3 = dot_f32(X + m * ldx, W3 + n * ldw3, K);
-            float v = oracle_act_f32(ORACLE_ACT_SILU, a1) * a3;
-            D[m * ldd + n] = oracle_f32_to_bf16(v);
+            float v = act_f32(ORACLE_ACT_SILU, a1) * a3;
+            D[m * ldd + n] = f32_to_bf16(v);
         }
     }
 }
@@ -222,7 +229,7 @@ void oracle_ffn_f64(const uint16_t* X, int64_t ldx, const uint16_t* W1, int64_t 
         for (int64_t n = 0; n < N; ++n) {
             double a1 = dot_f64(X + m * ldx, W1 + n * ldw1, K);
             double a3 = dot_f64(X + m * ldx, W3 + n * ldw3, K);
-            Y[m * ldy + n] = oracle_act_f64(ORACLE_ACT_SILU, a1) * a3;
+            Y[m * ldy + n] = act_f64(ORACLE_ACT_SILU, a1) * a3;
         }
     }
 }

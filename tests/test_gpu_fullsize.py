@@ -1,0 +1,124 @@
+"""Full-size workloads on the GPU, in the launch configuration the benchmark times,
+checked against the CPU oracle on a seeded sample of 65536 output entries (a
+256 x 256 grid of rows and columns that always includes the first/last row and
+column and tile boundaries), or on every entry when the oracle can afford it.
+
+Workloads (shapes and distributions as in ``dense_bf16_gemm_persistent_gb300.inputs``):
+MLP linear + bias + GELU_tanh 8192x14336x4096; Llama-FFN 8192x14336x4096; the
+ragged residual sweep (36 combos of M, N, K); the 2^32-element A of the 64-bit
+indexing case."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_bf16_gemm_persistent_gb300 as gb
+from dense_bf16_gemm_persistent_gb300 import inputs
+from tests.gpu_util import assert_bitexact, assert_close, bits, ulp_hist
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+FULL_COMPARE_MACS = 2 ** 33
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    gb.set_config(None)
+    yield
+    gb.device_status()
+    torch.cuda.empty_cache()
+
+
+def sample(M, N, seed=1234):
+    return inputs.sample_indices(M, N, seed=seed)
+
+
+def rows_of(t: torch.Tensor, idx: np.ndarray) -> np.ndarray:
+    return bits(t[torch.from_numpy(idx).to(t.device)])
+
+
+def grid_of(t: torch.Tensor, r: np.ndarray, c: np.ndarray) -> np.ndarray:
+    rr = torch.from_numpy(r).to(t.device)
+    cc = torch.from_numpy(c).to(t.device)
+    return bits(t[rr][:, cc])
+
+
+def test_mlp_gelu_8192x14336x4096():
+    w = inputs.mlp_gelu(device=DEV)
+    D = gb.linear(w["A"], w["B"], w["bias"], None, act="gelu_tanh")
+    gb.device_status()
+    r, c = sample(8192, 14336)
+    ref = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c), bits(w["bias"])[c], None, "gelu_tanh")
+    got = grid_of(D, r, c)
+    assert_close(got, ref, "mlp_gelu")
+    ref64 = oracle.linear_f64(rows_of(w["A"], r), rows_of(w["B"], c), bits(w["bias"])[c], None, "gelu_tanh")
+    h = ulp_hist(got, ref64)
+    assert sum(v for k, v in h.items() if k <= 1) >= 0.99 * got.size, h
+
+
+def test_llama_ffn_8192x14336x4096():
+    w = inputs.llama_ffn(device=DEV)
+    D = gb.ffn_gated(w["X"], w["W1"], w["W3"])
+    gb.device_status()
+    r, c = sample(8192, 14336, seed=4321)
+    ref = oracle.ffn_gated(rows_of(w["X"], r), rows_of(w["W1"], c), rows_of(w["W3"], c))
+    assert_close(grid_of(D, r, c), ref, "llama_ffn")
+
+
+@pytest.mark.parametrize("M,N,K", inputs.ragged_combos(), ids=lambda v: str(v))
+def test_ragged_residual(M, N, K):
+    """D = A.B^T + R with every tile edge predicated (M, N not tile multiples)."""
+    w = inputs.ragged(M, N, K, device=DEV)
+    D = gb.linear(w["A"], w["B"], None, w["R"])
+    gb.device_status()
+    if M * N * K <= FULL_COMPARE_MACS:
+        ref = oracle.linear(bits(w["A"]), bits(w["B"]), None, bits(w["R"]))
+        assert_close(bits(D), ref, f"ragged {M}x{N}x{K}")
+    else:
+        r, c = sample(M, N, seed=M + N + K)
+        ref = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c), None, grid_of(w["R"], r, c))
+        assert_close(grid_of(D, r, c), ref, f"ragged {M}x{N}x{K}")
+    if K == 4096:
+        # the product alone (R = 0), and the residual alone (A = 0: D must equal R exactly)
+        Z = torch.zeros_like(w["R"])
+        D0 = gb.linear(w["A"], w["B"], None, Z)
+        gb.device_status()
+        r, c = sample(M, N, seed=7)
+        ref0 = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c))
+        assert_close(grid_of(D0, r, c), ref0, "R=0")
+        DA = gb.linear(torch.zeros_like(w["A"]), w["B"], None, w["R"])
+        gb.device_status()
+        assert torch.equal(DA.view(torch.int16), w["R"].view(torch.int16))
+
+
+def test_int64_indexing_65536x4096x65536():
+    """A has 2^32 elements (8 GiB): rows past 32768 sit beyond byte offset 2^32."""
+    M, N, K = 65536, 4096, 65536
+    w = inputs.int64_case(device=DEV)
+    D = gb.linear(w["A"], w["B"])
+    gb.device_status()
+    r, c = sample(M, N, seed=99)
+    assert (r >= 32768).sum() >= 100
+    ref = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c))
+    assert_close(grid_of(D, r, c), ref, "int64")
+    # an index-revealing pattern: A[i, 0] = (i mod 7) - 3, B[n, 0] = 1, all else 0  ->  D[i, n] = (i mod 7) - 3
+    A = w["A"]
+    A.zero_()
+    A[:, 0] = ((torch.arange(M, device=DEV) % 7) - 3).to(torch.bfloat16)
+    B = w["B"]
+    B.zero_()
+    B[:, 0] = 1
+    D = gb.linear(A, B, out=D)
+    gb.device_status()
+    want = ((torch.arange(M, device=DEV) % 7) - 3).to(torch.bfloat16)[:, None].expand(M, N)
+    assert torch.equal(D.view(torch.int16), want.contiguous().view(torch.int16))
+    del w, A, B, D
+
+
+def test_bench_configuration_is_the_default():
+    """The benchmark times the default plan; the sampled checks above run under it."""
+    w = inputs.mlp_gelu(device=DEV, M=1024, N=2048, K=512)
+    gb.linear(w["A"], w["B"], w["bias"], None, act="gelu_tanh")
+    plan = gb.last_plan()
+    assert "kernel=linear" in plan and "bn=256" in plan and "d_store=tma" in plan

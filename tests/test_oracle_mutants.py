@@ -20,12 +20,12 @@ MUTANTS = [
     ("sum_sign", "acc = acc + p;", "acc = acc - p;", 0),
     ("transposed_operands", "float v = dot_f32(A + m * lda, B + n * ldb, K);", "float v = dot_f32(A + (n % M) * lda, B + (m % N) * ldb, K);", 0),
     ("acc_index", "C[m * ldc + n] = dot_f32(A + m * lda, B + n * ldb, K);", "C[m * ldc + n] = dot_f32(A + m * lda, B + m % N * ldb, K);", 0),
-    ("bias_dropped", "if (bias) v = v + oracle_bf16_to_f32(bias[n]);", "if (0) v = v + oracle_bf16_to_f32(bias[n]);", 0),
-    ("bias_index", "if (bias) v = v + oracle_bf16_to_f32(bias[n]);", "if (bias) v = v + oracle_bf16_to_f32(bias[0]);", 0),
-    ("bias_sign", "if (bias) v = v + oracle_bf16_to_f32(bias[n]);", "if (bias) v = v - oracle_bf16_to_f32(bias[n]);", 0),
-    ("residual_index", "if (R) v = v + oracle_bf16_to_f32(R[m * ldr + n]);", "if (R) v = v + oracle_bf16_to_f32(R[m * ldr]);", 0),
-    ("residual_before_act", "            v = oracle_act_f32(act, v);\n            if (R) v = v + oracle_bf16_to_f32(R[m * ldr + n]);",
-     "            if (R) v = v + oracle_bf16_to_f32(R[m * ldr + n]);\n            v = oracle_act_f32(act, v);", 0),
+    ("bias_dropped", "if (bias) v = v + bf16_to_f32(bias[n]);", "if (0) v = v + bf16_to_f32(bias[n]);", 0),
+    ("bias_index", "if (bias) v = v + bf16_to_f32(bias[n]);", "if (bias) v = v + bf16_to_f32(bias[0]);", 0),
+    ("bias_sign", "if (bias) v = v + bf16_to_f32(bias[n]);", "if (bias) v = v - bf16_to_f32(bias[n]);", 0),
+    ("residual_index", "if (R) v = v + bf16_to_f32(R[m * ldr + n]);", "if (R) v = v + bf16_to_f32(R[m * ldr]);", 0),
+    ("residual_before_act", "            v = act_f32(act, v);\n            if (R) v = v + bf16_to_f32(R[m * ldr + n]);",
+     "            if (R) v = v + bf16_to_f32(R[m * ldr + n]);\n            v = act_f32(act, v);", 0),
     ("gelu_cubic_coeff", "const float a = 0.044715f;", "const float a = 0.04715f;", 0),
     ("gelu_sqrt2pi", "const float c = 0.7978845608028654f;", "const float c = 0.7978845608028654f * 1.01f;", 0),
     ("gelu_half", "return 0.5f * x * (1.0f + tanhf(inner));", "return x * (1.0f + tanhf(inner));", 0),
@@ -34,9 +34,9 @@ MUTANTS = [
     ("round_truncate", "u += 0x7fffu + lsb;", "u += 0u * lsb;", 0),
     ("round_ties_away", "u += 0x7fffu + lsb;", "u += 0x8000u + 0u * lsb;", 0),
     ("f64_round_precision", "int qexp = e - 8;", "int qexp = e - 9;", 0),
-    ("ffn_swap_gate", "float v = oracle_act_f32(ORACLE_ACT_SILU, a1) * a3;", "float v = oracle_act_f32(ORACLE_ACT_SILU, a3) * a1;", 0),
+    ("ffn_swap_gate", "float v = act_f32(ORACLE_ACT_SILU, a1) * a3;", "float v = act_f32(ORACLE_ACT_SILU, a3) * a1;", 0),
     ("ffn_same_weight", "float a3 = dot_f32(X + m * ldx, W3 + n * ldw3, K);", "float a3 = dot_f32(X + m * ldx, W1 + n * ldw1, K);", 0),
-    ("ffn_f64_swap", "Y[m * ldy + n] = oracle_act_f64(ORACLE_ACT_SILU, a1) * a3;", "Y[m * ldy + n] = oracle_act_f64(ORACLE_ACT_SILU, a3) * a1;", 0),
+    ("ffn_f64_swap", "Y[m * ldy + n] = act_f64(ORACLE_ACT_SILU, a1) * a3;", "Y[m * ldy + n] = act_f64(ORACLE_ACT_SILU, a3) * a1;", 0),
     ("f64_dot_drop", "for (int64_t k = 0; k < K; ++k) {\n        double p", "for (int64_t k = 1; k < K; ++k) {\n        double p", 0),
 ]
 
