@@ -291,6 +291,7 @@ def run_ours(args, wl: dict):
     dist = dist_init(world, "nccl")
     import dense_bf16_gemm_persistent_gb300 as gb
     gb.lib()
+    gb.set_config(args.config)
 
     t = make_inputs(wl, device)
     out = torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16, device=device)
@@ -375,6 +376,7 @@ def run_ours(args, wl: dict):
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
     achieved = fl / (avg_launch_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     traffic = recorded_traffic(wl["name"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -384,6 +386,8 @@ def run_ours(args, wl: dict):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                      "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
+                     "frac_of_sustained": achieved / peak_sustained,
+                     "clock_note": "timed after a pre-warm, so under the power cap (see clocks)",
                      "kernel": "gb::gemm_persistent_kernel", "avg_launch_ms": avg_launch_ms,
                      "flops_per_launch": fl},
         "gpu_launches": args.steps,
@@ -411,6 +415,7 @@ def main(argv=None):
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of CPU-oracle work")
     ap.add_argument("--ref-step-s", type=float, default=4.0, help="reference arm: seconds per step")
+    ap.add_argument("--config", default=None, help="tile-configuration override (gb_set_config syntax)")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps >= 1 and --warmup >= 0")

@@ -50,6 +50,12 @@ def lib() -> ctypes.CDLL:
         i64, p, st = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         L.gb_gemm_linear.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64, p]
         L.gb_gemm_ffn_gated.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p]
+        L.gb_gemm_linear_splitk.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64,
+                                             ctypes.c_int, p, ctypes.c_size_t, p]
+        L.gb_gemm_ffn_gated_splitk.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, ctypes.c_int, p,
+                                               ctypes.c_size_t, p]
+        L.gb_splitk_workspace_bytes.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_size_t)]
         L.gb_get_device_status.argtypes = [p]
         L.gb_last_error.argtypes = []
         L.gb_last_error.restype = ctypes.c_char_p
@@ -59,7 +65,8 @@ def lib() -> ctypes.CDLL:
         L.gb_last_plan.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         L.gb_version.argtypes = []
         L.gb_version.restype = ctypes.c_char_p
-        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_get_device_status", "gb_set_config",
+        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_splitk", "gb_gemm_ffn_gated_splitk",
+                     "gb_splitk_workspace_bytes", "gb_get_device_status", "gb_set_config",
                      "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan"):
             getattr(L, name).restype = st
         _lib = L
@@ -91,9 +98,30 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def splitk_workspace_bytes(M: int, N: int, K: int, splits: int = 0, ffn: bool = False) -> int:
+    """Bytes of workspace the split-K call needs on the current device (0: no split)."""
+    n = ctypes.c_size_t(0)
+    _check(lib().gb_splitk_workspace_bytes(1 if ffn else 0, M, N, K, int(splits), ctypes.byref(n)))
+    return int(n.value)
+
+
+def _workspace(split_k, workspace, M, N, K, ffn, device):
+    splits = 0 if split_k == "auto" else int(split_k)
+    need = splitk_workspace_bytes(M, N, K, splits, ffn)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, {need} needed")
+    return splits, workspace
+
+
 def linear(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = None, R: torch.Tensor | None = None,
-           act: str = "none", out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """D = bf16(act(A @ B.T + bias) + R) on the GPU (A [M,K], B [N,K], bias [N], R [M,N])."""
+           act: str = "none", out: torch.Tensor | None = None, stream=None, split_k=None,
+           workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """D = bf16(act(A @ B.T + bias) + R) on the GPU (A [M,K], B [N,K], bias [N], R [M,N]).
+
+    split_k: None (never split), "auto", or a number of K ranges; the fp32 partials
+    go to `workspace` (a CUDA tensor, allocated here when not given)."""
     M, K = A.shape
     N = B.shape[0]
     if act not in ACT:
@@ -107,14 +135,19 @@ def linear(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = None, R
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     pd, ldd = _mat(out, "out", M, N)
-    _check(lib().gb_gemm_linear(pa, lda, pb, ldb, bias.data_ptr() if bias is not None else None, pr, ldr,
-                                ACT[act], pd, ldd, M, N, K, _stream(stream)))
+    pbias = bias.data_ptr() if bias is not None else None
+    if split_k is None:
+        _check(lib().gb_gemm_linear(pa, lda, pb, ldb, pbias, pr, ldr, ACT[act], pd, ldd, M, N, K, _stream(stream)))
+    else:
+        splits, ws = _workspace(split_k, workspace, M, N, K, False, A.device)
+        _check(lib().gb_gemm_linear_splitk(pa, lda, pb, ldb, pbias, pr, ldr, ACT[act], pd, ldd, M, N, K, splits,
+                                           ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
     return out
 
 
 def ffn_gated(X: torch.Tensor, W1: torch.Tensor, W3: torch.Tensor, out: torch.Tensor | None = None,
-              stream=None) -> torch.Tensor:
-    """D = bf16(silu(X @ W1.T) * (X @ W3.T)) on the GPU (X [M,K], W1/W3 [N,K])."""
+              stream=None, split_k=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """D = bf16(silu(X @ W1.T) * (X @ W3.T)) on the GPU (X [M,K], W1/W3 [N,K]); split_k as in linear()."""
     M, K = X.shape
     N = W1.shape[0]
     px, ldx = _mat(X, "X", M, K)
@@ -123,7 +156,12 @@ def ffn_gated(X: torch.Tensor, W1: torch.Tensor, W3: torch.Tensor, out: torch.Te
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     pd, ldd = _mat(out, "out", M, N)
-    _check(lib().gb_gemm_ffn_gated(px, ldx, p1, ld1, p3, ld3, pd, ldd, M, N, K, _stream(stream)))
+    if split_k is None:
+        _check(lib().gb_gemm_ffn_gated(px, ldx, p1, ld1, p3, ld3, pd, ldd, M, N, K, _stream(stream)))
+    else:
+        splits, ws = _workspace(split_k, workspace, M, N, K, True, X.device)
+        _check(lib().gb_gemm_ffn_gated_splitk(px, ldx, p1, ld1, p3, ld3, pd, ldd, M, N, K, splits, ws.data_ptr(),
+                                              ws.numel() * ws.element_size(), _stream(stream)))
     return out
 
 

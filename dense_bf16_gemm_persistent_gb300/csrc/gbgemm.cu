@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <list>
 #include <mutex>
 #include <string>
@@ -49,6 +50,7 @@ struct Config {
     int persistent = 1;  // 0 = one tile per CTA
     int group = 0;       // 0 = heuristic
     int zigzag = -1;     // -1 = heuristic
+    int pair = -1;       // -1 = heuristic, 0 = single CTAs, 1 = CTA pairs
 };
 
 std::mutex g_cfg_mu;
@@ -171,28 +173,76 @@ gb_status_t make_tmap(CUtensorMap* out, const void* base, uint64_t inner, uint64
 
 // ---------------------------------------------------------------- kernels and launch
 
-template <int BN, int NUM_B, int STAGES>
-gb_status_t launch(const GemmParams& p, int grid, int dev, const DeviceInfo& info, cudaStream_t stream) {
-    using S = gb::KernelShape<BN, NUM_B, STAGES>;
-    auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES>;
-    static bool attr_set[64] = {};
-    static std::mutex mu;
-    if (S::kSmemBytes > info.smem_optin)
-        return fail(GB_ERR_UNSUPPORTED, "kernel needs %u bytes of shared memory, device allows %zu", S::kSmemBytes,
-                    info.smem_optin);
-    {
+// One kernel variant: its launch attributes are set once per device, and for CTA
+// pairs the number of co-resident clusters is queried once per device.
+template <int BN, int NUM_B, int STAGES, bool PAIR>
+struct Variant {
+    using S = gb::KernelShape<BN, NUM_B, STAGES, PAIR>;
+    static constexpr int kStages = STAGES;
+    static constexpr bool kPair = PAIR;
+    static constexpr int kTileM = S::kTileM;
+
+    static gb_status_t prepare(int dev, const DeviceInfo& info, int* max_units) {
+        static std::mutex mu;
+        static bool ready[64] = {};
+        static int units[64] = {};
+        auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR>;
+        if (S::kSmemBytes > info.smem_optin)
+            return fail(GB_ERR_UNSUPPORTED, "kernel needs %u bytes of shared memory, device allows %zu",
+                        S::kSmemBytes, info.smem_optin);
         std::lock_guard<std::mutex> lk(mu);
-        if (!attr_set[dev]) {
+        if (!ready[dev]) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-            attr_set[dev] = true;
+            if (PAIR) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(2 * (info.sms / 2), 1, 1);
+                cfg.blockDim = dim3(gb::kThreads, 1, 1);
+                cfg.dynamicSmemBytes = S::kSmemBytes;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+                if (n < 1) return fail(GB_ERR_UNSUPPORTED, "no CTA pair fits on this device");
+                units[dev] = n;
+            } else {
+                units[dev] = info.sms;
+            }
+            ready[dev] = true;
         }
+        *max_units = units[dev];
+        return GB_OK;
     }
-    kern<<<grid, gb::kThreads, S::kSmemBytes, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-    return GB_OK;
-}
+
+    static gb_status_t launch(const GemmParams& p, int units, cudaStream_t stream) {
+        auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR>;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(units * S::kCG, 1, 1);
+        cfg.blockDim = dim3(gb::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = S::kSmemBytes;
+        cfg.stream = stream;
+        if (PAIR) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx");
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        return GB_OK;
+    }
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
@@ -250,41 +300,80 @@ gb_status_t validate(const Problem& pr) {
     return GB_OK;
 }
 
-gb_status_t run(const Problem& pr, void* stream_ptr) {
-    gb_status_t st = validate(pr);
-    if (st != GB_OK) return st;
-    if (pr.m == 0 || pr.n == 0) {
-        t_plan = "empty (no launch)";
-        return GB_OK;
-    }
-    int dev = 0;
-    DeviceInfo info;
-    if ((st = device_info(&dev, &info)) != GB_OK) return st;
-    uint64_t timeout_ns;
-    int inject;
-    const Config cfg = current_config(&timeout_ns, &inject);
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+struct SplitReq {
+    bool allowed = false;    // the caller supplied a workspace (or asked for its size)
+    int splits = 1;          // <= 0: choose automatically
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    bool query_only = false;  // compute the workspace size, launch nothing
+    size_t* ws_needed = nullptr;
+};
 
-    // Tile width: the FFN kernel holds two 128-column accumulators per buffer;
-    // the linear kernel uses 256 columns unless N fits in 128.
-    int bn = pr.ffn ? 128 : (cfg.bn ? cfg.bn : (pr.n <= 128 ? 128 : 256));
-    if (pr.ffn && cfg.bn && cfg.bn != 128) return fail(GB_ERR_UNSUPPORTED, "the FFN kernel supports bn=128 only");
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <class V>
+gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int dev, const DeviceInfo& info,
+                            uint64_t timeout_ns, int inject, cudaStream_t stream, const SplitReq& sr) {
+    gb_status_t st;
+    int max_units = 0;
+    if ((st = V::prepare(dev, info, &max_units)) != GB_OK) return st;
 
     GemmParams prm;
     memset(&prm, 0, sizeof prm);
     prm.m = static_cast<int32_t>(pr.m);
     prm.n = static_cast<int32_t>(pr.n);
     prm.k = static_cast<int32_t>(pr.k);
-    prm.num_m_blocks = static_cast<int32_t>(cdiv(pr.m, gb::kBM));
+    prm.num_m_blocks = static_cast<int32_t>(cdiv(pr.m, V::kTileM));
     prm.num_n_blocks = static_cast<int32_t>(cdiv(pr.n, bn));
     prm.num_k_blocks = static_cast<int32_t>(cdiv(pr.k, gb::kBK));
     const int64_t tiles = static_cast<int64_t>(prm.num_m_blocks) * prm.num_n_blocks;
     if (tiles > kMaxDim) return fail(GB_ERR_UNSUPPORTED, "too many tiles");
     prm.num_tiles = static_cast<int32_t>(tiles);
-    int group = cfg.group ? cfg.group : 16;
+
+    // Split-K: only with a workspace.  Auto: when the tiles would leave more than
+    // half of the scheduling units idle, cut K so that tiles x splits fills them,
+    // keeping at least 4 k-blocks per split.
+    int splits = 1;
+    if (sr.allowed && prm.num_k_blocks > 1) {
+        if (sr.splits > 0) {
+            splits = sr.splits;
+        } else if (prm.num_k_blocks >= 8 && 2 * tiles <= max_units) {
+            splits = static_cast<int>(std::min<int64_t>(max_units / tiles, prm.num_k_blocks / 4));
+        }
+        splits = std::max(1, std::min(splits, prm.num_k_blocks));
+    }
+    prm.kb_per_split = static_cast<int32_t>(cdiv(prm.num_k_blocks, splits));
+    if (prm.kb_per_split > 0) splits = static_cast<int>(cdiv(prm.num_k_blocks, prm.kb_per_split));
+    prm.splits = splits;
+    const int64_t work = tiles * splits;
+    if (work > kMaxDim) return fail(GB_ERR_UNSUPPORTED, "too many work items");
+
+    const int num_b = pr.ffn ? 2 : 1;
+    const size_t cnt_bytes = splits > 1 ? align_up(static_cast<size_t>(tiles) * 4 * (V::kPair ? 2 : 1) * 4, kWsAlign) : 0;
+    const size_t part_bytes =
+        splits > 1 ? static_cast<size_t>(work) * num_b * V::kTileM * static_cast<size_t>(bn) * sizeof(float) : 0;
+    const size_t ws_needed = cnt_bytes + part_bytes;
+    if (sr.query_only) {
+        *sr.ws_needed = ws_needed;
+        return GB_OK;
+    }
+    if (ws_needed > 0) {
+        if (!sr.ws) return fail(GB_ERR_INVALID_ARG, "split-K needs a workspace of %zu bytes", ws_needed);
+        if (sr.ws_bytes < ws_needed)
+            return fail(GB_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", sr.ws_bytes,
+                        ws_needed);
+        if (reinterpret_cast<uintptr_t>(sr.ws) % kWsAlign)
+            return fail(GB_ERR_INVALID_ARG, "workspace must be %zu-byte aligned", kWsAlign);
+        prm.ws_cnt = static_cast<uint32_t*>(sr.ws);
+        prm.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(sr.ws) + cnt_bytes);
+    }
+
+    int group = cfg.group ? cfg.group : (V::kPair ? 8 : 16);
     if (group > prm.num_m_blocks) group = prm.num_m_blocks;
     prm.group_m = group < 1 ? 1 : group;
-    prm.zigzag = cfg.zigzag >= 0 ? cfg.zigzag : (prm.num_k_blocks >= 256 ? 1 : 0);
+    prm.zigzag = cfg.zigzag >= 0 ? cfg.zigzag : (prm.kb_per_split >= 256 ? 1 : 0);
     prm.act = pr.ffn ? GB_ACT_NONE : pr.act;
     prm.bias = static_cast<const uint16_t*>(pr.bias);
     prm.r = static_cast<const uint16_t*>(pr.r);
@@ -300,39 +389,84 @@ gb_status_t run(const Problem& pr, void* stream_ptr) {
     if (d_tma) flags |= gb::kFlagDTma;
     prm.flags = flags;
 
+    const uint32_t b_rows = static_cast<uint32_t>(bn / (V::kPair ? 2 : 1));
     if (pr.k > 0) {
         if ((st = make_tmap(&prm.tm_a, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             GB_OK)
             return st;
-        if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.k, pr.n, pr.ldb0 * 2, gb::kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-            GB_OK)
+        if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.k, pr.n, pr.ldb0 * 2, gb::kBK, b_rows,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
             return st;
-        if (pr.ffn &&
-            (st = make_tmap(&prm.tm_b1, pr.b1, pr.k, pr.n, pr.ldb1 * 2, gb::kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-                GB_OK)
+        if (pr.ffn && (st = make_tmap(&prm.tm_b1, pr.b1, pr.k, pr.n, pr.ldb1 * 2, gb::kBK, b_rows,
+                                      CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
             return st;
     }
     if (d_tma &&
         (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
         return st;
 
-    int grid = cfg.persistent ? info.sms : prm.num_tiles;
-    if (cfg.grid > 0 && cfg.grid < grid) grid = cfg.grid;
-    if (grid > prm.num_tiles) grid = prm.num_tiles;
+    // Scheduling units: CTAs, or CTA pairs.  Persistent: at most one per SM (pair
+    // of SMs); one work item per unit otherwise.
+    int64_t units = cfg.persistent ? max_units : work;
+    if (cfg.grid > 0) {
+        const int64_t cap = V::kPair ? (cfg.grid + 1) / 2 : cfg.grid;
+        if (cap < units) units = cap;
+    }
+    if (units > work) units = work;
+    if (units < 1) units = 1;
 
-    char plan[256];
+    char plan[360];
     snprintf(plan, sizeof plan,
-             "kernel=%s bm=%d bn=%d bk=%d stages=%d grid=%d tiles=%d k_blocks=%d group=%d zigzag=%d d_store=%s "
-             "r_load=%s",
-             pr.ffn ? "ffn_gated" : "linear", gb::kBM, bn, gb::kBK, (pr.ffn || bn == 256) ? 4 : 6, grid, prm.num_tiles, prm.num_k_blocks,
+             "kernel=%s pair=%d tile=%dx%dx%d stages=%d grid=%lld tiles=%d k_blocks=%d splits=%d group=%d zigzag=%d "
+             "d_store=%s r_load=%s",
+             pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kTileM, bn, gb::kBK, V::kStages,
+             static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, d_tma ? "tma" : "st.global",
              pr.r ? ((flags & gb::kFlagRVec) ? "ld.v4" : "ld.b16") : "none");
     t_plan = plan;
+    if (cnt_bytes) {
+        cudaError_t e = cudaMemsetAsync(prm.ws_cnt, 0, cnt_bytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(split-K counters)");
+    }
+    return V::launch(prm, static_cast<int>(units), stream);
+}
 
-    if (pr.ffn) return launch<128, 2, 4>(prm, grid, dev, info, stream);
-    if (bn == 256) return launch<256, 1, 4>(prm, grid, dev, info, stream);
-    if (bn == 128) return launch<128, 1, 6>(prm, grid, dev, info, stream);
-    return fail(GB_ERR_UNSUPPORTED, "unsupported tile width bn=%d (128 or 256)", bn);
+gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitReq()) {
+    gb_status_t st = validate(pr);
+    if (st != GB_OK) return st;
+    if (pr.m == 0 || pr.n == 0) {
+        t_plan = "empty (no launch)";
+        if (sr.query_only) *sr.ws_needed = 0;
+        return GB_OK;
+    }
+    int dev = 0;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != GB_OK) return st;
+    uint64_t timeout_ns;
+    int inject;
+    const Config cfg = current_config(&timeout_ns, &inject);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    // Tile width: the FFN kernel holds two 128-column accumulators per buffer;
+    // the linear kernel uses 256 columns unless N fits in 128.  CTA pairs
+    // (256-row tiles) unless M fits in one 128-row tile.
+    const int bn = pr.ffn ? 128 : (cfg.bn ? cfg.bn : (pr.n <= 128 ? 128 : 256));
+    if (pr.ffn && cfg.bn && cfg.bn != 128) return fail(GB_ERR_UNSUPPORTED, "the FFN kernel supports bn=128 only");
+    bool pair = cfg.pair >= 0 ? cfg.pair == 1 : pr.m > gb::kBM;
+    if (!pr.ffn && bn == 128) pair = false;  // the 128-wide linear tile runs on single CTAs
+
+    using LinPair = Variant<256, 1, 6, true>;
+    using LinSingle = Variant<256, 1, 4, false>;
+    using LinNarrow = Variant<128, 1, 6, false>;
+    using FfnPair = Variant<128, 2, 6, true>;
+    using FfnSingle = Variant<128, 2, 4, false>;
+    if (pr.ffn)
+        return pair ? plan_and_launch<FfnPair>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr)
+                    : plan_and_launch<FfnSingle>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
+    if (bn == 256)
+        return pair ? plan_and_launch<LinPair>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr)
+                    : plan_and_launch<LinSingle>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
+    return plan_and_launch<LinNarrow>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
 }
 
 bool parse_int(const char* s, size_t n, long* out) {
@@ -360,6 +494,50 @@ gb_status_t gb_gemm_ffn_gated(const void* X, int64_t ldx, const void* W1, int64_
     t_error.clear();
     Problem pr{X, ldx, W1, ldw1, W3, ldw3, nullptr, nullptr, 0, GB_ACT_NONE, D, ldd, M, N, K, true};
     return run(pr, stream);
+}
+
+gb_status_t gb_gemm_linear_splitk(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                                  const void* R, int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N,
+                                  int64_t K, int splits, void* workspace, size_t workspace_bytes, void* stream) {
+    t_error.clear();
+    Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false};
+    SplitReq sr;
+    sr.allowed = true;
+    sr.splits = splits;
+    sr.ws = workspace;
+    sr.ws_bytes = workspace_bytes;
+    return run(pr, stream, sr);
+}
+
+gb_status_t gb_gemm_ffn_gated_splitk(const void* X, int64_t ldx, const void* W1, int64_t ldw1, const void* W3,
+                                     int64_t ldw3, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int splits,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    t_error.clear();
+    Problem pr{X, ldx, W1, ldw1, W3, ldw3, nullptr, nullptr, 0, GB_ACT_NONE, D, ldd, M, N, K, true};
+    SplitReq sr;
+    sr.allowed = true;
+    sr.splits = splits;
+    sr.ws = workspace;
+    sr.ws_bytes = workspace_bytes;
+    return run(pr, stream, sr);
+}
+
+gb_status_t gb_splitk_workspace_bytes(int ffn, int64_t M, int64_t N, int64_t K, int splits, size_t* bytes) {
+    t_error.clear();
+    if (!bytes) return fail(GB_ERR_INVALID_ARG, "bytes is null");
+    if (M < 0 || N < 0 || K < 0) return fail(GB_ERR_INVALID_ARG, "negative size");
+    // Sizes only: fake, never-dereferenced operand addresses that pass validation.
+    static const uint16_t dummy[8] __attribute__((aligned(16))) = {};
+    const int64_t kk = K > 0 ? ((K + 7) / 8) * 8 : 0;
+    Problem pr{dummy, kk, dummy, kk, ffn ? dummy : nullptr, kk, nullptr, nullptr, 0, GB_ACT_NONE,
+               const_cast<uint16_t*>(dummy), N, M, N, K, ffn != 0};
+    SplitReq sr;
+    sr.allowed = true;
+    sr.splits = splits;
+    sr.query_only = true;
+    sr.ws_needed = bytes;
+    *bytes = 0;
+    return run(pr, nullptr, sr);
 }
 
 gb_status_t gb_get_device_status(void* stream) {
@@ -399,6 +577,7 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "persistent" && (v == 0 || v == 1)) c.persistent = static_cast<int>(v);
             else if (key == "group" && v >= 1 && v <= 1000000) c.group = static_cast<int>(v);
             else if (key == "zigzag" && v >= -1 && v <= 1) c.zigzag = static_cast<int>(v);
+            else if (key == "pair" && v >= -1 && v <= 1) c.pair = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

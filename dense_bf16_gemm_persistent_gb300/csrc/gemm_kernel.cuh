@@ -80,6 +80,15 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     uint32_t flags;
     uint64_t timeout_ns;
     int32_t inject;
+    // split-K: each tile's k-blocks are cut into `splits` ranges of `kb_per_split`;
+    // work item w = tile * splits + split.  With splits > 1 every epilogue warp
+    // writes its fp32 partial slab to `ws` and the last of the splits (counted in
+    // `ws_cnt`, one counter per 32-row slab, zero on entry) reduces them in split
+    // order and runs the epilogue.
+    int32_t splits;
+    int32_t kb_per_split;
+    float* ws;
+    uint32_t* ws_cnt;
 };
 
 struct SharedCtl {
@@ -196,27 +205,119 @@ __device__ __forceinline__ void add_bf16_row(float (&v)[32], const uint16_t* src
     }
 }
 
+// Bias, activation and epilogue input (linear), bf16 rounding, and the store of
+// one 32-column chunk of row m (this lane) of the warp's 32-row slab at row0.
+template <int NUM_B>
+__device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32], int32_t m, int32_t row0,
+                                             int32_t n0, int lane, int q, uint8_t* dstage, uint32_t& dcount) {
+    const int valid = min(32, p.n - n0);
+    if (NUM_B == 1) {
+        if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, valid, p.flags & kFlagBiasVec);
+        switch (p.act) {
+            case 1:
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                break;
+            case 2:
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                break;
+            case 3:
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                break;
+            default:
+                break;
+        }
+        if ((p.flags & kFlagResidual) && m < p.m)
+            add_bf16_row(v, p.r + static_cast<int64_t>(m) * p.ldr + n0, valid, p.flags & kFlagRVec);
+    }
+
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+
+    if (p.flags & kFlagDTma) {
+        uint8_t* buf = dstage + (q * 2 + (dcount & 1u)) * kDStageBytes;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+        __syncwarp();
+        // 64-byte rows, 16-byte units XOR-swizzled with (row / 2) % 4 (TMA 64B swizzle).
+        const uint32_t row_addr = smem_addr(buf) + lane * 64;
+        const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
+                         packed[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&p.tm_d, smem_addr(buf), n0, row0);
+            bulk_commit_group();
+        }
+        ++dcount;
+    } else if (m < p.m) {
+        uint16_t* dst = p.d + static_cast<int64_t>(m) * p.ldd + n0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < valid)
+                dst[j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16) : (packed[j >> 1] & 0xffffu));
+        }
+    }
+}
+
+__device__ __forceinline__ void st_global_f32x32(float* dst, const uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i), "r"(r[4 * i]), "r"(r[4 * i + 1]),
+                     "r"(r[4 * i + 2]), "r"(r[4 * i + 3])
+                     : "memory");
+}
+
+// v += 32 floats at src (bypassing L1: written by other CTAs of this launch).
+__device__ __forceinline__ void add_f32x32_cg(float (&v)[32], const float* src) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(src) + i);
+        v[4 * i] += x.x;
+        v[4 * i + 1] += x.y;
+        v[4 * i + 2] += x.z;
+        v[4 * i + 3] += x.w;
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 
-template <int BN, int NUM_B, int STAGES>
+// Compile-time shape of one kernel variant.
+//   BN    : MMA N, i.e. tile width per B operand (the pair's width when PAIR)
+//   NUM_B : 1 (linear) or 2 (FFN: W1 and W3 share the A tile)
+//   PAIR  : CTA pair with cta_group::2 (tile 256 x BN, each CTA holds 128 rows
+//           of A and BN/2 rows of each B operand) or a single CTA (128 x BN)
+template <int BN, int NUM_B, int STAGES, bool PAIR>
 struct KernelShape {
+    static constexpr int kCG = PAIR ? 2 : 1;
+    static constexpr int kTileM = kBM * kCG;
+    static constexpr int kBRows = BN / kCG;  // rows of each B operand this CTA loads
     static constexpr uint32_t kABytes = kBM * kBK * 2;
-    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + NUM_B * kBBytes;
+    static constexpr uint32_t kTxBytes = kCG * kStageBytes;  // bytes the leader's full barrier waits for
     static constexpr uint32_t kRingBytes = STAGES * kStageBytes;
     static constexpr uint32_t kDStageTotal = 4 * 2 * kDStageBytes;
     static constexpr uint32_t kBarBytes = 2 * STAGES * 8;
     static constexpr uint32_t kSmemBytes =
         1024 /* alignment slack */ + kRingBytes + kDStageTotal + kBarBytes + sizeof(SharedCtl);
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
+    static constexpr uint32_t kAccEmptyArrivals = 4 * kCG;  // epilogue warps of every CTA in the pair
     static_assert(NUM_B * BN <= kAccStride, "accumulator buffer holds at most 256 columns");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    static_assert(kBRows % 8 == 0 && kBRows <= 256, "B box rows");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-template <int BN, int NUM_B, int STAGES>
+template <int BN, int NUM_B, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p) {
-    using S = KernelShape<BN, NUM_B, STAGES>;
+    using S = KernelShape<BN, NUM_B, STAGES, PAIR>;
+    constexpr int CG = S::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
@@ -228,6 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t tmo = p.timeout_ns;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // position in the CTA pair
+    const bool leader = rank == 0;
+    const int32_t unit = PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
+    const int32_t units = PAIR ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
+    const int32_t num_work = p.num_tiles * p.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -236,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&ctl->acc_full[b]), 1);
-            mbar_init(smem_addr(&ctl->acc_empty[b]), 4);
+            mbar_init(smem_addr(&ctl->acc_empty[b]), S::kAccEmptyArrivals);
         }
         mbar_init(smem_addr(&ctl->drain), 1);
         ctl->abort = 0;
@@ -251,46 +357,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
         if (p.flags & kFlagDTma) tma_prefetch_desc(&p.tm_d);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish<CG>();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int32_t* abort_flag = &ctl->abort;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer (every CTA)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             int32_t local = 0;
-            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+            for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
+                const int32_t tile = w / p.splits;
+                const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
+                const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
                 int32_t mb, nb;
                 tile_coords(tile, p, mb, nb);
                 const bool reverse = p.zigzag && (local & 1);
-                for (int32_t kk = 0; kk < p.num_k_blocks; ++kk, ++it) {
-                    const int32_t kb = reverse ? p.num_k_blocks - 1 - kk : kk;
+                const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
+                const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
+                for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
+                    const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, tmo, kRoleProducer, s)) {
                         ok = false;
                         break;
                     }
-                    if (p.inject == kInjectSkipFirstStage && it == 0) continue;  // test hook: never arrives
+                    if (p.inject == kInjectSkipFirstStage && it == 0 && leader) continue;  // test hook
                     uint8_t* st = ring + s * S::kStageBytes;
-                    const uint32_t fb = smem_addr(&full[s]);
-                    mbar_arrive_expect_tx(fb, S::kStageBytes);
-                    tma_load_2d(smem_addr(st), &p.tm_a, fb, kb * kBK, mb * kBM);
-                    tma_load_2d(smem_addr(st + S::kABytes), &p.tm_b0, fb, kb * kBK, nb * BN);
-                    if (NUM_B == 2)
-                        tma_load_2d(smem_addr(st + S::kABytes + S::kBBytes), &p.tm_b1, fb, kb * kBK, nb * BN);
+                    const uint32_t own_full = smem_addr(&full[s]);
+                    if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
+                    if constexpr (PAIR) {
+                        const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
+                        tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);
+                        tma_load_2d_pair(smem_addr(st + S::kABytes), &p.tm_b0, fb, kb * kBK, b_row);
+                        if (NUM_B == 2)
+                            tma_load_2d_pair(smem_addr(st + S::kABytes + S::kBBytes), &p.tm_b1, fb, kb * kBK, b_row);
+                    } else {
+                        tma_load_2d(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row);
+                        tma_load_2d(smem_addr(st + S::kABytes), &p.tm_b0, own_full, kb * kBK, b_row);
+                        if (NUM_B == 2)
+                            tma_load_2d(smem_addr(st + S::kABytes + S::kBBytes), &p.tm_b1, own_full, kb * kBK, b_row);
+                    }
                 }
             }
-            if (!ok) {
-                // Drain: the loads issued in the last STAGES k-blocks before the stop may
-                // still be in flight; wait (bounded) for each to land.
+            if (!ok && leader) {
+                // Drain: the leader's full barriers count the bytes of both CTAs; wait
+                // (bounded) for the loads of the last STAGES k-blocks to land.
                 const uint32_t first = it > STAGES ? it - STAGES : 0u;
                 for (uint32_t i = first; i < it; ++i) {
                     if (p.inject == kInjectSkipFirstStage && i == 0) continue;
@@ -300,13 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
             uint32_t it = 0;
             bool ok = true;
             bool issued = false;
             int32_t local = 0;
-            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+            for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
+                const int32_t tile = w / p.splits;
+                const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
+                const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
                 const uint32_t b = local & 1;
                 const uint32_t aph = (local >> 1) & 1u;
                 if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, tmo, kRoleMma, 0x100u | b)) {
@@ -315,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int32_t kk = 0; kk < p.num_k_blocks; ++kk, ++it) {
+                for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s)) {
@@ -330,32 +452,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                     for (int j = 0; j < kBK / 16; ++j) {
                         // +32 bytes along K per 16-element slice: +2 in the >>4-encoded address
                         const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
-                        mma_bf16(d_tmem, adesc + 2 * j, bdesc + 2 * j, S::kIdesc, acc);
+                        mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, S::kIdesc, acc);
                         if (NUM_B == 2) {
                             const uint64_t b1desc = sdesc_kmajor_sw128(a_addr + S::kABytes + S::kBBytes);
-                            mma_bf16(d_tmem + BN, adesc + 2 * j, b1desc + 2 * j, S::kIdesc, acc);
+                            mma_bf16<CG>(d_tmem + BN, adesc + 2 * j, b1desc + 2 * j, S::kIdesc, acc);
                         }
                     }
                     issued = true;
-                    mma_commit(smem_addr(&empty[s]));
+                    if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
+                    else mma_commit<1>(smem_addr(&empty[s]));
                 }
                 if (!ok) break;
-                mma_commit(smem_addr(&ctl->acc_full[b]));
+                if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), 0x3);
+                else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
             }
             if (!ok && issued) {
                 // Drain: every MMA issued so far must finish before TMEM is freed.
-                mma_commit(smem_addr(&ctl->drain));
+                mma_commit<CG>(smem_addr(&ctl->drain));
                 drain_bar(smem_addr(&ctl->drain), 0, tmo);
             }
         }
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------ epilogue (every CTA)
         const int q = warp - kEpiWarp0;  // == warp % 4: this warp's TMEM lane quadrant
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const int32_t slab_row = static_cast<int32_t>(rank) * kBM + q * 32 + lane;  // row within the tile
+        constexpr int64_t kPartFloats = static_cast<int64_t>(S::kTileM) * BN;       // one partial accumulator
         uint32_t dcount = 0;
         int32_t local = 0;
-        for (int32_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+        for (int32_t w = unit; w < num_work; w += units, ++local) {
             const uint32_t b = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
             bool ok = true;
@@ -365,12 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             if (!ok) break;
             tc_fence_after_sync();
 
+            const int32_t tile = w / p.splits;
             int32_t mb, nb;
             tile_coords(tile, p, mb, nb);
-            const int32_t row0 = mb * kBM + q * 32;      // first row of this warp's slab
+            const int32_t row0 = mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;  // this warp's slab
             const int32_t m = row0 + lane;
             const bool warp_rows = row0 < p.m;
             const uint32_t tcol = tmem_base + lane_base + b * kAccStride;
+            const bool split_mode = p.splits > 1;
+            float* part = p.ws + static_cast<int64_t>(w) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
 
 #pragma unroll 1
             for (int c = 0; c < BN / kDChunk; ++c) {
@@ -384,89 +513,89 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         uint32_t r1[32];
                         tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
                         tmem_wait_ld();
+                        if (split_mode) {
+                            st_global_f32x32(part + c * kDChunk, r0);
+                            st_global_f32x32(part + kPartFloats + c * kDChunk, r1);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                            for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                        }
                     } else {
                         tmem_wait_ld();
+                        if (split_mode) {
+                            st_global_f32x32(part + c * kDChunk, r0);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                        }
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
                 if (c == BN / kDChunk - 1) {
-                    // All TMEM reads of this buffer are done: hand it back to the MMA warp.
+                    // All TMEM reads of this buffer are done: hand it back to the MMA issuer.
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(&ctl->acc_empty[b]));
-                }
-                if (!chunk_on) continue;
-
-                const int valid = min(32, p.n - n0);
-                if (NUM_B == 1) {
-                    if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, valid, p.flags & kFlagBiasVec);
-                    switch (p.act) {
-                        case 1:
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
-                            break;
-                        case 2:
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
-                            break;
-                        case 3:
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
-                            break;
-                        default:
-                            break;
-                    }
-                    if ((p.flags & kFlagResidual) && m < p.m)
-                        add_bf16_row(v, p.r + static_cast<int64_t>(m) * p.ldr + n0, valid, p.flags & kFlagRVec);
-                }
-
-                uint32_t packed[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-
-                if (p.flags & kFlagDTma) {
-                    uint8_t* buf = dstage + (q * 2 + (dcount & 1u)) * kDStageBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
-                    __syncwarp();
-                    // 64-byte rows, 16-byte units XOR-swizzled with (row / 2) % 4 (TMA 64B swizzle).
-                    const uint32_t row_addr = smem_addr(buf) + lane * 64;
-                    const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
-                                     packed[4 * u + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tm_d, smem_addr(buf), n0, row0);
-                        bulk_commit_group();
-                    }
-                    ++dcount;
-                } else if (m < p.m) {
-                    uint16_t* dst = p.d + static_cast<int64_t>(m) * p.ldd + n0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (j < valid) dst[j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16) : (packed[j >> 1] & 0xffffu));
+                        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), 0));
+                        else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                     }
                 }
+                if (!chunk_on || split_mode) continue;
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, q, dstage, dcount);
             }
+            if (!split_mode || !warp_rows) continue;
+
+            // split-K: publish this partial; the last split of this slab reduces all of them.
+            __threadfence();
+            __syncwarp();
+            uint32_t* cnt = p.ws_cnt + tile * (4 * S::kCG) + static_cast<int32_t>(rank) * 4 + q;
+            uint32_t arrived = 0;
+            if (lane == 0) arrived = atomicAdd(cnt, 1u);
+            arrived = __shfl_sync(0xffffffffu, arrived, 0);
+            if (arrived != static_cast<uint32_t>(p.splits - 1)) continue;
+            __threadfence();
+            const float* base = p.ws + static_cast<int64_t>(tile) * p.splits * NUM_B * kPartFloats +
+                                static_cast<int64_t>(slab_row) * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / kDChunk; ++c) {
+                const int32_t n0 = nb * BN + c * kDChunk;
+                if (n0 >= p.n) break;
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                if (NUM_B == 2) {
+                    float v3[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v3[j] = 0.0f;
+                    for (int32_t sp = 0; sp < p.splits; ++sp) {
+                        const float* src = base + static_cast<int64_t>(sp) * NUM_B * kPartFloats + c * kDChunk;
+                        add_f32x32_cg(v, src);
+                        add_f32x32_cg(v3, src + kPartFloats);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = silu(v[j]) * v3[j];
+                } else {
+                    for (int32_t sp = 0; sp < p.splits; ++sp)
+                        add_f32x32_cg(v, base + static_cast<int64_t>(sp) * kPartFloats + c * kDChunk);
+                }
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, q, dstage, dcount);
+            }
+            if (lane == 0) atomicExch(cnt, 0u);  // ready for the next launch
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
     }
 
     // ---------------------------------------------------------------- teardown
+    // (for a pair, the cluster barrier also keeps each CTA's shared memory alive
+    // until the peer has stopped signalling its barriers)
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc<CG>(tmem_base, kTmemCols);
     }
 }
 

@@ -112,6 +112,49 @@ GB_API gb_status_t gb_gemm_ffn_gated(const void* X, int64_t ldx, const void* W1,
                               int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * Split-K variants, for problems with too few output tiles to fill the GPU
+ * (the skinny shapes: M or N of one tile, long K).  Split-K and stream-K are the
+ * two schedules "Implement persistent matmul scheduling" (NVIDIA/Fuser PR #3812,
+ * reviewer guide) records as unsupported by its persistent Hopper scheduler.
+ *
+ * The k-blocks of every output tile are cut into `splits` contiguous ranges;
+ * each (tile, range) is one work item of the persistent kernel.  Every range
+ * writes its fp32 partial accumulator to the workspace; the last range to
+ * finish a 32-row slab of a tile (a per-slab counter in the workspace) sums
+ * the partials in range order -- so the result is deterministic -- and applies
+ * the same epilogue as the non-split call.  Results equal a sequential fp32
+ * sum up to rounding, like every other call.
+ *   splits     <= 0: chosen automatically (1 when the tiles already fill the
+ *              GPU); otherwise clamped to [1, number of 64-wide k-blocks].
+ *   workspace  device memory owned by the caller, 256-byte aligned, at least
+ *              gb_splitk_workspace_bytes() bytes (may be NULL when that is 0).
+ *              Its counters are cleared on `stream` by each call, so calls that
+ *              share one workspace must be ordered on the GPU (same stream or
+ *              events); overlapping calls on one workspace race.
+ * Other arguments, errors and limits as gb_gemm_linear / gb_gemm_ffn_gated.
+ * GB_ERR_INVALID_ARG if the workspace is missing, too small or misaligned.
+ */
+GB_API gb_status_t gb_gemm_linear_splitk(const void* A, int64_t lda, const void* B, int64_t ldb,
+                                         const void* bias, const void* R, int64_t ldr, int act,
+                                         void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                                         int splits, void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
+GB_API gb_status_t gb_gemm_ffn_gated_splitk(const void* X, int64_t ldx, const void* W1, int64_t ldw1,
+                                            const void* W3, int64_t ldw3, void* D, int64_t ldd,
+                                            int64_t M, int64_t N, int64_t K, int splits,
+                                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes the split-K call needs for this problem on the current
+ * device under the current configuration (ffn: 0 = linear, 1 = FFN fusion;
+ * splits as above).  Writes 0 when the plan does not split.  Needs a CUDA
+ * device (the plan depends on the SM count); launches nothing.
+ */
+GB_API gb_status_t gb_splitk_workspace_bytes(int ffn, int64_t M, int64_t N, int64_t K, int splits,
+                                             size_t* bytes);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word.
  * GB_OK if no kernel recorded a fault since the last call; GB_ERR_TIMEOUT if a
  * pipeline wait ran out of time (the kernel then stopped early and its output
@@ -129,7 +172,9 @@ GB_API const char* gb_last_error(void);
  * a comma-separated list of key=value pairs, or NULL / "" to restore the
  * built-in heuristic.  Keys: bn (linear tile width: 128 or 256), grid (maximum
  * number of CTAs; 0 = one per SM), persistent (0 = one tile per CTA),
- * group (tile-swizzle group size along M, >= 1), zigzag (0, 1, or -1 = auto).
+ * group (tile-swizzle group size along M, >= 1), zigzag (0, 1, or -1 = auto),
+ * pair (1 = CTA pairs with 256-row tiles, 0 = single CTAs with 128-row tiles,
+ * -1 = auto; the 128-wide linear tile always runs on single CTAs).
  * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
  */
 GB_API gb_status_t gb_set_config(const char* spec);

@@ -123,3 +123,17 @@ def test_kernels_have_no_stack_frame_or_spills(L):
     assert entries and len(props) >= len(entries)
     for e, (stack, st, ld) in zip(entries, props):
         assert (int(stack), int(st), int(ld)) == (0, 0, 0), e
+
+
+def test_splitk_entry_points_validate_first(L):
+    assert L.gb_splitk_workspace_bytes(0, 16, 16, 16, 0, None) == GB_ERR_INVALID_ARG
+    n = ctypes.c_size_t(7)
+    assert L.gb_splitk_workspace_bytes(0, -1, 16, 16, 0, ctypes.byref(n)) == GB_ERR_INVALID_ARG
+    assert L.gb_gemm_linear_splitk(None, 64, P16, 64, None, None, 0, 0, P16, 32, 16, 32, 64, 4, P16, 1 << 20,
+                                   None) == GB_ERR_INVALID_ARG
+    assert b"A is null" in L.gb_last_error()
+    assert L.gb_gemm_ffn_gated_splitk(P16, 64, P16, 64, None, 64, P16, 32, 16, 32, 64, 4, P16, 1 << 20,
+                                      None) == GB_ERR_INVALID_ARG
+    # empty problems need no workspace and no device
+    assert L.gb_gemm_linear_splitk(None, 0, None, 0, None, None, 0, 0, None, 0, 0, 5, 7, 0, None, 0,
+                                   None) == GB_OK

@@ -1,0 +1,49 @@
+"""Failure detection on the GPU without a GPU fault: the test hook makes the
+producer never issue its first pipeline stage, so a bounded wait inside the
+kernel runs out.  The kernel must drain what it has in flight, free TMEM,
+return, and report GB_ERR_TIMEOUT through the device status word; the CUDA
+context must stay usable (a normal call right after is correct)."""
+import numpy as np
+import pytest
+
+import oracle
+import dense_bf16_gemm_persistent_gb300 as gb
+from dense_bf16_gemm_persistent_gb300 import inputs
+from tests.gpu_util import assert_close, bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("kind", ["linear", "ffn"])
+@pytest.mark.parametrize("pair", [0, 1])
+def test_wait_timeout_is_reported_and_context_survives(kind, pair):
+    M, N, K = 512, 768, 1024
+    A = inputs.randn_bf16((M, K), seed=1).cuda()
+    B = inputs.randn_bf16((N, K), seed=2, std=1.0 / np.sqrt(K)).cuda()
+    B3 = inputs.randn_bf16((N, K), seed=3, std=1.0 / np.sqrt(K)).cuda()
+    gb.device_status()
+    gb.set_config(f"pair={pair}")
+    gb.set_wait_timeout_ns(100_000_000)  # 0.1 s
+    gb.set_fault_injection(1)
+    try:
+        if kind == "linear":
+            gb.linear(A, B)
+        else:
+            gb.ffn_gated(A, B, B3)
+        with pytest.raises(gb.GBError) as ei:
+            gb.device_status()
+        assert ei.value.status == 4, str(ei.value)
+        assert "timed out" in str(ei.value)
+    finally:
+        gb.set_fault_injection(0)
+        gb.set_wait_timeout_ns(0)
+    gb.device_status()  # the status word was cleared by the read above
+    if kind == "linear":
+        D = gb.linear(A, B)
+        gb.device_status()
+        assert_close(bits(D), oracle.linear(bits(A), bits(B)), "after timeout")
+    else:
+        D = gb.ffn_gated(A, B, B3)
+        gb.device_status()
+        assert_close(bits(D), oracle.ffn_gated(bits(A), bits(B), bits(B3)), "after timeout")
+    gb.set_config(None)

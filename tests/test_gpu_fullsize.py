@@ -66,11 +66,13 @@ def test_llama_ffn_8192x14336x4096():
     assert_close(grid_of(D, r, c), ref, "llama_ffn")
 
 
+@pytest.mark.parametrize("split_k", [None, "auto"], ids=["nosplit", "autosplit"])
 @pytest.mark.parametrize("M,N,K", inputs.ragged_combos(), ids=lambda v: str(v))
-def test_ragged_residual(M, N, K):
-    """D = A.B^T + R with every tile edge predicated (M, N not tile multiples)."""
+def test_ragged_residual(M, N, K, split_k):
+    """D = A.B^T + R with every tile edge predicated (M, N not tile multiples); also
+    through the split-K entry point with its automatic split count."""
     w = inputs.ragged(M, N, K, device=DEV)
-    D = gb.linear(w["A"], w["B"], None, w["R"])
+    D = gb.linear(w["A"], w["B"], None, w["R"], split_k=split_k)
     gb.device_status()
     if M * N * K <= FULL_COMPARE_MACS:
         ref = oracle.linear(bits(w["A"]), bits(w["B"]), None, bits(w["R"]))
@@ -79,7 +81,7 @@ def test_ragged_residual(M, N, K):
         r, c = sample(M, N, seed=M + N + K)
         ref = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c), None, grid_of(w["R"], r, c))
         assert_close(grid_of(D, r, c), ref, f"ragged {M}x{N}x{K}")
-    if K == 4096:
+    if K == 4096 and split_k is None:
         # the product alone (R = 0), and the residual alone (A = 0: D must equal R exactly)
         Z = torch.zeros_like(w["R"])
         D0 = gb.linear(w["A"], w["B"], None, Z)
@@ -121,4 +123,4 @@ def test_bench_configuration_is_the_default():
     w = inputs.mlp_gelu(device=DEV, M=1024, N=2048, K=512)
     gb.linear(w["A"], w["B"], w["bias"], None, act="gelu_tanh")
     plan = gb.last_plan()
-    assert "kernel=linear" in plan and "bn=256" in plan and "d_store=tma" in plan
+    assert "kernel=linear pair=1 tile=256x256x64" in plan and "d_store=tma" in plan, plan

@@ -42,11 +42,13 @@ def test_plain_256x384x512():
     assert_close(run_linear(w["A"], w["B"]), ref_linear(w["A"], w["B"]), "plain")
 
 
+@pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (300, 700, 520), (1, 1, 8), (129, 257, 72),
                                    (127, 255, 4096), (513, 96, 1000)])
-def test_integer_inputs_bit_exact(M, N, K):
+def test_integer_inputs_bit_exact(M, N, K, pair):
     """Small-integer operands: every partial sum is exact in fp32 in any order, so the
     GPU must reproduce the oracle bit for bit."""
+    gb.set_config(f"pair={pair}")
     A = int_tensor((M, K), 1)
     B = int_tensor((N, K), 2)
     bias = int_tensor((N,), 3, -4, 4)
@@ -69,7 +71,7 @@ def test_index_pattern_exact():
     assert_bitexact(run_linear(A, B), bits(want), "index pattern")
 
 
-@pytest.mark.parametrize("M", [1, 127, 128, 129, 255, 257])
+@pytest.mark.parametrize("M", [1, 127, 128, 129, 255, 257, 513])
 @pytest.mark.parametrize("N", [1, 96, 128, 129, 256, 257, 520])
 @pytest.mark.parametrize("K", [8, 64, 200])
 def test_tile_edges(M, N, K):
@@ -151,8 +153,10 @@ def test_empty_outputs():
     assert gb.linear(B, A).shape == (32, 0)
 
 
+@pytest.mark.parametrize("pair", [-1, 0, 1])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 500, 200), (1, 7, 8), (257, 129, 1000)])
-def test_ffn_gated(M, N, K):
+def test_ffn_gated(M, N, K, pair):
+    gb.set_config(f"pair={pair}")
     X = inputs.randn_bf16((M, K), seed=70)
     W1 = inputs.randn_bf16((N, K), seed=71, std=1.0 / np.sqrt(K))
     W3 = inputs.randn_bf16((N, K), seed=72, std=1.0 / np.sqrt(K))
@@ -178,7 +182,9 @@ def test_ffn_integer_bit_exact_when_gate_is_relu_like():
 
 
 @pytest.mark.parametrize("spec", ["bn=128", "bn=256", "persistent=0", "grid=3", "grid=1", "group=1",
-                                  "group=3,grid=5", "bn=128,grid=7,group=2"])
+                                  "group=3,grid=5", "bn=128,grid=7,group=2", "pair=0", "pair=1",
+                                  "pair=1,grid=2", "pair=1,persistent=0", "pair=0,grid=5,group=2",
+                                  "pair=1,group=1,grid=6"])
 def test_config_overrides_give_identical_bits(spec):
     """Tile size, grid, swizzle and persistence change which CTA computes a tile but not
     the per-element accumulation order within the tile: identical bits."""

@@ -1,0 +1,128 @@
+"""Split-K (the schedule the pages' persistent Hopper scheduler lacks): the CUDA
+path against the CPU oracle for skinny shapes, explicit split counts, CTA pairs,
+the FFN fusion, workspace reuse across calls, determinism, and bit-exactness on
+integer inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_bf16_gemm_persistent_gb300 as gb
+from dense_bf16_gemm_persistent_gb300 import inputs
+from tests.gpu_util import assert_bitexact, assert_close, bits, int_tensor
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _reset():
+    gb.set_config(None)
+    yield
+    gb.set_config(None)
+    gb.device_status()
+
+
+def _lin(M, N, K, seed=0, bias=False, R=False, act="none"):
+    A = inputs.randn_bf16((M, K), seed=seed)
+    B = inputs.randn_bf16((N, K), seed=seed + 1, std=1.0 / np.sqrt(K))
+    b = inputs.randn_bf16((N,), seed=seed + 2, std=0.1) if bias else None
+    r = inputs.randn_bf16((M, N), seed=seed + 3) if R else None
+    ref = oracle.linear(bits(A), bits(B), None if b is None else bits(b), None if r is None else bits(r), act)
+    dev = [None if t is None else t.to(DEV) for t in (A, B, b, r)]
+    return dev, ref
+
+
+@pytest.mark.parametrize("M,N,K", [(127, 96, 65536), (1000, 96, 4096), (127, 4099, 4096), (3001, 96, 4096),
+                                   (200, 300, 2000), (129, 257, 520)])
+def test_auto_split_matches_oracle(M, N, K):
+    (A, B, b, r), ref = _lin(M, N, K, bias=True, R=True, act="gelu_tanh")
+    D = gb.linear(A, B, b, r, act="gelu_tanh", split_k="auto")
+    gb.device_status()
+    assert_close(bits(D), ref, f"{M}x{N}x{K} {gb.last_plan()}")
+
+
+def test_auto_split_actually_splits_skinny_shapes():
+    A = torch.zeros((127, 65536), dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros((96, 65536), dtype=torch.bfloat16, device=DEV)
+    gb.linear(A, B, split_k="auto")
+    gb.device_status()
+    plan = gb.last_plan()
+    splits = int(plan.split("splits=")[1].split()[0])
+    assert splits > 16, plan
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64, 1000])
+@pytest.mark.parametrize("pair", [0, 1])
+def test_explicit_splits(splits, pair):
+    gb.set_config(f"pair={pair}")
+    M, N, K = 300, 520, 1000      # 16 k-blocks; 1000 is clamped to 16
+    (A, B, b, r), ref = _lin(M, N, K, seed=10, bias=True, R=True, act="silu")
+    D = gb.linear(A, B, b, r, act="silu", split_k=splits)
+    gb.device_status()
+    assert_close(bits(D), ref, f"splits={splits} {gb.last_plan()}")
+
+
+@pytest.mark.parametrize("splits", [2, 5])
+def test_integer_inputs_bit_exact(splits):
+    M, N, K = 260, 300, 640
+    A, B = int_tensor((M, K), 20), int_tensor((N, K), 21)
+    R = int_tensor((M, N), 22, -3, 3)
+    ref = oracle.linear(bits(A), bits(B), None, bits(R))
+    D = gb.linear(A.to(DEV), B.to(DEV), None, R.to(DEV), split_k=splits)
+    gb.device_status()
+    assert_bitexact(bits(D), ref, f"splits={splits}")
+
+
+def test_deterministic_across_runs():
+    (A, B, _, _), _ = _lin(127, 1000, 8192, seed=30)
+    ws = torch.empty(gb.splitk_workspace_bytes(127, 1000, 8192, 0), dtype=torch.uint8, device=DEV)
+    d1 = gb.linear(A, B, split_k="auto", workspace=ws)
+    d2 = gb.linear(A, B, split_k="auto", workspace=ws)
+    gb.device_status()
+    assert torch.equal(d1.view(torch.int16), d2.view(torch.int16))
+
+
+def test_workspace_reuse_across_shapes():
+    """One workspace for calls of different shapes in a row: the per-slab counters are
+    cleared by every call, so each result is right."""
+    cases = [(127, 96, 8192), (300, 200, 4096), (127, 96, 8192)]
+    need = max(gb.splitk_workspace_bytes(M, N, K, 0) for M, N, K in cases)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    for i, (M, N, K) in enumerate(cases):
+        (A, B, _, r), ref = _lin(M, N, K, seed=40 + i, R=True)
+        D = gb.linear(A, B, None, r, split_k="auto", workspace=ws)
+        gb.device_status()
+        assert_close(bits(D), ref, f"case {i}")
+
+
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("splits", ["auto", 3])
+def test_ffn_split(pair, splits):
+    gb.set_config(f"pair={pair}")
+    M, N, K = 300, 260, 2048
+    X = inputs.randn_bf16((M, K), seed=50)
+    W1 = inputs.randn_bf16((N, K), seed=51, std=1.0 / np.sqrt(K))
+    W3 = inputs.randn_bf16((N, K), seed=52, std=1.0 / np.sqrt(K))
+    D = gb.ffn_gated(X.to(DEV), W1.to(DEV), W3.to(DEV), split_k=splits)
+    gb.device_status()
+    assert_close(bits(D), oracle.ffn_gated(bits(X), bits(W1), bits(W3)), f"ffn {gb.last_plan()}")
+
+
+def test_workspace_checks():
+    A = torch.zeros((127, 4096), dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros((96, 4096), dtype=torch.bfloat16, device=DEV)
+    D = torch.empty((127, 96), dtype=torch.bfloat16, device=DEV)
+    need = gb.splitk_workspace_bytes(127, 96, 4096, 8)
+    assert need > 0
+    L = gb.lib()
+    small = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    st = L.gb_gemm_linear_splitk(A.data_ptr(), 4096, B.data_ptr(), 4096, None, None, 0, 0, D.data_ptr(), 96,
+                                 127, 96, 4096, 8, small.data_ptr(), small.numel(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == 1 and b"smaller" in L.gb_last_error()
+    st = L.gb_gemm_linear_splitk(A.data_ptr(), 4096, B.data_ptr(), 4096, None, None, 0, 0, D.data_ptr(), 96,
+                                 127, 96, 4096, 8, None, 0, torch.cuda.current_stream().cuda_stream)
+    assert st == 1 and b"workspace" in L.gb_last_error()
+    # no split needed -> no workspace needed
+    assert gb.splitk_workspace_bytes(8192, 8192, 4096, 0) == 0
