@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
                                                ctypes.c_size_t, p]
         L.gb_splitk_workspace_bytes.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_size_t)]
+        L.gb_gemm_linear_splitk_noalloc.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64,
+                                                     i64, ctypes.c_int, p]
+        L.gb_static_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
         L.gb_get_device_status.argtypes = [p]
         L.gb_last_error.argtypes = []
         L.gb_last_error.restype = ctypes.c_char_p
@@ -66,7 +69,8 @@ def lib() -> ctypes.CDLL:
         L.gb_version.argtypes = []
         L.gb_version.restype = ctypes.c_char_p
         for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_splitk", "gb_gemm_ffn_gated_splitk",
-                     "gb_splitk_workspace_bytes", "gb_get_device_status", "gb_set_config",
+                     "gb_splitk_workspace_bytes", "gb_gemm_linear_splitk_noalloc", "gb_static_scratch_bytes",
+                     "gb_get_device_status", "gb_set_config",
                      "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan"):
             getattr(L, name).restype = st
         _lib = L

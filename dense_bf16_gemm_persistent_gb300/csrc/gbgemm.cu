@@ -478,6 +478,44 @@ bool parse_int(const char* s, size_t n, long* out) {
     return true;
 }
 
+// ---------------------------------------------------------------- static split-K scratch
+
+// Scratch for gb_gemm_linear_splitk_noalloc: a fixed array in this library's own
+// device memory, so that callers who may not allocate device memory can still
+// run the split-K schedule.  Every GPU that loads the library holds these bytes
+// until the process exits.  All calls share it.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+// The device address of g_static_scratch on the current device `dev`.  In host
+// code the array's name is only a host-side stand-in, so the address is looked
+// up once per device (with that device current) and cached.
+gb_status_t static_scratch_address(int dev, void** out) {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static split-K scratch)");
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return GB_OK;
+}
+
+// Workspace bytes the existing split-K plan needs for this problem and split count.
+gb_status_t splitk_bytes_for(const Problem& pr, int splits, size_t* bytes) {
+    SplitReq sr;
+    sr.allowed = true;
+    sr.splits = splits;
+    sr.query_only = true;
+    sr.ws_needed = bytes;
+    *bytes = 0;
+    return run(pr, nullptr, sr);
+}
+
 }  // namespace
 
 extern "C" {
@@ -538,6 +576,61 @@ gb_status_t gb_splitk_workspace_bytes(int ffn, int64_t M, int64_t N, int64_t K, 
     sr.ws_needed = bytes;
     *bytes = 0;
     return run(pr, nullptr, sr);
+}
+
+gb_status_t gb_gemm_linear_splitk_noalloc(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                                          const void* R, int64_t ldr, int act, void* D, int64_t ldd, int64_t M,
+                                          int64_t N, int64_t K, int splits, void* stream) {
+    t_error.clear();
+    Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false};
+    gb_status_t st = validate(pr);
+    if (st != GB_OK) return st;
+    if (pr.m == 0 || pr.n == 0) {
+        t_plan = "empty (no launch)";
+        return GB_OK;
+    }
+    int dev = 0;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != GB_OK) return st;
+    void* scratch = nullptr;
+    if ((st = static_scratch_address(dev, &scratch)) != GB_OK) return st;
+
+    size_t need = 0;
+    if ((st = splitk_bytes_for(pr, splits, &need)) != GB_OK) return st;
+    if (need > kStaticScratchBytes) {
+        if (splits > 0)
+            return fail(GB_ERR_UNSUPPORTED,
+                        "split-K with %d splits needs %zu bytes of scratch, more than the %zu-byte static scratch "
+                        "of gb_gemm_linear_splitk_noalloc; use fewer splits or gb_gemm_linear_splitk",
+                        splits, need, kStaticScratchBytes);
+        // Automatic split count: the largest one whose partials fit the static scratch.
+        const int kb = static_cast<int>(cdiv(pr.k, gb::kBK));
+        int lo = 1, hi = kb;
+        while (lo < hi) {
+            const int mid = lo + (hi - lo + 1) / 2;
+            size_t b = 0;
+            if ((st = splitk_bytes_for(pr, mid, &b)) != GB_OK) return st;
+            if (b <= kStaticScratchBytes) lo = mid;
+            else hi = mid - 1;
+        }
+        splits = lo;
+        if ((st = splitk_bytes_for(pr, splits, &need)) != GB_OK) return st;
+        if (need > kStaticScratchBytes)
+            return fail(GB_ERR_UNSUPPORTED, "problem needs %zu bytes of split-K scratch, more than the %zu-byte static "
+                        "scratch", need, kStaticScratchBytes);
+    }
+    SplitReq sr;
+    sr.allowed = true;
+    sr.splits = splits;
+    sr.ws = scratch;
+    sr.ws_bytes = kStaticScratchBytes;
+    return run(pr, stream, sr);
+}
+
+gb_status_t gb_static_scratch_bytes(size_t* bytes) {
+    if (!bytes) return fail(GB_ERR_INVALID_ARG, "bytes is null");
+    *bytes = kStaticScratchBytes;
+    return GB_OK;
 }
 
 gb_status_t gb_get_device_status(void* stream) {

@@ -155,6 +155,36 @@ GB_API gb_status_t gb_splitk_workspace_bytes(int ffn, int64_t M, int64_t N, int6
                                              size_t* bytes);
 
 /*
+ * gb_gemm_linear_splitk without a workspace argument: the split-K partials and
+ * counters live in a fixed 32 MiB array in this library's own device memory
+ * (gb_static_scratch_bytes), so the call allocates no device memory at all.
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that may not allocate device memory themselves and cannot lend one --
+ * for example a framework whose own caching allocator must own every device
+ * allocation, or a serving runtime that reserves all memory at start-up and may
+ * not allocate while it handles requests.
+ *   splits  > 0: used as given (clamped as in gb_gemm_linear_splitk); if its
+ *           partials do not fit the static scratch the call returns
+ *           GB_ERR_UNSUPPORTED with the bytes needed and allowed.
+ *           <= 0: automatic, lowered if needed until the partials fit.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that first
+ * call before any stream capture.  Every call on a device shares the one array,
+ * which keeps the previous call's contents: each call clears its counters on
+ * `stream` first, and calls that overlap on the GPU (different streams without
+ * ordering) race on the array.  Other arguments, errors and limits as
+ * gb_gemm_linear_splitk.
+ */
+GB_API gb_status_t gb_gemm_linear_splitk_noalloc(const void* A, int64_t lda, const void* B, int64_t ldb,
+                                                 const void* bias, const void* R, int64_t ldr, int act,
+                                                 void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                                                 int splits, void* stream);
+
+/* Size in bytes of the static scratch gb_gemm_linear_splitk_noalloc uses
+ * (GB_ERR_INVALID_ARG for a null pointer). */
+GB_API gb_status_t gb_static_scratch_bytes(size_t* bytes);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word.
  * GB_OK if no kernel recorded a fault since the last call; GB_ERR_TIMEOUT if a
  * pipeline wait ran out of time (the kernel then stopped early and its output
