@@ -389,7 +389,7 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     if (d_tma) flags |= gb::kFlagDTma;
     prm.flags = flags;
 
-    const uint32_t b_rows = static_cast<uint32_t>(bn / (V::kPair ? 2 : 1));
+    const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
     if (pr.k > 0) {
         if ((st = make_tmap(&prm.tm_a, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             GB_OK)

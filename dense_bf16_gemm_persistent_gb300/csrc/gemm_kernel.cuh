@@ -288,29 +288,37 @@ __device__ __forceinline__ void add_f32x32_cg(float (&v)[32], const float* src) 
 // ---------------------------------------------------------------- the kernel
 
 // Compile-time shape of one kernel variant.
-//   BN    : MMA N, i.e. tile width per B operand (the pair's width when PAIR)
+//   BN    : output tile width (columns of D per tile)
 //   NUM_B : 1 (linear) or 2 (FFN: W1 and W3 share the A tile)
-//   PAIR  : CTA pair with cta_group::2 (tile 256 x BN, each CTA holds 128 rows
-//           of A and BN/2 rows of each B operand) or a single CTA (128 x BN)
+//   PAIR  : CTA pair with cta_group::2 (256-row tiles, each CTA holds 128 rows
+//           of A) or a single CTA (128-row tiles)
+// Every variant issues ONE MMA per 16-wide K slice with N = NUM_B * BN: for the
+// FFN the B operand is [W1 tile ; W3 tile], so the accumulator holds
+// [X.W1^T | X.W3^T] and the A tile is read once for both products.  In a pair
+// the B operand is split along N between the two CTAs, so the even CTA loads
+// the W1 tile and the odd CTA the W3 tile.
 template <int BN, int NUM_B, int STAGES, bool PAIR>
 struct KernelShape {
     static constexpr int kCG = PAIR ? 2 : 1;
     static constexpr int kTileM = kBM * kCG;
-    static constexpr int kBRows = BN / kCG;  // rows of each B operand this CTA loads
+    static constexpr int kMmaN = NUM_B * BN;
+    static constexpr int kBRows = kMmaN / kCG;  // rows of the B operand this CTA holds
+    static constexpr int kBBox = NUM_B == 1 ? kBRows : BN;  // rows per B TMA box
     static constexpr uint32_t kABytes = kBM * kBK * 2;
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
-    static constexpr uint32_t kStageBytes = kABytes + NUM_B * kBBytes;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTxBytes = kCG * kStageBytes;  // bytes the leader's full barrier waits for
     static constexpr uint32_t kRingBytes = STAGES * kStageBytes;
     static constexpr uint32_t kDStageTotal = 4 * 2 * kDStageBytes;
     static constexpr uint32_t kBarBytes = 2 * STAGES * 8;
     static constexpr uint32_t kSmemBytes =
         1024 /* alignment slack */ + kRingBytes + kDStageTotal + kBarBytes + sizeof(SharedCtl);
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kMmaN);
     static constexpr uint32_t kAccEmptyArrivals = 4 * kCG;  // epilogue warps of every CTA in the pair
-    static_assert(NUM_B * BN <= kAccStride, "accumulator buffer holds at most 256 columns");
+    static_assert(kMmaN <= kAccStride, "accumulator buffer holds at most 256 columns");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
-    static_assert(kBRows % 8 == 0 && kBRows <= 256, "B box rows");
+    static_assert(kBRows % 8 == 0 && kBRows <= 256 && kMmaN % 16 == 0, "B operand rows");
+    static_assert(NUM_B == 1 || BN == kBRows || 2 * BN == kBRows, "FFN: one product per CTA or both stacked");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -393,17 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                     uint8_t* st = ring + s * S::kStageBytes;
                     const uint32_t own_full = smem_addr(&full[s]);
                     if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
+                    uint8_t* sb = st + S::kABytes;
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
                         tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);
-                        tma_load_2d_pair(smem_addr(st + S::kABytes), &p.tm_b0, fb, kb * kBK, b_row);
-                        if (NUM_B == 2)
-                            tma_load_2d_pair(smem_addr(st + S::kABytes + S::kBBytes), &p.tm_b1, fb, kb * kBK, b_row);
+                        if (NUM_B == 1)
+                            tma_load_2d_pair(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row);
+                        else  // this CTA's half of the N = 2 BN operand is one whole product
+                            tma_load_2d_pair(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK, nb * BN);
                     } else {
                         tma_load_2d(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row);
-                        tma_load_2d(smem_addr(st + S::kABytes), &p.tm_b0, own_full, kb * kBK, b_row);
+                        tma_load_2d(smem_addr(sb), &p.tm_b0, own_full, kb * kBK, NUM_B == 1 ? b_row : nb * BN);
                         if (NUM_B == 2)
-                            tma_load_2d(smem_addr(st + S::kABytes + S::kBBytes), &p.tm_b1, own_full, kb * kBK, b_row);
+                            tma_load_2d(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK, nb * BN);
                     }
                 }
             }
@@ -453,10 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         // +32 bytes along K per 16-element slice: +2 in the >>4-encoded address
                         const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
                         mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, S::kIdesc, acc);
-                        if (NUM_B == 2) {
-                            const uint64_t b1desc = sdesc_kmajor_sw128(a_addr + S::kABytes + S::kBBytes);
-                            mma_bf16<CG>(d_tmem + BN, adesc + 2 * j, b1desc + 2 * j, S::kIdesc, acc);
-                        }
                     }
                     issued = true;
                     if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
