@@ -36,11 +36,26 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1000 * 1000
 
 WORKLOADS = {
-    "mlp_gelu": dict(M=8192, N=14336, K=4096, kind="linear", act="gelu_tanh", bias=True,
+    "mlp_gelu": dict(M=8192, N=14336, K=4096, kind="linear", act="gelu_tanh", bias=True, residual=False,
                      name="mlp_gelu_8192x14336x4096"),
-    "llama_ffn": dict(M=8192, N=14336, K=4096, kind="ffn", act="silu*", bias=False,
+    "llama_ffn": dict(M=8192, N=14336, K=4096, kind="ffn", act="none", bias=False, residual=False,
                       name="llama_ffn_8192x14336x4096"),
+    "plain": dict(M=256, N=384, K=512, kind="linear", act="none", bias=False, residual=False,
+                  name="plain_256x384x512"),
+    "int64": dict(M=65536, N=4096, K=65536, kind="linear", act="none", bias=False, residual=False,
+                  name="int64_65536x4096x65536"),
 }
+
+
+def workload(spec: str) -> dict:
+    """A named workload, or "ragged:M,N,K" (D = A.B^T + R through the split-K entry point)."""
+    if spec in WORKLOADS:
+        return dict(WORKLOADS[spec])
+    if spec.startswith("ragged:"):
+        M, N, K = (int(v) for v in spec.split(":", 1)[1].split(","))
+        return dict(M=M, N=N, K=K, kind="linear", act="none", bias=False, residual=True, split_k="auto",
+                    name=f"ragged_residual_{M}x{N}x{K}")
+    raise SystemExit(f"unknown workload {spec!r}")
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -185,9 +200,31 @@ def recorded_traffic(workload: str):
 
 def make_inputs(wl: dict, device):
     from dense_bf16_gemm_persistent_gb300 import inputs
+    M, N, K = wl["M"], wl["N"], wl["K"]
     if wl["kind"] == "ffn":
-        return inputs.llama_ffn(device=device, M=wl["M"], N=wl["N"], K=wl["K"])
-    return inputs.mlp_gelu(device=device, M=wl["M"], N=wl["N"], K=wl["K"])
+        return inputs.llama_ffn(device=device, M=M, N=N, K=K)
+    if wl["name"].startswith("ragged"):
+        t = inputs.ragged(M, N, K, device=device)
+    elif wl["name"].startswith("int64"):
+        t = inputs.int64_case(device=device, M=M, N=N, K=K)
+    elif wl["name"].startswith("plain"):
+        t = inputs.plain(device=device, M=M, N=N, K=K)
+    else:
+        return inputs.mlp_gelu(device=device, M=M, N=N, K=K)
+    t.setdefault("bias", None)
+    t.setdefault("R", None)
+    return t
+
+
+def algorithmic_bytes(wl: dict) -> float:
+    """One read of every input and one write of D (bf16)."""
+    M, N, K = wl["M"], wl["N"], wl["K"]
+    b = M * K + N * K * (2 if wl["kind"] == "ffn" else 1) + M * N
+    if wl.get("bias"):
+        b += N
+    if wl.get("residual"):
+        b += M * N
+    return 2.0 * b
 
 
 def flops_per_step(wl: dict) -> float:
@@ -195,26 +232,23 @@ def flops_per_step(wl: dict) -> float:
     return 2 * per if wl["kind"] == "ffn" else per
 
 
-def step_fn(wl: dict, t: dict, out):
+def step_fn(wl: dict, t: dict, out, workspace=None):
     import dense_bf16_gemm_persistent_gb300 as gb
     if wl["kind"] == "ffn":
         return lambda: gb.ffn_gated(t["X"], t["W1"], t["W3"], out=out)
-    return lambda: gb.linear(t["A"], t["B"], t["bias"], None, act=t["act"], out=out)
+    split = wl.get("split_k")
+    return lambda: gb.linear(t["A"], t["B"], t.get("bias"), t.get("R"), act=t["act"], out=out, split_k=split,
+                             workspace=workspace)
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
 
-def oracle_sample_inputs(wl: dict, rows: int, seed: int = 0) -> dict:
-    """CPU-generated inputs (same recipe as the GPU run) for `rows` output rows."""
+def oracle_sample_inputs(wl: dict, rows: int) -> dict:
+    """CPU-generated inputs of the workload's recipe for its first `rows` output rows."""
     from dense_bf16_gemm_persistent_gb300 import inputs
-    K, N = wl["K"], wl["N"]
-    if wl["kind"] == "ffn":
-        return {"X": inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed)),
-                "W1": inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02)),
-                "W3": inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 2, std=0.02))}
-    return {"A": inputs.to_bits(inputs.randn_bf16((rows, K), seed=seed)),
-            "B": inputs.to_bits(inputs.randn_bf16((N, K), seed=seed + 1, std=0.02)),
-            "bias": inputs.to_bits(inputs.randn_bf16((N,), seed=seed + 2, std=0.02))}
+    small = dict(wl, M=rows)
+    t = make_inputs(small, "cpu")
+    return {k: (inputs.to_bits(v) if hasattr(v, "dtype") else v) for k, v in t.items() if v is not None}
 
 
 def oracle_sample_run(wl: dict, h: dict, rows: int):
@@ -225,8 +259,9 @@ def oracle_sample_run(wl: dict, h: dict, rows: int):
         t0 = time.perf_counter()
         oracle.ffn_gated(h["X"][:rows], h["W1"], h["W3"])
         return time.perf_counter() - t0, 4.0 * rows * N * K, oracle.num_threads()
+    R = h.get("R")
     t0 = time.perf_counter()
-    oracle.linear(h["A"][:rows], h["B"], h["bias"], None, "gelu_tanh")
+    oracle.linear(h["A"][:rows], h["B"], h.get("bias"), None if R is None else R[:rows], h["act"])
     return time.perf_counter() - t0, 2.0 * rows * N * K, oracle.num_threads()
 
 
@@ -272,11 +307,26 @@ def run_reference(args, wl: dict):
     return 0
 
 
+def needs_l2_flush(wl: dict) -> bool:
+    return algorithmic_bytes(wl) < 2 * L2_BYTES
+
+
 def config_of(wl: dict) -> dict:
-    ws = 2 * (wl["M"] * wl["K"] + wl["N"] * wl["K"] * (2 if wl["kind"] == "ffn" else 1) + wl["M"] * wl["N"])
-    return {"workload": wl["name"], "M": wl["M"], "N": wl["N"], "K": wl["K"],
-            "epilogue": "gelu_tanh(acc + bias)" if wl["kind"] == "linear" else "silu(acc1) * acc3",
-            "l2": f"no flush: inputs+output {ws / 1e6:.0f} MB > 129 MB L2"}
+    ws = algorithmic_bytes(wl)
+    if wl["kind"] == "ffn":
+        epi = "silu(acc1) * acc3"
+    elif wl.get("residual"):
+        epi = "acc + R"
+    elif wl.get("bias"):
+        epi = f"{wl['act']}(acc + bias)"
+    else:
+        epi = "none"
+    cfg = {"workload": wl["name"], "M": wl["M"], "N": wl["N"], "K": wl["K"], "epilogue": epi,
+           "l2": (f"flushed between timed steps (256 MB write; inputs+output {ws / 1e6:.1f} MB)"
+                  if needs_l2_flush(wl) else f"no flush: inputs+output {ws / 1e6:.0f} MB > 2x 129 MB L2")}
+    if wl.get("split_k"):
+        cfg["split_k"] = wl["split_k"]
+    return cfg
 
 
 # ------------------------------------------------------------------ our arm
@@ -295,9 +345,14 @@ def run_ours(args, wl: dict):
 
     t = make_inputs(wl, device)
     out = torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16, device=device)
-    step = step_fn(wl, t, out)
+    ws = None
+    if wl.get("split_k"):
+        ws = torch.empty(max(1, gb.splitk_workspace_bytes(wl["M"], wl["N"], wl["K"], 0)), dtype=torch.uint8,
+                         device=device)
+    step = step_fn(wl, t, out, ws)
     stream = torch.cuda.current_stream(device)
     fl = flops_per_step(wl)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device) if needs_l2_flush(wl) else None
 
     # pre-warm (clocks to steady state) + W warm-up steps, all untimed
     sampler = ClockSampler(local)
@@ -312,34 +367,39 @@ def run_ours(args, wl: dict):
         step()
     gb.device_status()
 
-    # timed region: K steps, one event per launch boundary on the launching stream
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # timed region: K steps; an event pair around each launch on the launching stream
+    # (an L2 flush, when the working set fits in L2, runs between the pairs).
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(dist, device)
     torch.cuda.synchronize()
     sampler.mark()
-    evs[0].record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev0[i].record(stream)
         step()
-        evs[i + 1].record(stream)
+        ev1[i].record(stream)
     torch.cuda.synchronize()
     sampler.mark()
     barrier(dist, device)
-    local_ms = evs[0].elapsed_time(evs[-1])
-    launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    launch_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    local_ms = sum(launch_ms)
     gb.device_status()
     clocks = sampler.stop()
     value, slowest_s = aggregate_replicas(fl * args.steps / 1e12, local_ms / 1e3, dist, device)
+    plan = gb.last_plan()
 
     # end to end through the public API: pinned host inputs -> device -> kernel -> host
     e2e = None
     if not args.skip_e2e:
-        names = ["X", "W1", "W3"] if wl["kind"] == "ffn" else ["A", "B", "bias"]
+        names = ["X", "W1", "W3"] if wl["kind"] == "ffn" else [k for k in ("A", "B", "bias", "R") if t.get(k) is not None]
         host = {k: t[k].cpu().pin_memory() for k in names}
         dev_in = {k: torch.empty_like(t[k]) for k in names}
         host_out = torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16).pin_memory()
         tin = dict(dev_in)
         tin["act"] = t.get("act")
-        e2e_step = step_fn(wl, tin, out)
+        e2e_step = step_fn(wl, tin, out, ws)
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = host_out.numel() * host_out.element_size()
 
@@ -377,23 +437,32 @@ def run_ours(args, wl: dict):
     achieved = fl / (avg_launch_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg_bytes = algorithmic_bytes(wl)
     traffic = recorded_traffic(wl["name"])
+    if fl / alg_bytes >= peak * 1e12 / (hbm * 1e9):
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                    "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
+                    "frac_of_sustained": achieved / peak_sustained}
+    else:
+        gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (copy)",
+                    "tflops": achieved}
+    roofline.update({"kernel": "gb::gemm_persistent_kernel", "avg_launch_ms": avg_launch_ms,
+                     "flops_per_launch": fl, "algorithmic_bytes_per_launch": alg_bytes,
+                     "clock_note": "timed after a pre-warm, so under the power cap (see clocks)"})
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": slowest_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(wl),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                     "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
-                     "frac_of_sustained": achieved / peak_sustained,
-                     "clock_note": "timed after a pre-warm, so under the power cap (see clocks)",
-                     "kernel": "gb::gemm_persistent_kernel", "avg_launch_ms": avg_launch_ms,
-                     "flops_per_launch": fl},
+        "roofline": roofline,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "e2e": e2e,
-        "plan": gb.last_plan(),
+        "plan": plan,
     }
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_s)
@@ -409,7 +478,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mlp_gelu")
+    ap.add_argument("--workload", default="mlp_gelu",
+                    help=f"one of {sorted(WORKLOADS)} or ragged:M,N,K (epilogue input, split-K entry point)")
     ap.add_argument("--prewarm-s", type=float, default=1.0, help="untimed seconds of steps before warm-up")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
@@ -419,7 +489,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps >= 1 and --warmup >= 0")
-    wl = WORKLOADS[args.workload]
+    wl = workload(args.workload)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
