@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
         i64, p, st = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         L.gb_gemm_linear.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64, p]
         L.gb_gemm_ffn_gated.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p]
+        L.gb_gemm_linear_preact.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, p, i64, i64, i64, i64,
+                                            p]
         L.gb_gemm_linear_splitk.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64,
                                              ctypes.c_int, p, ctypes.c_size_t, p]
         L.gb_gemm_ffn_gated_splitk.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, ctypes.c_int, p,
@@ -68,7 +70,8 @@ def lib() -> ctypes.CDLL:
         L.gb_last_plan.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         L.gb_version.argtypes = []
         L.gb_version.restype = ctypes.c_char_p
-        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_splitk", "gb_gemm_ffn_gated_splitk",
+        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_preact", "gb_gemm_linear_splitk",
+                     "gb_gemm_ffn_gated_splitk",
                      "gb_splitk_workspace_bytes", "gb_gemm_linear_splitk_noalloc", "gb_static_scratch_bytes",
                      "gb_get_device_status", "gb_set_config",
                      "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan"):
@@ -147,6 +150,31 @@ def linear(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = None, R
         _check(lib().gb_gemm_linear_splitk(pa, lda, pb, ldb, pbias, pr, ldr, ACT[act], pd, ldd, M, N, K, splits,
                                            ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
     return out
+
+
+def linear_preact(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = None, R: torch.Tensor | None = None,
+                  act: str = "none", out: torch.Tensor | None = None, preact: torch.Tensor | None = None,
+                  stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """(D, Z): D as linear(), Z = bf16(A @ B.T + bias), the pre-activation, from the same pass."""
+    M, K = A.shape
+    N = B.shape[0]
+    if act not in ACT:
+        raise ValueError(f"act must be one of {sorted(ACT)}")
+    pa, lda = _mat(A, "A", M, K)
+    pb, ldb = _mat(B, "B", N, K)
+    pr, ldr = _mat(R, "R", M, N)
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.shape != (N,) or (N > 1 and bias.stride(0) != 1):
+            raise ValueError("bias: expected a contiguous CUDA bfloat16 tensor of shape (N,)")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if preact is None:
+        preact = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    pd, ldd = _mat(out, "out", M, N)
+    pz, ldz = _mat(preact, "preact", M, N)
+    _check(lib().gb_gemm_linear_preact(pa, lda, pb, ldb, bias.data_ptr() if bias is not None else None, pr, ldr,
+                                       ACT[act], pd, ldd, pz, ldz, M, N, K, _stream(stream)))
+    return out, preact
 
 
 def ffn_gated(X: torch.Tensor, W1: torch.Tensor, W3: torch.Tensor, out: torch.Tensor | None = None,

@@ -31,6 +31,32 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _check_register_budgets(log: str) -> None:
+    """Refuse a build whose kernels could block forever in setmaxnreg.inc: for every
+    kernel with two epilogue warpgroups (384 threads), the launch register count
+    times the threads must cover the budgets the warpgroups lower and raise to
+    (constants of WarpLayout in gemm_kernel.cuh)."""
+    import re
+    src = open(os.path.join(CSRC, "gemm_kernel.cuh")).read()
+
+    def const(name):
+        return int(re.search(rf"static constexpr int {name} = (\d+);", src).group(1))
+
+    control, epilogue = const("kRegsControl"), const("kRegsEpilogue")
+    entries = re.findall(r"Compiling entry function '(\w+)'.*?Used (\d+) registers", log, flags=re.S)
+    if not entries:
+        raise RuntimeError("no kernels in the ptxas report")
+    for name, regs in entries:
+        m = re.search(r"Li(\d+)EEEv", name)  # the last template argument: epilogue warpgroups
+        epi = int(m.group(1)) if m else 1
+        if epi != 2:
+            continue
+        threads, need = 384, 128 * control + 256 * epilogue
+        if int(regs) * threads < need:
+            raise RuntimeError(f"{name} launches with {regs} registers/thread x {threads} threads, less than "
+                               f"the {need} its warpgroup register budgets need")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Build libgbgemm.so next to this file; the -Xptxas -v report goes to _build/ptxas.log."""
     if not force and not _stale():
@@ -43,6 +69,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stderr[-4000:]}")
+    _check_register_budgets(res.stdout + res.stderr)
     if verbose:
         print(res.stderr)
     os.replace(tmp, LIB)

@@ -51,6 +51,8 @@ struct Config {
     int group = 0;       // 0 = heuristic
     int zigzag = -1;     // -1 = heuristic
     int pair = -1;       // -1 = heuristic, 0 = single CTAs, 1 = CTA pairs
+    int stages = 0;      // 0 = the deepest ring that fits
+    int epi = 0;         // epilogue warpgroups: 0 = heuristic, 1 or 2
 };
 
 std::mutex g_cfg_mu;
@@ -175,9 +177,10 @@ gb_status_t make_tmap(CUtensorMap* out, const void* base, uint64_t inner, uint64
 
 // One kernel variant: its launch attributes are set once per device, and for CTA
 // pairs the number of co-resident clusters is queried once per device.
-template <int BN, int NUM_B, int STAGES, bool PAIR>
+template <int BN, int NUM_B, int STAGES, bool PAIR, int EPI>
 struct Variant {
-    using S = gb::KernelShape<BN, NUM_B, STAGES, PAIR>;
+    using S = gb::KernelShape<BN, NUM_B, STAGES, PAIR, EPI>;
+    static constexpr int kEpi = EPI;
     static constexpr int kStages = STAGES;
     static constexpr bool kPair = PAIR;
     static constexpr int kTileM = S::kTileM;
@@ -186,13 +189,15 @@ struct Variant {
         static std::mutex mu;
         static bool ready[64] = {};
         static int units[64] = {};
-        auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR>;
-        if (S::kSmemBytes > info.smem_optin)
+        auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR, EPI>;
+        const uint32_t smem_max = S::smem_bytes(STAGES, false);
+        if (S::smem_bytes(2, NUM_B == 1) > info.smem_optin)
             return fail(GB_ERR_UNSUPPORTED, "kernel needs %u bytes of shared memory, device allows %zu",
-                        S::kSmemBytes, info.smem_optin);
+                        S::smem_bytes(2, NUM_B == 1), info.smem_optin);
         std::lock_guard<std::mutex> lk(mu);
         if (!ready[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+            const int attr_bytes = static_cast<int>(info.smem_optin);
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, attr_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
             if (PAIR) {
                 cudaLaunchConfig_t cfg = {};
@@ -202,8 +207,8 @@ struct Variant {
                 attr[0].val.clusterDim.y = 1;
                 attr[0].val.clusterDim.z = 1;
                 cfg.gridDim = dim3(2 * (info.sms / 2), 1, 1);
-                cfg.blockDim = dim3(gb::kThreads, 1, 1);
-                cfg.dynamicSmemBytes = S::kSmemBytes;
+                cfg.blockDim = dim3(S::kThreads, 1, 1);
+                cfg.dynamicSmemBytes = smem_max;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
                 int n = 0;
@@ -220,13 +225,20 @@ struct Variant {
         return GB_OK;
     }
 
+    // The deepest ring (<= STAGES, >= 2) that fits next to the staging boxes.
+    static int max_stages(bool r_boxes, size_t smem_optin) {
+        int st = STAGES;
+        while (st > 2 && S::smem_bytes(st, r_boxes) > smem_optin) --st;
+        return st;
+    }
+
     static gb_status_t launch(const GemmParams& p, int units, cudaStream_t stream) {
-        auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR>;
+        auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR, EPI>;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         cfg.gridDim = dim3(units * S::kCG, 1, 1);
-        cfg.blockDim = dim3(gb::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = S::kSmemBytes;
+        cfg.blockDim = dim3(S::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = S::smem_bytes(p.stages, NUM_B == 1 && (p.flags & gb::kFlagResidual));
         cfg.stream = stream;
         if (PAIR) {
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -264,6 +276,8 @@ struct Problem {
     int64_t ldd;
     int64_t m, n, k;
     bool ffn;
+    void* z = nullptr;  // optional second output (linear): the pre-activation
+    int64_t ldz = 0;
 };
 
 gb_status_t validate(const Problem& pr) {
@@ -294,8 +308,10 @@ gb_status_t validate(const Problem& pr) {
         if (pr.lda > kMaxLd || pr.ldb0 > kMaxLd || (pr.ffn && pr.ldb1 > kMaxLd))
             return fail(GB_ERR_UNSUPPORTED, "operand leading dimension too large for TMA");
     }
-    if (!aligned2(pr.d) || (pr.r && !aligned2(pr.r)) || (pr.bias && !aligned2(pr.bias)))
-        return fail(GB_ERR_UNSUPPORTED, "D, R and bias must be 2-byte aligned");
+    if (pr.z && pr.ldz < pr.n) return fail(GB_ERR_INVALID_ARG, "ldz=%" PRId64 " < N=%" PRId64, pr.ldz, pr.n);
+    if (!aligned2(pr.d) || (pr.r && !aligned2(pr.r)) || (pr.bias && !aligned2(pr.bias)) || (pr.z && !aligned2(pr.z)))
+        return fail(GB_ERR_UNSUPPORTED, "D, R, Z and bias must be 2-byte aligned");
+    if (pr.z && pr.ldz > kMaxLd) return fail(GB_ERR_UNSUPPORTED, "leading dimension too large");
     if (pr.ldd > kMaxLd || (pr.r && pr.ldr > kMaxLd)) return fail(GB_ERR_UNSUPPORTED, "leading dimension too large");
     return GB_OK;
 }
@@ -351,9 +367,10 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     if (work > kMaxDim) return fail(GB_ERR_UNSUPPORTED, "too many work items");
 
     const int num_b = pr.ffn ? 2 : 1;
-    const size_t cnt_bytes = splits > 1 ? align_up(static_cast<size_t>(tiles) * 4 * (V::kPair ? 2 : 1) * 4, kWsAlign) : 0;
+    const size_t cnt_bytes = splits > 1 ? align_up(static_cast<size_t>(tiles) * V::S::kSlabs * 4, kWsAlign) : 0;
+    // one fp32 accumulator tile per output tile (per product for the FFN)
     const size_t part_bytes =
-        splits > 1 ? static_cast<size_t>(work) * num_b * V::kTileM * static_cast<size_t>(bn) * sizeof(float) : 0;
+        splits > 1 ? static_cast<size_t>(tiles) * num_b * V::kTileM * static_cast<size_t>(bn) * sizeof(float) : 0;
     const size_t ws_needed = cnt_bytes + part_bytes;
     if (sr.query_only) {
         *sr.ws_needed = ws_needed;
@@ -387,7 +404,18 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     if (!pr.ffn && pr.r) flags |= gb::kFlagResidual | ((aligned16(pr.r) && pr.ldr % 8 == 0) ? gb::kFlagRVec : 0u);
     const bool d_tma = aligned16(pr.d) && pr.ldd % 8 == 0;
     if (d_tma) flags |= gb::kFlagDTma;
+    const bool r_tma = !pr.ffn && pr.r && aligned16(pr.r) && pr.ldr % 8 == 0 && splits == 1;
+    if (r_tma) flags |= gb::kFlagRTma;
+    const bool z_tma = pr.z && aligned16(pr.z) && pr.ldz % 8 == 0;
+    if (!pr.ffn && pr.z) flags |= gb::kFlagZ | (z_tma ? gb::kFlagZTma : 0u);
+    prm.z = static_cast<uint16_t*>(pr.z);
+    prm.ldz = pr.ldz;
     prm.flags = flags;
+    {
+        const int deepest = V::max_stages(!pr.ffn && pr.r, info.smem_optin);
+        int st = cfg.stages > 0 ? std::min(cfg.stages, deepest) : deepest;
+        prm.stages = std::max(2, st);
+    }
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
     if (pr.k > 0) {
@@ -404,6 +432,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     if (d_tma &&
         (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
         return st;
+    if (r_tma &&
+        (st = make_tmap(&prm.tm_r, pr.r, pr.n, pr.m, pr.ldr * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
+        return st;
+    if (z_tma &&
+        (st = make_tmap(&prm.tm_z, pr.z, pr.n, pr.m, pr.ldz * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
+        return st;
 
     // Scheduling units: CTAs, or CTA pairs.  Persistent: at most one per SM (pair
     // of SMs); one work item per unit otherwise.
@@ -417,18 +451,37 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
 
     char plan[360];
     snprintf(plan, sizeof plan,
-             "kernel=%s pair=%d tile=%dx%dx%d stages=%d grid=%lld tiles=%d k_blocks=%d splits=%d group=%d zigzag=%d "
-             "d_store=%s r_load=%s",
-             pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kTileM, bn, gb::kBK, V::kStages,
+             "kernel=%s pair=%d epi=%d tile=%dx%dx%d stages=%d grid=%lld tiles=%d k_blocks=%d splits=%d group=%d "
+             "zigzag=%d "
+             "d_store=%s r_load=%s z_store=%s",
+             pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kEpi, V::kTileM, bn, gb::kBK, prm.stages,
              static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
-             prm.group_m, prm.zigzag, d_tma ? "tma" : "st.global",
-             pr.r ? ((flags & gb::kFlagRVec) ? "ld.v4" : "ld.b16") : "none");
+             prm.group_m, prm.zigzag, d_tma ? "tma" : "st.transposed",
+             pr.r ? (r_tma ? "tma" : (flags & gb::kFlagRVec) ? "ld.v4" : "ld.transposed") : "none",
+             pr.z ? (z_tma ? "tma" : "st.transposed") : "none");
     t_plan = plan;
-    if (cnt_bytes) {
-        cudaError_t e = cudaMemsetAsync(prm.ws_cnt, 0, cnt_bytes, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(split-K counters)");
+    if (ws_needed) {  // counters and accumulators start at zero
+        cudaError_t e = cudaMemsetAsync(prm.ws_cnt, 0, ws_needed, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(split-K workspace)");
     }
     return V::launch(prm, static_cast<int>(units), stream);
+}
+
+template <int EPI>
+gb_status_t dispatch(const Problem& pr, const Config& cfg, int bn, bool pair, int dev, const DeviceInfo& info,
+                     uint64_t timeout_ns, int inject, cudaStream_t stream, const SplitReq& sr) {
+    using LinPair = Variant<256, 1, 6, true, EPI>;
+    using LinSingle = Variant<256, 1, 4, false, EPI>;
+    using LinNarrow = Variant<128, 1, 6, false, EPI>;
+    using FfnPair = Variant<128, 2, 6, true, EPI>;
+    using FfnSingle = Variant<128, 2, 4, false, EPI>;
+    if (pr.ffn)
+        return pair ? plan_and_launch<FfnPair>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr)
+                    : plan_and_launch<FfnSingle>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
+    if (bn == 256)
+        return pair ? plan_and_launch<LinPair>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr)
+                    : plan_and_launch<LinSingle>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
+    return plan_and_launch<LinNarrow>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
 }
 
 gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitReq()) {
@@ -455,18 +508,19 @@ gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitR
     bool pair = cfg.pair >= 0 ? cfg.pair == 1 : pr.m > gb::kBM;
     if (!pr.ffn && bn == 128) pair = false;  // the 128-wide linear tile runs on single CTAs
 
-    using LinPair = Variant<256, 1, 6, true>;
-    using LinSingle = Variant<256, 1, 4, false>;
-    using LinNarrow = Variant<128, 1, 6, false>;
-    using FfnPair = Variant<128, 2, 6, true>;
-    using FfnSingle = Variant<128, 2, 4, false>;
-    if (pr.ffn)
-        return pair ? plan_and_launch<FfnPair>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr)
-                    : plan_and_launch<FfnSingle>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
-    if (bn == 256)
-        return pair ? plan_and_launch<LinPair>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr)
-                    : plan_and_launch<LinSingle>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
-    return plan_and_launch<LinNarrow>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
+    // Epilogue warpgroups: two when the epilogue carries more than the tile's MMAs
+    // hide (short K, a split-K plan over few tiles, rows moved by the shared-memory
+    // transpose, an epilogue input or a second output), one otherwise (measured on
+    // GB300: one is 1-2% faster on the long-K MLP and FFN shapes, two up to 1.4x
+    // faster on short-K shapes with an epilogue input).
+    const int64_t kb = cdiv(pr.k, gb::kBK);
+    const bool d_rows_aligned = aligned16(pr.d) && pr.ldd % 8 == 0;
+    const int64_t tiles_est = cdiv(pr.m, pair ? 2 * gb::kBM : gb::kBM) * cdiv(pr.n, bn);
+    const bool few_tiles_split = sr.allowed && 2 * tiles_est <= info.sms;
+    const int epi = cfg.epi > 0 ? cfg.epi
+                                : ((kb <= 16 || few_tiles_split || !d_rows_aligned || pr.r || pr.z) ? 2 : 1);
+    return epi == 2 ? dispatch<2>(pr, cfg, bn, pair, dev, info, timeout_ns, inject, stream, sr)
+                    : dispatch<1>(pr, cfg, bn, pair, dev, info, timeout_ns, inject, stream, sr);
 }
 
 bool parse_int(const char* s, size_t n, long* out) {
@@ -524,6 +578,15 @@ gb_status_t gb_gemm_linear(const void* A, int64_t lda, const void* B, int64_t ld
                            int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
     t_error.clear();
     Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false};
+    return run(pr, stream);
+}
+
+gb_status_t gb_gemm_linear_preact(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                                  const void* R, int64_t ldr, int act, void* D, int64_t ldd, void* Z, int64_t ldz,
+                                  int64_t M, int64_t N, int64_t K, void* stream) {
+    t_error.clear();
+    if (!Z && M > 0 && N > 0) return fail(GB_ERR_INVALID_ARG, "Z is null");
+    Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false, Z, ldz};
     return run(pr, stream);
 }
 
@@ -671,6 +734,8 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "group" && v >= 1 && v <= 1000000) c.group = static_cast<int>(v);
             else if (key == "zigzag" && v >= -1 && v <= 1) c.zigzag = static_cast<int>(v);
             else if (key == "pair" && v >= -1 && v <= 1) c.pair = static_cast<int>(v);
+            else if (key == "stages" && v >= 0 && v <= 16) c.stages = static_cast<int>(v);
+            else if (key == "epi" && v >= 0 && v <= 2) c.epi = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

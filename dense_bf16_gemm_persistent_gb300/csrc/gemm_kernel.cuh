@@ -13,11 +13,14 @@
 //                       double-buffered fp32 accumulator and tcgen05.commit
 //                       to release each stage once (section "Syncing issues":
 //                       one commit per stage, one per tile).
-//   * warps 4..7     -- epilogue: tcgen05.ld of 32-column chunks, bias,
-//                       activation, epilogue input, bf16 rounding, and a
-//                       chunked TMA store whose shared-memory wait is delayed
-//                       until the buffer is reused (sections "Epilogue inputs"
-//                       and "TMA store and stmatrix").
+//   * warps 4..11    -- epilogue, two warpgroups: tcgen05.ld of 32-column
+//                       chunks, bias, activation, epilogue input (prefetched by
+//                       TMA), bf16 rounding, and a chunked TMA store whose
+//                       shared-memory wait is delayed until the buffer is reused
+//                       (sections "Epilogue inputs" and "TMA store and
+//                       stmatrix").
+//   * registers move from the control warpgroup to the epilogue warpgroups
+//     with setmaxnreg after the role split (section "Register usage/spilling").
 //   * all barriers are initialised once, outside the persistent tile loop, and
 //     the ring position comes from a k-block counter that runs on across
 //     tiles (section "Syncing persistent matmuls").
@@ -41,8 +44,29 @@ namespace gb {
 
 constexpr int kBM = 128;          // tile rows (TMEM lanes)
 constexpr int kBK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 256;     // 8 warps: producer, MMA, 2 spare, 4 epilogue
+// Warpgroup 0: producer (warp 0), TMEM allocator + MMA issuer (warp 1), two
+// spare warps.  Warpgroups 1..EPI: epilogue; epilogue warp e = warp - 4 reads
+// TMEM lane quadrant e % 4 (= warp % 4) and takes every EPI-th 32-column chunk
+// starting at e / 4.  One epilogue warpgroup suits long-K tiles (the epilogue
+// hides under the MMAs); two suit epilogue-bound shapes (short K, epilogue
+// input, unaligned rows).
 constexpr int kEpiWarp0 = 4;
+template <int EPI>
+struct WarpLayout {
+    static constexpr int kGroups = EPI;
+    static constexpr int kEpiWarps = 4 * EPI;
+    static constexpr int kThreads = 128 * (1 + EPI);
+    // With two epilogue warpgroups, registers move to them after the role split
+    // (setmaxnreg).  The launch gives every thread 65536 / kThreads registers
+    // (rounded down to 8); the budgets must fit in that pool.
+    static constexpr bool kRealloc = EPI == 2;
+    static constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;
+    static constexpr int kRegsControl = 80;
+    static constexpr int kRegsEpilogue = 208;
+    static_assert(!kRealloc || 128 * kRegsControl + 128 * EPI * kRegsEpilogue <= kThreads * kRegsLaunch,
+                  "register budgets exceed the launch pool");
+    static_assert(EPI == 1 || EPI == 2, "one or two epilogue warpgroups");
+};
 constexpr int kTmemCols = 512;    // two accumulator buffers of 256 columns
 constexpr int kAccStride = 256;
 constexpr int kDChunk = 32;       // epilogue chunk: 32 columns
@@ -54,6 +78,9 @@ enum : uint32_t {
     kFlagDTma = 4u,      // D stored by TMA (16-byte aligned rows)
     kFlagRVec = 8u,      // R rows 16-byte aligned: vector loads
     kFlagBiasVec = 16u,  // bias 16-byte aligned: vector loads
+    kFlagRTma = 32u,     // R loaded by TMA into shared memory, prefetched ahead of use
+    kFlagZ = 64u,        // also store the pre-activation Z = bf16(acc + bias)
+    kFlagZTma = 128u,    // Z stored by TMA (16-byte aligned rows)
 };
 
 // Codes written to the device status word (low byte = gb_status_t).
@@ -67,9 +94,13 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     CUtensorMap tm_b0;  // B (or W1) [N, K], box {64, BN}, 128B swizzle
     CUtensorMap tm_b1;  // W3 [N, K] (FFN only)
     CUtensorMap tm_d;   // D [M, N], box {32, 32}, 64B swizzle (TMA store path)
+    CUtensorMap tm_r;   // R [M, N], box {32, 32}, 64B swizzle (TMA load path)
+    CUtensorMap tm_z;   // Z [M, N], box {32, 32}, 64B swizzle (TMA store path)
     const uint16_t* bias;
     const uint16_t* r;
     uint16_t* d;
+    uint16_t* z;
+    int64_t ldz;
     int64_t ldr;
     int64_t ldd;
     int32_t m, n, k;
@@ -82,13 +113,15 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     int32_t inject;
     // split-K: each tile's k-blocks are cut into `splits` ranges of `kb_per_split`;
     // work item w = tile * splits + split.  With splits > 1 every epilogue warp
-    // writes its fp32 partial slab to `ws` and the last of the splits (counted in
-    // `ws_cnt`, one counter per 32-row slab, zero on entry) reduces them in split
-    // order and runs the epilogue.
+    // adds its fp32 partial slab into the tile's accumulator in `ws` (fp32
+    // reductions in L2; zero on entry), and the last split to finish a 32-row
+    // slab (counted in `ws_cnt`, zero on entry) reads the sum and runs the
+    // epilogue.
     int32_t splits;
     int32_t kb_per_split;
     float* ws;
     uint32_t* ws_cnt;
+    int32_t stages;  // depth of the operand ring (<= the variant's maximum)
 };
 
 struct SharedCtl {
@@ -205,14 +238,128 @@ __device__ __forceinline__ void add_bf16_row(float (&v)[32], const uint16_t* src
     }
 }
 
+// Add this lane's row of a 32x32 bf16 box staged by TMA with 64-byte swizzling.
+__device__ __forceinline__ void add_bf16_box_row(float (&v)[32], uint32_t box, int lane) {
+    const uint32_t row = box + lane * 64;
+    const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(row + ((u ^ sw) << 4)));
+        v[8 * u + 0] += bf16_lo(w0);
+        v[8 * u + 1] += bf16_hi(w0);
+        v[8 * u + 2] += bf16_lo(w1);
+        v[8 * u + 3] += bf16_hi(w1);
+        v[8 * u + 4] += bf16_lo(w2);
+        v[8 * u + 5] += bf16_hi(w2);
+        v[8 * u + 6] += bf16_lo(w3);
+        v[8 * u + 7] += bf16_hi(w3);
+    }
+}
+
+// Rows of D or R that are not 16-byte aligned (e.g. N = 4099): go through a
+// per-warp shared-memory transpose with a 68-byte row stride (conflict-free), so
+// every global access instruction covers one contiguous 64-byte row segment
+// instead of 32 scattered 2-byte ones.  Warp-collective.
+constexpr uint32_t kTRow = 68;
+static_assert(32 * kTRow <= 2 * kDStageBytes, "transpose buffer fits in a warp's two staging boxes");
+
+__device__ __forceinline__ void store_rows_transposed(const GemmParams& p, uint16_t* out, int64_t ld,
+                                                      const uint32_t (&packed)[16], int32_t row0, int32_t n0,
+                                                      int valid, int lane, uint8_t* tbuf) {
+    if (lane == 0) bulk_wait_group_read<0>();  // TMA stores of this warp no longer read the buffers
+    __syncwarp();
+    uint32_t* mine = reinterpret_cast<uint32_t*>(tbuf + lane * kTRow);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mine[j] = packed[j];
+    __syncwarp();
+    const int rows = min(32, p.m - row0);
+    const uint16_t* col = reinterpret_cast<const uint16_t*>(tbuf) + lane;
+    uint16_t h[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) h[r] = col[r * (kTRow / 2)];  // all reads first...
+    uint16_t* dst = out + static_cast<int64_t>(row0) * ld + n0 + lane;
+    if (lane < valid) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r)  // ...then one coalesced 64-byte row segment per store
+            if (r < rows) dst[static_cast<int64_t>(r) * ld] = h[r];
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void add_rows_transposed(const GemmParams& p, float (&v)[32], int32_t row0, int32_t n0,
+                                                    int valid, int lane, uint8_t* tbuf) {
+    const int rows = min(32, p.m - row0);
+    const uint16_t* src = p.r + static_cast<int64_t>(row0) * p.ldr + n0 + lane;
+    uint16_t h[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r)  // all 32 coalesced row-segment loads in flight together
+        h[r] = (r < rows && lane < valid) ? __ldg(src + static_cast<int64_t>(r) * p.ldr) : uint16_t(0);
+    uint16_t* col = reinterpret_cast<uint16_t*>(tbuf) + lane;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) col[r * (kTRow / 2)] = h[r];
+    __syncwarp();
+    const uint32_t* mine = reinterpret_cast<const uint32_t*>(tbuf + lane * kTRow);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t w = mine[j];
+        v[2 * j] += bf16_lo(w);
+        v[2 * j + 1] += bf16_hi(w);
+    }
+    __syncwarp();
+}
+
+// Store one 32x32 bf16 chunk of an output: by TMA from this warp's next staging
+// box (two boxes alternate; a box is rewritten only after the store that used it
+// has read it -- so several outputs share the boxes), or through the
+// shared-memory transpose when the output's rows are not 16-byte aligned.
+__device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorMap* tm, uint16_t* out, int64_t ld,
+                                            bool by_tma, const uint32_t (&packed)[16], int32_t row0, int32_t n0,
+                                            int valid, int lane, int e, uint8_t* dstage, uint32_t& dcount) {
+    if (by_tma) {
+        uint8_t* buf = dstage + (e * 2 + (dcount & 1u)) * kDStageBytes;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+        __syncwarp();
+        // 64-byte rows, 16-byte units XOR-swizzled with (row / 2) % 4 (TMA 64B swizzle).
+        const uint32_t row_addr = smem_addr(buf) + lane * 64;
+        const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
+                         packed[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, smem_addr(buf), n0, row0);
+            bulk_commit_group();
+        }
+        ++dcount;
+    } else {
+        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, dstage + e * 2 * kDStageBytes);
+    }
+}
+
 // Bias, activation and epilogue input (linear), bf16 rounding, and the store of
 // one 32-column chunk of row m (this lane) of the warp's 32-row slab at row0.
 template <int NUM_B>
+// `rbox` is the shared-memory address of this chunk's R box when R came by TMA
+// (0: read R from global memory); `tbuf_r` is this warp's transpose buffer for an
+// R whose rows are not 16-byte aligned; `e` indexes this warp's staging boxes.
+// Warp-collective.
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32], int32_t m, int32_t row0,
-                                             int32_t n0, int lane, int q, uint8_t* dstage, uint32_t& dcount) {
+                                             int32_t n0, int lane, int e, uint8_t* dstage, uint32_t& dcount,
+                                             uint32_t rbox, uint8_t* tbuf_r) {
     const int valid = min(32, p.n - n0);
     if (NUM_B == 1) {
         if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, valid, p.flags & kFlagBiasVec);
+        if (p.flags & kFlagZ) {  // second output: the pre-activation
+            uint32_t zp[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) zp[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+            store_chunk(p, &p.tm_z, p.z, p.ldz, p.flags & kFlagZTma, zp, row0, n0, valid, lane, e, dstage, dcount);
+        }
         switch (p.act) {
             case 1:
 #pragma unroll
@@ -229,47 +376,30 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
             default:
                 break;
         }
-        if ((p.flags & kFlagResidual) && m < p.m)
-            add_bf16_row(v, p.r + static_cast<int64_t>(m) * p.ldr + n0, valid, p.flags & kFlagRVec);
+        if (rbox) {
+            add_bf16_box_row(v, rbox, lane);
+        } else if (p.flags & kFlagResidual) {
+            if (p.flags & kFlagRVec) {
+                if (m < p.m) add_bf16_row(v, p.r + static_cast<int64_t>(m) * p.ldr + n0, valid, true);
+            } else {
+                add_rows_transposed(p, v, row0, n0, valid, lane, tbuf_r);
+            }
+        }
     }
 
     uint32_t packed[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-
-    if (p.flags & kFlagDTma) {
-        uint8_t* buf = dstage + (q * 2 + (dcount & 1u)) * kDStageBytes;
-        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
-        __syncwarp();
-        // 64-byte rows, 16-byte units XOR-swizzled with (row / 2) % 4 (TMA 64B swizzle).
-        const uint32_t row_addr = smem_addr(buf) + lane * 64;
-        const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
-                         packed[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(&p.tm_d, smem_addr(buf), n0, row0);
-            bulk_commit_group();
-        }
-        ++dcount;
-    } else if (m < p.m) {
-        uint16_t* dst = p.d + static_cast<int64_t>(m) * p.ldd + n0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (j < valid)
-                dst[j] = static_cast<uint16_t>((j & 1) ? (packed[j >> 1] >> 16) : (packed[j >> 1] & 0xffffu));
-        }
-    }
+    store_chunk(p, &p.tm_d, p.d, p.ldd, p.flags & kFlagDTma, packed, row0, n0, valid, lane, e, dstage, dcount);
 }
 
-__device__ __forceinline__ void st_global_f32x32(float* dst, const uint32_t (&r)[32]) {
+// 32 floats added into global memory with vector fp32 reductions (performed in L2).
+__device__ __forceinline__ void red_add_f32x32(float* dst, const uint32_t (&r)[32]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i), "r"(r[4 * i]), "r"(r[4 * i + 1]),
-                     "r"(r[4 * i + 2]), "r"(r[4 * i + 3])
+        asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i),
+                     "f"(__uint_as_float(r[4 * i])), "f"(__uint_as_float(r[4 * i + 1])),
+                     "f"(__uint_as_float(r[4 * i + 2])), "f"(__uint_as_float(r[4 * i + 3]))
                      : "memory");
 }
 
@@ -297,9 +427,13 @@ __device__ __forceinline__ void add_f32x32_cg(float (&v)[32], const float* src) 
 // [X.W1^T | X.W3^T] and the A tile is read once for both products.  In a pair
 // the B operand is split along N between the two CTAs, so the even CTA loads
 // the W1 tile and the odd CTA the W3 tile.
-template <int BN, int NUM_B, int STAGES, bool PAIR>
+template <int BN, int NUM_B, int STAGES, bool PAIR, int EPI>
 struct KernelShape {
+    using W = WarpLayout<EPI>;
+    static constexpr int kEpiWarps = W::kEpiWarps;
+    static constexpr int kThreads = W::kThreads;
     static constexpr int kCG = PAIR ? 2 : 1;
+    static constexpr int kMaxStages = STAGES;  // the ring depth is chosen at launch, up to this
     static constexpr int kTileM = kBM * kCG;
     static constexpr int kMmaN = NUM_B * BN;
     static constexpr int kBRows = kMmaN / kCG;  // rows of the B operand this CTA holds
@@ -308,31 +442,43 @@ struct KernelShape {
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTxBytes = kCG * kStageBytes;  // bytes the leader's full barrier waits for
-    static constexpr uint32_t kRingBytes = STAGES * kStageBytes;
-    static constexpr uint32_t kDStageTotal = 4 * 2 * kDStageBytes;
-    static constexpr uint32_t kBarBytes = 2 * STAGES * 8;
-    static constexpr uint32_t kSmemBytes =
-        1024 /* alignment slack */ + kRingBytes + kDStageTotal + kBarBytes + sizeof(SharedCtl);
+    static constexpr uint32_t kDStageTotal = kEpiWarps * 2 * kDStageBytes;
+    static constexpr uint32_t kRStageTotal = NUM_B == 1 ? kEpiWarps * 2 * kDStageBytes : 0;  // R boxes (linear)
+    static constexpr uint32_t kBarBytes = 2 * STAGES * 8 + 2 * kEpiWarps * 8;  // ring + 2 R barriers per warp
+    // Layout: [ring: stages x stage][D boxes][R boxes, only with an epilogue input][barriers][control].
+    static constexpr uint32_t smem_bytes(int stages, bool r_boxes) {
+        return 1024 /* alignment slack */ + stages * kStageBytes + kDStageTotal + (r_boxes ? kRStageTotal : 0) +
+               kBarBytes + sizeof(SharedCtl);
+    }
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kMmaN);
-    static constexpr uint32_t kAccEmptyArrivals = 4 * kCG;  // epilogue warps of every CTA in the pair
+    static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * kCG;  // epilogue warps of every CTA in the pair
+    static constexpr int kSlabs = kEpiWarps * kCG;                     // split-K counters per tile
     static_assert(kMmaN <= kAccStride, "accumulator buffer holds at most 256 columns");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(kBRows % 8 == 0 && kBRows <= 256 && kMmaN % 16 == 0, "B operand rows");
     static_assert(NUM_B == 1 || BN == kBRows || 2 * BN == kBRows, "FFN: one product per CTA or both stacked");
-    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(smem_bytes(STAGES, false) <= 232448, "the deepest ring fits without R boxes");
+    static_assert(smem_bytes(2, true) <= 232448, "a two-stage ring fits with R boxes");
 };
 
-template <int BN, int NUM_B, int STAGES, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p) {
-    using S = KernelShape<BN, NUM_B, STAGES, PAIR>;
+template <int BN, int NUM_B, int STAGES, bool PAIR, int EPI>
+__global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(const __grid_constant__ GemmParams p) {
+    using S = KernelShape<BN, NUM_B, STAGES, PAIR, EPI>;
+    using W = WarpLayout<EPI>;
+    constexpr int kEpiWarps = W::kEpiWarps;
+    constexpr int kEpiGroups = W::kGroups;
     constexpr int CG = S::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t stages = static_cast<uint32_t>(p.stages);
+    const bool r_boxes = (NUM_B == 1) && (p.flags & kFlagResidual);
     uint8_t* ring = smem;
-    uint8_t* dstage = smem + S::kRingBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(dstage + S::kDStageTotal);
+    uint8_t* dstage = smem + stages * S::kStageBytes;
+    uint8_t* rstage = dstage + S::kDStageTotal;
+    uint64_t* full = reinterpret_cast<uint64_t*>(rstage + (r_boxes ? S::kRStageTotal : 0u));
     uint64_t* empty = full + STAGES;
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(empty + STAGES);
+    uint64_t* rbar = empty + STAGES;  // two per epilogue warp
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(rbar + 2 * kEpiWarps);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -344,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     const int32_t num_work = p.num_tiles * p.splits;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (uint32_t s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
         }
@@ -353,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             mbar_init(smem_addr(&ctl->acc_empty[b]), S::kAccEmptyArrivals);
         }
         mbar_init(smem_addr(&ctl->drain), 1);
+        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(smem_addr(&rbar[i]), 1);
         ctl->abort = 0;
         fence_mbar_init();
     }
@@ -363,6 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             if (NUM_B == 2) tma_prefetch_desc(&p.tm_b1);
         }
         if (p.flags & kFlagDTma) tma_prefetch_desc(&p.tm_d);
+        if (p.flags & kFlagRTma) tma_prefetch_desc(&p.tm_r);
+        if (p.flags & kFlagZTma) tma_prefetch_desc(&p.tm_z);
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_addr(&ctl->tmem_base), kTmemCols);
@@ -374,119 +523,180 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int32_t* abort_flag = &ctl->abort;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer (every CTA)
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            int32_t local = 0;
-            for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
-                const int32_t tile = w / p.splits;
-                const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
-                const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
-                int32_t mb, nb;
-                tile_coords(tile, p, mb, nb);
-                const bool reverse = p.zigzag && (local & 1);
-                const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
-                const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
-                for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
-                    const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, tmo, kRoleProducer, s)) {
-                        ok = false;
-                        break;
+    // Role split.  Each warpgroup sets its register budget inside its own branch, so
+    // the compiler holds the control roles to the small budget and gives the
+    // epilogue the large one; only the short teardown after the branches is shared.
+    if (warp < kEpiWarp0) {
+        if constexpr (W::kRealloc) setmaxnreg_dec<W::kRegsControl>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer (every CTA)
+            if (lane == 0) {
+                uint32_t it = 0;
+                uint32_t s = 0, ph = 0;  // ring slot and phase of k-block `it`
+                bool ok = true;
+                int32_t local = 0;
+                for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
+                    const int32_t tile = w / p.splits;
+                    const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
+                    const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
+                    int32_t mb, nb;
+                    tile_coords(tile, p, mb, nb);
+                    const bool reverse = p.zigzag && (local & 1);
+                    const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
+                    const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
+                    for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
+                        const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
+                        if (kk > 0 || it > 0) {
+                            if (++s == stages) {
+                                s = 0;
+                                ph ^= 1u;
+                            }
+                        }
+                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, tmo, kRoleProducer, s)) {
+                            ok = false;
+                            break;
+                        }
+                        if (p.inject == kInjectSkipFirstStage && it == 0 && leader) continue;  // test hook
+                        uint8_t* st = ring + s * S::kStageBytes;
+                        const uint32_t own_full = smem_addr(&full[s]);
+                        if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
+                        uint8_t* sb = st + S::kABytes;
+                        if constexpr (PAIR) {
+                            const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
+                            tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);
+                            if (NUM_B == 1)
+                                tma_load_2d_pair(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row);
+                            else  // this CTA's half of the N = 2 BN operand is one whole product
+                                tma_load_2d_pair(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK, nb * BN);
+                        } else {
+                            tma_load_2d(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row);
+                            tma_load_2d(smem_addr(sb), &p.tm_b0, own_full, kb * kBK, NUM_B == 1 ? b_row : nb * BN);
+                            if (NUM_B == 2)
+                                tma_load_2d(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK, nb * BN);
+                        }
                     }
-                    if (p.inject == kInjectSkipFirstStage && it == 0 && leader) continue;  // test hook
-                    uint8_t* st = ring + s * S::kStageBytes;
-                    const uint32_t own_full = smem_addr(&full[s]);
-                    if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
-                    uint8_t* sb = st + S::kABytes;
-                    if constexpr (PAIR) {
-                        const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
-                        tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);
-                        if (NUM_B == 1)
-                            tma_load_2d_pair(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row);
-                        else  // this CTA's half of the N = 2 BN operand is one whole product
-                            tma_load_2d_pair(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK, nb * BN);
-                    } else {
-                        tma_load_2d(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row);
-                        tma_load_2d(smem_addr(sb), &p.tm_b0, own_full, kb * kBK, NUM_B == 1 ? b_row : nb * BN);
-                        if (NUM_B == 2)
-                            tma_load_2d(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK, nb * BN);
+                }
+                if (!ok && leader) {
+                    // Drain: the leader's full barriers count the bytes of both CTAs; wait
+                    // (bounded) for the loads of the last `stages` k-blocks to land.
+                    const uint32_t first = it > stages ? it - stages : 0u;
+                    for (uint32_t i = first; i < it; ++i) {
+                        if (p.inject == kInjectSkipFirstStage && i == 0) continue;
+                        drain_bar(smem_addr(&full[i % stages]), (i / stages) & 1u, tmo);
                     }
                 }
             }
-            if (!ok && leader) {
-                // Drain: the leader's full barriers count the bytes of both CTAs; wait
-                // (bounded) for the loads of the last STAGES k-blocks to land.
-                const uint32_t first = it > STAGES ? it - STAGES : 0u;
-                for (uint32_t i = first; i < it; ++i) {
-                    if (p.inject == kInjectSkipFirstStage && i == 0) continue;
-                    drain_bar(smem_addr(&full[i % STAGES]), (i / STAGES) & 1u, tmo);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (leader CTA)
-        if (lane == 0 && leader) {
-            uint32_t it = 0;
-            bool ok = true;
-            bool issued = false;
-            int32_t local = 0;
-            for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
-                const int32_t tile = w / p.splits;
-                const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
-                const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
-                const uint32_t b = local & 1;
-                const uint32_t aph = (local >> 1) & 1u;
-                if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, tmo, kRoleMma, 0x100u | b)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s)) {
+            __syncwarp();
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer (leader CTA)
+            if (lane == 0 && leader) {
+                uint32_t it = 0;
+                uint32_t s = 0, ph = 0;  // ring slot and phase of k-block `it`
+                bool ok = true;
+                bool issued = false;
+                int32_t local = 0;
+                for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
+                    const int32_t tile = w / p.splits;
+                    const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
+                    const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
+                    const uint32_t b = local & 1;
+                    const uint32_t aph = (local >> 1) & 1u;
+                    if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, tmo, kRoleMma, 0x100u | b)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = smem_addr(ring + s * S::kStageBytes);
-                    const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
-                    const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + S::kABytes);
-#pragma unroll
-                    for (int j = 0; j < kBK / 16; ++j) {
-                        // +32 bytes along K per 16-element slice: +2 in the >>4-encoded address
-                        const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
-                        mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, S::kIdesc, acc);
+                    const uint32_t d_tmem = tmem_base + b * kAccStride;
+                    for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
+                        if (it > 0 && ++s == stages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_addr = smem_addr(ring + s * S::kStageBytes);
+                        const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
+                        const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + S::kABytes);
+    #pragma unroll
+                        for (int j = 0; j < kBK / 16; ++j) {
+                            // +32 bytes along K per 16-element slice: +2 in the >>4-encoded address
+                            const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
+                            mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, S::kIdesc, acc);
+                        }
+                        issued = true;
+                        if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
+                        else mma_commit<1>(smem_addr(&empty[s]));
                     }
-                    issued = true;
-                    if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
-                    else mma_commit<1>(smem_addr(&empty[s]));
+                    if (!ok) break;
+                    if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), 0x3);
+                    else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
                 }
-                if (!ok) break;
-                if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), 0x3);
-                else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
+                if (!ok && issued) {
+                    // Drain: every MMA issued so far must finish before TMEM is freed.
+                    mma_commit<CG>(smem_addr(&ctl->drain));
+                    drain_bar(smem_addr(&ctl->drain), 0, tmo);
+                }
             }
-            if (!ok && issued) {
-                // Drain: every MMA issued so far must finish before TMEM is freed.
-                mma_commit<CG>(smem_addr(&ctl->drain));
-                drain_bar(smem_addr(&ctl->drain), 0, tmo);
-            }
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp >= kEpiWarp0) {
+    } else {
+        if constexpr (W::kRealloc) setmaxnreg_inc<W::kRegsEpilogue>();
         // ------------------------------------------------------------ epilogue (every CTA)
-        const int q = warp - kEpiWarp0;  // == warp % 4: this warp's TMEM lane quadrant
+        const int e = warp - kEpiWarp0;  // epilogue warp index: staging buffers, counters
+        const int q = e & 3;              // == warp % 4: this warp's TMEM lane quadrant
+        const int g = e >> 2;             // chunk phase: chunks g, g + kEpiGroups, ...
+        constexpr int kChunks = BN / kDChunk;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const int32_t slab_row = static_cast<int32_t>(rank) * kBM + q * 32 + lane;  // row within the tile
         constexpr int64_t kPartFloats = static_cast<int64_t>(S::kTileM) * BN;       // one partial accumulator
         uint32_t dcount = 0;
         int32_t local = 0;
+
+        // R by TMA (linear, no split): a cursor over this warp's future (tile, chunk)
+        // pairs keeps up to two 32x32 R boxes in flight ahead of their use, so the
+        // loads for the next tile overlap the current tile's MMAs.
+        const bool r_tma = (NUM_B == 1) && (p.flags & kFlagRTma);
+        // transpose buffer for unaligned R rows (the R boxes are unused then)
+        uint8_t* tbuf_r = NUM_B == 1 ? rstage + e * 2 * kDStageBytes : nullptr;
+        int32_t rc_w = unit, rc_c = g, rc_mb = -1, rc_nb = -1;
+        uint32_t r_issued = 0, r_used = 0, r_phase = 0;
+        auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
+            while (rc_w < num_work) {
+                if (rc_mb < 0) tile_coords(rc_w, p, rc_mb, rc_nb);
+                const int32_t r0 = rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;
+                if (rc_c < kChunks && r0 < p.m && rc_nb * BN + rc_c * kDChunk < p.n) return true;
+                rc_c += kEpiGroups;
+                if (rc_c >= kChunks) {
+                    rc_c = g;
+                    rc_w += units;
+                    rc_mb = -1;
+                }
+            }
+            return false;
+        };
+        auto r_issue = [&]() {
+            if (!r_tma || !r_find()) return;
+            const uint32_t buf = r_issued & 1u;
+            if (lane == 0) {
+                const uint32_t bar = smem_addr(&rbar[e * 2 + buf]);
+                mbar_arrive_expect_tx(bar, kDStageBytes);
+                tma_load_2d(smem_addr(rstage + (e * 2 + buf) * kDStageBytes), &p.tm_r, bar,
+                            rc_nb * BN + rc_c * kDChunk, rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32);
+            }
+            ++r_issued;
+            rc_c += kEpiGroups;
+            if (rc_c >= kChunks) {
+                rc_c = g;
+                rc_w += units;
+                rc_mb = -1;
+            }
+        };
+        r_issue();
+        r_issue();
+
         for (int32_t w = unit; w < num_work; w += units, ++local) {
             const uint32_t b = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
@@ -505,10 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
             const bool warp_rows = row0 < p.m;
             const uint32_t tcol = tmem_base + lane_base + b * kAccStride;
             const bool split_mode = p.splits > 1;
-            float* part = p.ws + static_cast<int64_t>(w) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
+            // this slab's rows of the tile's fp32 accumulator (split-K only)
+            float* acc_ws = p.ws + static_cast<int64_t>(tile) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
 
 #pragma unroll 1
-            for (int c = 0; c < BN / kDChunk; ++c) {
+            for (int c = g; c < kChunks; c += kEpiGroups) {
                 const int32_t n0 = nb * BN + c * kDChunk;
                 const bool chunk_on = warp_rows && n0 < p.n;
                 float v[32];
@@ -520,8 +731,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                         tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
                         tmem_wait_ld();
                         if (split_mode) {
-                            st_global_f32x32(part + c * kDChunk, r0);
-                            st_global_f32x32(part + kPartFloats + c * kDChunk, r1);
+                            if (m < p.m) {
+                                red_add_f32x32(acc_ws + c * kDChunk, r0);
+                                red_add_f32x32(acc_ws + kPartFloats + c * kDChunk, r1);
+                            }
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
@@ -529,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                     } else {
                         tmem_wait_ld();
                         if (split_mode) {
-                            st_global_f32x32(part + c * kDChunk, r0);
+                            if (m < p.m) red_add_f32x32(acc_ws + c * kDChunk, r0);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
@@ -539,8 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
-                if (c == BN / kDChunk - 1) {
-                    // All TMEM reads of this buffer are done: hand it back to the MMA issuer.
+                if (c + kEpiGroups >= kChunks) {
+                    // This warp's TMEM reads of this buffer are done: hand it back to the MMA issuer.
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
@@ -549,49 +762,67 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_persistent_kernel(const __gr
                     }
                 }
                 if (!chunk_on || split_mode) continue;
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, q, dstage, dcount);
+                uint32_t rbox = 0;
+                if (r_tma) {
+                    const uint32_t buf = r_used & 1u;
+                    const uint32_t bar = smem_addr(&rbar[e * 2 + buf]);
+                    const uint32_t par = (r_phase >> buf) & 1u;
+                    bool rok = true;
+                    if (lane == 0) rok = wait_bar(bar, par, abort_flag, tmo, kRoleEpilogue, 0x200u | buf);
+                    rok = __shfl_sync(0xffffffffu, rok, 0);
+                    if (!rok) break;
+                    while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
+                    }
+                    r_phase ^= 1u << buf;
+                    rbox = smem_addr(rstage + (e * 2 + buf) * kDStageBytes);
+                }
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, e, dstage, dcount, rbox, tbuf_r);
+                if (r_tma) {
+                    __syncwarp();  // every lane has read the box: refill its buffer
+                    fence_proxy_async_smem();
+                    ++r_used;
+                    r_issue();
+                }
             }
+            if (*abort_flag) break;
             if (!split_mode || !warp_rows) continue;
 
-            // split-K: publish this partial; the last split of this slab reduces all of them.
+            // split-K: this partial is in the accumulator; the last split of the slab finishes it.
             __threadfence();
             __syncwarp();
-            uint32_t* cnt = p.ws_cnt + tile * (4 * S::kCG) + static_cast<int32_t>(rank) * 4 + q;
+            uint32_t* cnt = p.ws_cnt + tile * S::kSlabs + static_cast<int32_t>(rank) * kEpiWarps + e;
             uint32_t arrived = 0;
             if (lane == 0) arrived = atomicAdd(cnt, 1u);
             arrived = __shfl_sync(0xffffffffu, arrived, 0);
             if (arrived != static_cast<uint32_t>(p.splits - 1)) continue;
             __threadfence();
-            const float* base = p.ws + static_cast<int64_t>(tile) * p.splits * NUM_B * kPartFloats +
-                                static_cast<int64_t>(slab_row) * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN / kDChunk; ++c) {
+            for (int c = g; c < kChunks; c += kEpiGroups) {
                 const int32_t n0 = nb * BN + c * kDChunk;
                 if (n0 >= p.n) break;
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                add_f32x32_cg(v, acc_ws + c * kDChunk);
                 if (NUM_B == 2) {
                     float v3[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v3[j] = 0.0f;
-                    for (int32_t sp = 0; sp < p.splits; ++sp) {
-                        const float* src = base + static_cast<int64_t>(sp) * NUM_B * kPartFloats + c * kDChunk;
-                        add_f32x32_cg(v, src);
-                        add_f32x32_cg(v3, src + kPartFloats);
-                    }
+                    add_f32x32_cg(v3, acc_ws + kPartFloats + c * kDChunk);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = silu(v[j]) * v3[j];
-                } else {
-                    for (int32_t sp = 0; sp < p.splits; ++sp)
-                        add_f32x32_cg(v, base + static_cast<int64_t>(sp) * kPartFloats + c * kDChunk);
                 }
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, q, dstage, dcount);
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, e, dstage, dcount, 0u, tbuf_r);
             }
-            if (lane == 0) atomicExch(cnt, 0u);  // ready for the next launch
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if (lane == 0) {
+            // R boxes still in flight after an early stop: wait (bounded) for them to land.
+            for (uint32_t i = r_used; i < r_issued; ++i)
+                drain_bar(smem_addr(&rbar[e * 2 + (i & 1u)]), (r_phase >> (i & 1u)) & 1u, tmo);
+            bulk_wait_group<0>();
+        }
         __syncwarp();
+
     }
 
     // ---------------------------------------------------------------- teardown

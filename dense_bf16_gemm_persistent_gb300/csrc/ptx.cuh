@@ -266,6 +266,21 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- register reallocation
+
+// All warps of a warpgroup: lower (dec) or raise (inc) this warp's register
+// budget to N.  An inc waits until the CTA's pool (threads x registers at
+// launch) has N registers per thread free, so the warpgroups' budgets must sum
+// to at most that pool.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- misc
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {

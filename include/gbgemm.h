@@ -101,6 +101,24 @@ GB_API gb_status_t gb_gemm_linear(const void* A, int64_t lda, const void* B, int
                            void* stream);
 
 /*
+ * gb_gemm_linear with a second output: Z = bf16(A . B^T + bias), the
+ * pre-activation a backward pass of the activation needs, stored from the
+ * same epilogue pass; D as in gb_gemm_linear.  Both outputs leave through the
+ * same per-warp staging boxes, each box rewritten only after the store that
+ * used it has read it ("Automate performant Hopper matmul", section "TMA store
+ * and stmatrix": reuse shared memory for TMA stores of several outputs by
+ * waiting for the earlier stores).
+ *   Z  [M,N] with leading dimension ldz (elements); required if M,N > 0; any
+ *      2-byte alignment (TMA when 16-byte aligned rows, else the transpose
+ *      path); must not overlap A, B, bias, R or D.
+ * Errors and limits as gb_gemm_linear.
+ */
+GB_API gb_status_t gb_gemm_linear_preact(const void* A, int64_t lda, const void* B, int64_t ldb,
+                                         const void* bias, const void* R, int64_t ldr, int act,
+                                         void* D, int64_t ldd, void* Z, int64_t ldz,
+                                         int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * D = bf16( silu(X . W1^T) * (X . W3^T) ): the Llama-FFN horizontal fusion,
  * two products sharing the X operand, both fp32-accumulated before the
  * epilogue ("Translate MmaOp patterns properly on Hopper", commit "Fix llama
@@ -119,18 +137,21 @@ GB_API gb_status_t gb_gemm_ffn_gated(const void* X, int64_t ldx, const void* W1,
  *
  * The k-blocks of every output tile are cut into `splits` contiguous ranges;
  * each (tile, range) is one work item of the persistent kernel.  Every range
- * writes its fp32 partial accumulator to the workspace; the last range to
- * finish a 32-row slab of a tile (a per-slab counter in the workspace) sums
- * the partials in range order -- so the result is deterministic -- and applies
- * the same epilogue as the non-split call.  Results equal a sequential fp32
- * sum up to rounding, like every other call.
+ * adds its fp32 partial accumulator into the tile's fp32 accumulator in the
+ * workspace (fp32 reductions performed in L2); the last range to finish a
+ * 32-row slab of a tile (a per-slab counter in the workspace) reads the sum
+ * and applies the same epilogue as the non-split call.  The order of the fp32
+ * additions across ranges is not fixed, so two calls may differ by rounding;
+ * results equal a sequential fp32 sum up to rounding, like every other call
+ * (inputs whose partial sums are exact give identical bits).
  *   splits     <= 0: chosen automatically (1 when the tiles already fill the
  *              GPU); otherwise clamped to [1, number of 64-wide k-blocks].
  *   workspace  device memory owned by the caller, 256-byte aligned, at least
- *              gb_splitk_workspace_bytes() bytes (may be NULL when that is 0).
- *              Its counters are cleared on `stream` by each call, so calls that
- *              share one workspace must be ordered on the GPU (same stream or
- *              events); overlapping calls on one workspace race.
+ *              gb_splitk_workspace_bytes() bytes (may be NULL when that is 0):
+ *              one fp32 accumulator tile per output tile plus the counters.
+ *              Each call clears it on `stream` first, so calls that share one
+ *              workspace must be ordered on the GPU (same stream or events);
+ *              overlapping calls on one workspace race.
  * Other arguments, errors and limits as gb_gemm_linear / gb_gemm_ffn_gated.
  * GB_ERR_INVALID_ARG if the workspace is missing, too small or misaligned.
  */
@@ -170,7 +191,7 @@ GB_API gb_status_t gb_splitk_workspace_bytes(int ffn, int64_t M, int64_t N, int6
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current and caches it; make that first
  * call before any stream capture.  Every call on a device shares the one array,
- * which keeps the previous call's contents: each call clears its counters on
+ * which keeps the previous call's contents: each call clears the part it uses on
  * `stream` first, and calls that overlap on the GPU (different streams without
  * ordering) race on the array.  Other arguments, errors and limits as
  * gb_gemm_linear_splitk.
@@ -204,7 +225,10 @@ GB_API const char* gb_last_error(void);
  * number of CTAs; 0 = one per SM), persistent (0 = one tile per CTA),
  * group (tile-swizzle group size along M, >= 1), zigzag (0, 1, or -1 = auto),
  * pair (1 = CTA pairs with 256-row tiles, 0 = single CTAs with 128-row tiles,
- * -1 = auto; the 128-wide linear tile always runs on single CTAs).
+ * -1 = auto; the 128-wide linear tile always runs on single CTAs), stages
+ * (depth of the operand ring, >= 2; 0 = the deepest that fits in shared
+ * memory, which is one less when an epilogue input needs staging boxes), epi
+ * (epilogue warpgroups: 1 or 2; 0 = auto: two for epilogue-bound shapes).
  * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
  */
 GB_API gb_status_t gb_set_config(const char* spec);

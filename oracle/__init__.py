@@ -66,6 +66,8 @@ class Oracle:
         i64, p = ctypes.c_int64, ctypes.c_void_p
         lib.oracle_linear_f32.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64]
         lib.oracle_linear_f64.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64]
+        lib.oracle_linear_preact_f32.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, p, i64,
+                                                 i64, i64, i64]
         lib.oracle_ffn_f32.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64]
         lib.oracle_ffn_f64.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64]
         lib.oracle_acc_f32.argtypes = [p, i64, p, i64, p, i64, i64, i64, i64]
@@ -74,7 +76,8 @@ class Oracle:
         lib.oracle_f32_to_bf16_array.argtypes = [p, p, i64]
         lib.oracle_f64_to_bf16_array.argtypes = [p, p, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
-        for name in ("oracle_linear_f32", "oracle_linear_f64", "oracle_ffn_f32", "oracle_ffn_f64",
+        for name in ("oracle_linear_f32", "oracle_linear_f64", "oracle_linear_preact_f32", "oracle_ffn_f32",
+                     "oracle_ffn_f64",
                      "oracle_acc_f32", "oracle_act_f32_array", "oracle_act_f64_array",
                      "oracle_f32_to_bf16_array", "oracle_f64_to_bf16_array"):
             getattr(lib, name).restype = None
@@ -103,6 +106,19 @@ class Oracle:
         pr, ldr = _mat(R, "R")
         self.lib.oracle_linear_f32(pa, lda, pb, ldb, pbias, pr, ldr, ACT[act], D.ctypes.data, N, M, N, K)
         return D
+
+    def linear_preact(self, A, B, bias=None, R=None, act: str = "none"):
+        """(D, Z): D as in linear(), Z[M,N] = bf16(A.B^T + bias), the pre-activation."""
+        M, N, K = self._dims(A, B)
+        D = np.empty((M, N), dtype=np.uint16)
+        Z = np.empty((M, N), dtype=np.uint16)
+        pa, lda = _mat(A, "A")
+        pb, ldb = _mat(B, "B")
+        pbias, _ = _mat(bias, "bias")
+        pr, ldr = _mat(R, "R")
+        self.lib.oracle_linear_preact_f32(pa, lda, pb, ldb, pbias, pr, ldr, ACT[act], D.ctypes.data, N,
+                                          Z.ctypes.data, N, M, N, K)
+        return D, Z
 
     def linear_f64(self, A, B, bias=None, R=None, act: str = "none"):
         """The same expression in float64, unrounded (diagnostic / error bounds)."""
@@ -188,6 +204,10 @@ def linear(A, B, bias=None, R=None, act: str = "none"):
 
 def linear_f64(A, B, bias=None, R=None, act: str = "none"):
     return default().linear_f64(A, B, bias, R, act)
+
+
+def linear_preact(A, B, bias=None, R=None, act: str = "none"):
+    return default().linear_preact(A, B, bias, R, act)
 
 
 def ffn_gated(X, W1, W3):

@@ -21,6 +21,7 @@
  *               the product of two bf16 values is exact in fp32.
  *   linear :   v = acc;  v += f32(bias[n]) if bias;  v = act(v);
  *              v += f32(R[m][n]) if R;  D[m][n] = bf16_rne(v)
+ *              optional second output (pre-activation): Z[m][n] = bf16_rne(acc + bias)
  *   ffn    :   a1 = acc(X, W1);  a3 = acc(X, W3);
  *              D[m][n] = bf16_rne( silu(a1) * a3 )
  *
@@ -183,6 +184,25 @@ void oracle_linear_f32(const uint16_t* A, int64_t lda, const uint16_t* B, int64_
         for (int64_t n = 0; n < N; ++n) {
             float v = dot_f32(A + m * lda, B + n * ldb, K);
             if (bias) v = v + bf16_to_f32(bias[n]);
+            v = act_f32(act, v);
+            if (R) v = v + bf16_to_f32(R[m * ldr + n]);
+            D[m * ldd + n] = f32_to_bf16(v);
+        }
+    }
+}
+
+/* The same, also writing the pre-activation Z[m][n] = bf16_rne(acc + bias) (the
+ * value a backward pass of the activation needs), before act and R. */
+void oracle_linear_preact_f32(const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                              const uint16_t* bias, const uint16_t* R, int64_t ldr, int act,
+                              uint16_t* D, int64_t ldd, uint16_t* Z, int64_t ldz,
+                              int64_t M, int64_t N, int64_t K) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            float v = dot_f32(A + m * lda, B + n * ldb, K);
+            if (bias) v = v + bf16_to_f32(bias[n]);
+            Z[m * ldz + n] = f32_to_bf16(v);
             v = act_f32(act, v);
             if (R) v = v + bf16_to_f32(R[m * ldr + n]);
             D[m * ldd + n] = f32_to_bf16(v);

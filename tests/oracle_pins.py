@@ -292,7 +292,30 @@ def check_leading_dims(o) -> None:
     np.testing.assert_array_equal(o.linear(A, B), o.linear(np.ascontiguousarray(A), np.ascontiguousarray(B)))
 
 
+def check_preact_output(o) -> None:
+    """The second output is the pre-activation bf16(acc + bias): exact on integer
+    operands (so a ReLU that clips negatives shows whether it was taken before or
+    after the activation), and D is unchanged by asking for it."""
+    rng = np.random.default_rng(19)
+    M, N, K = 9, 14, 32
+    A, a = int_bf16(rng, (M, K))
+    B, b = int_bf16(rng, (N, K))
+    bias, bv = int_bf16(rng, (N,), -5, 5)
+    R, rv = int_bf16(rng, (M, N), -2, 2)
+    D, Z = o.linear_preact(A, B, bias=bias, R=R, act="relu")
+    pre = a @ b.T + bv[None, :]
+    assert (pre < 0).any()
+    np.testing.assert_array_equal(Z, lib_round_bf16(pre.astype(np.float32)))
+    np.testing.assert_array_equal(D, lib_round_bf16((np.maximum(pre, 0) + rv).astype(np.float32)))
+    np.testing.assert_array_equal(D, o.linear(A, B, bias=bias, R=R, act="relu"))
+    A2 = rand_bf16(rng, (M, K))
+    B2 = rand_bf16(rng, (N, K), 0.3)
+    D2, Z2 = o.linear_preact(A2, B2, act="none")
+    np.testing.assert_array_equal(D2, Z2)
+
+
 ALL_CHECKS = [check_f32_to_bf16, check_f64_to_bf16, check_acc_error_bound, check_integer_exact,
               check_transpose_and_index, check_identity_b, check_zero_bias_and_linearity,
               check_bias_broadcast_and_residual, check_k_zero, check_activation_closed_forms,
-              check_activation_vs_library, check_epilogue_order, check_ffn, check_leading_dims]
+              check_activation_vs_library, check_epilogue_order, check_ffn, check_leading_dims,
+              check_preact_output]

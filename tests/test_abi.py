@@ -96,10 +96,10 @@ def test_ffn_rejects(L, args, needle):
 
 
 def test_config_parser(L):
-    assert L.gb_set_config(b"bn=128,grid=4,persistent=0,group=8,zigzag=1") == GB_OK
+    assert L.gb_set_config(b"bn=128,grid=4,persistent=0,group=8,zigzag=1,pair=1,stages=3") == GB_OK
     assert L.gb_set_config(None) == GB_OK
     assert L.gb_set_config(b"") == GB_OK
-    for bad in (b"bn=96", b"nope=1", b"grid", b"group=0", b"zigzag=2", b"bn=12x"):
+    for bad in (b"bn=96", b"nope=1", b"grid", b"group=0", b"zigzag=2", b"bn=12x", b"pair=2", b"stages=-1"):
         assert L.gb_set_config(bad) == GB_ERR_INVALID_ARG, bad
     assert L.gb_set_config(None) == GB_OK
 
@@ -137,3 +137,17 @@ def test_splitk_entry_points_validate_first(L):
     # empty problems need no workspace and no device
     assert L.gb_gemm_linear_splitk(None, 0, None, 0, None, None, 0, 0, None, 0, 0, 5, 7, 0, None, 0,
                                    None) == GB_OK
+
+
+def test_preact_entry_point_validates_first(L):
+    args = dict(A=P16, lda=64, B=P16, ldb=64, bias=None, R=None, ldr=0, act=0, D=P16, ldd=32, M=16, N=32, K=64)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.gb_gemm_linear_preact(a["A"], a["lda"], a["B"], a["ldb"], a["bias"], a["R"], a["ldr"], a["act"],
+                                       a["D"], a["ldd"], kw.get("Z", P16), kw.get("ldz", 32), a["M"], a["N"], a["K"],
+                                       None)
+    assert call(Z=None) == GB_ERR_INVALID_ARG and b"Z is null" in L.gb_last_error()
+    assert call(ldz=16) == GB_ERR_INVALID_ARG and b"ldz" in L.gb_last_error()
+    assert call(Z=P1) == GB_ERR_UNSUPPORTED
+    assert L.gb_gemm_linear_preact(None, 0, None, 0, None, None, 0, 0, None, 0, None, 0, 0, 4, 4, None) == GB_OK

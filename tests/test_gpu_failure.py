@@ -14,15 +14,16 @@ from tests.gpu_util import assert_close, bits
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("epi", [1, 2])
 @pytest.mark.parametrize("kind", ["linear", "ffn"])
 @pytest.mark.parametrize("pair", [0, 1])
-def test_wait_timeout_is_reported_and_context_survives(kind, pair):
+def test_wait_timeout_is_reported_and_context_survives(kind, pair, epi):
     M, N, K = 512, 768, 1024
     A = inputs.randn_bf16((M, K), seed=1).cuda()
     B = inputs.randn_bf16((N, K), seed=2, std=1.0 / np.sqrt(K)).cuda()
     B3 = inputs.randn_bf16((N, K), seed=3, std=1.0 / np.sqrt(K)).cuda()
     gb.device_status()
-    gb.set_config(f"pair={pair}")
+    gb.set_config(f"pair={pair},epi={epi}")
     gb.set_wait_timeout_ns(100_000_000)  # 0.1 s
     gb.set_fault_injection(1)
     try:

@@ -94,13 +94,13 @@ def test_epilogue_variants(act, with_bias, with_r):
 
 def test_unaligned_d_and_r_use_plain_loads_and_stores():
     """N = 4099: rows of D and R are 8198 bytes apart (not a multiple of 16), so the
-    kernel takes the predicated st.global / scalar-load path."""
+    kernel moves them through its shared-memory transpose with plain loads/stores."""
     M, N, K = 200, 4099, 128
     A = inputs.randn_bf16((M, K), seed=30)
     B = inputs.randn_bf16((N, K), seed=31, std=1.0 / np.sqrt(K))
     R = inputs.randn_bf16((M, N), seed=32)
     got = run_linear(A, B, None, R)
-    assert "d_store=st.global" in gb.last_plan()
+    assert "d_store=st.transposed" in gb.last_plan() and "r_load=ld.transposed" in gb.last_plan()
     assert_close(got, ref_linear(A, B, None, R), "N=4099")
 
 
@@ -153,10 +153,11 @@ def test_empty_outputs():
     assert gb.linear(B, A).shape == (32, 0)
 
 
+@pytest.mark.parametrize("epi", [1, 2])
 @pytest.mark.parametrize("pair", [-1, 0, 1])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 500, 200), (1, 7, 8), (257, 129, 1000)])
-def test_ffn_gated(M, N, K, pair):
-    gb.set_config(f"pair={pair}")
+def test_ffn_gated(M, N, K, pair, epi):
+    gb.set_config(f"pair={pair},epi={epi}")
     X = inputs.randn_bf16((M, K), seed=70)
     W1 = inputs.randn_bf16((N, K), seed=71, std=1.0 / np.sqrt(K))
     W3 = inputs.randn_bf16((N, K), seed=72, std=1.0 / np.sqrt(K))
@@ -184,7 +185,9 @@ def test_ffn_integer_bit_exact_when_gate_is_relu_like():
 @pytest.mark.parametrize("spec", ["bn=128", "bn=256", "persistent=0", "grid=3", "grid=1", "group=1",
                                   "group=3,grid=5", "bn=128,grid=7,group=2", "pair=0", "pair=1",
                                   "pair=1,grid=2", "pair=1,persistent=0", "pair=0,grid=5,group=2",
-                                  "pair=1,group=1,grid=6"])
+                                  "pair=1,group=1,grid=6", "stages=2", "stages=3,pair=1,grid=3",
+                                  "stages=4,pair=0", "stages=16", "epi=1", "epi=2", "epi=1,pair=0,grid=3",
+                                  "epi=2,pair=1,grid=2,stages=3"])
 def test_config_overrides_give_identical_bits(spec):
     """Tile size, grid, swizzle and persistence change which CTA computes a tile but not
     the per-element accumulation order within the tile: identical bits."""
@@ -240,3 +243,95 @@ def test_repeated_calls_and_streams():
     gb.device_status(s)
     for o in outs:
         assert_close(bits(o), ref, "repeat")
+
+
+@pytest.mark.parametrize("spec", ["", "grid=1", "grid=3", "pair=0,grid=2", "pair=1,grid=2", "bn=128,grid=3",
+                                  "persistent=0", "epi=1,grid=2", "epi=2,grid=2", "epi=1,pair=0"])
+@pytest.mark.parametrize("M,N", [(700, 904), (129, 264), (1, 8), (520, 1000)])
+def test_residual_by_tma(spec, M, N):
+    """R with 16-byte aligned rows is prefetched by TMA; a small grid makes each
+    epilogue warp's prefetch run across many tiles."""
+    gb.set_config(spec or None)
+    K = 192
+    A = inputs.randn_bf16((M, K), seed=110)
+    B = inputs.randn_bf16((N, K), seed=111, std=0.1)
+    bias = inputs.randn_bf16((N,), seed=112, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=113)
+    got = run_linear(A, B, bias, R, "gelu_tanh")
+    assert "r_load=tma" in gb.last_plan(), gb.last_plan()
+    assert_close(got, ref_linear(A, B, bias, R, "gelu_tanh"), f"{spec} {M}x{N}")
+
+
+def test_residual_by_tma_aliasing_d():
+    M, N, K = 600, 520, 128
+    A = inputs.randn_bf16((M, K), seed=120)
+    B = inputs.randn_bf16((N, K), seed=121, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=122)
+    ref = ref_linear(A, B, None, R, "relu")
+    gb.set_config("grid=2")
+    RD = R.to(DEV).clone()
+    gb.linear(A.to(DEV), B.to(DEV), None, RD, act="relu", out=RD)
+    gb.device_status()
+    assert "r_load=tma" in gb.last_plan()
+    assert_close(bits(RD), ref, "D == R by TMA")
+
+
+@pytest.mark.parametrize("spec", ["", "pair=0", "grid=3", "epi=1", "epi=1,pair=0,grid=2"])
+@pytest.mark.parametrize("M,N", [(300, 4099), (33, 1001), (129, 17), (257, 263)])
+def test_unaligned_rows_all_epilogues(spec, M, N):
+    """Odd N (rows only 2-byte aligned): D and R through the transpose, every row and
+    column tail, with bias and activation, and D written into a strided view."""
+    gb.set_config(spec or None)
+    K = 136
+    A = inputs.randn_bf16((M, K), seed=130)
+    B = inputs.randn_bf16((N, K), seed=131, std=0.1)
+    bias = inputs.randn_bf16((N,), seed=132, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=133)
+    Dbig = torch.zeros((M, N + 3), dtype=torch.bfloat16, device=DEV)
+    D = Dbig[:, 1:1 + N]
+    gb.linear(A.to(DEV), B.to(DEV), bias.to(DEV), R.to(DEV), act="silu", out=D)
+    gb.device_status()
+    assert "st.transposed" in gb.last_plan()
+    assert_close(bits(D), ref_linear(A, B, bias, R, "silu"), f"{spec} {M}x{N}")
+    assert torch.all(Dbig[:, 0] == 0) and torch.all(Dbig[:, 1 + N:] == 0)
+
+
+@pytest.mark.parametrize("spec", ["", "epi=1", "epi=2", "pair=0,grid=3", "pair=1,grid=2,epi=1"])
+@pytest.mark.parametrize("act", ["gelu_tanh", "relu"])
+@pytest.mark.parametrize("d_off,z_off", [(0, 0), (0, 1), (1, 0), (1, 1)], ids=["dz_tma", "z_transp", "d_transp",
+                                                                               "both_transp"])
+def test_preact_second_output(spec, act, d_off, z_off):
+    """Z = bf16(A.B^T + bias) next to D = bf16(act(.) + R); outputs offset by one element
+    (rows no longer 16-byte aligned) take the shared-memory transpose path."""
+    gb.set_config(spec or None)
+    M, N, K = 333, 520, 200
+    A = inputs.randn_bf16((M, K), seed=140)
+    B = inputs.randn_bf16((N, K), seed=141, std=0.1)
+    bias = inputs.randn_bf16((N,), seed=142, std=0.5)
+    R = inputs.randn_bf16((M, N), seed=143)
+    Dbuf = torch.zeros((M, N + 8), dtype=torch.bfloat16, device=DEV)
+    Zbuf = torch.zeros((M, N + 8), dtype=torch.bfloat16, device=DEV)
+    D, Z = Dbuf[:, d_off:d_off + N], Zbuf[:, z_off:z_off + N]
+    gb.linear_preact(A.to(DEV), B.to(DEV), bias.to(DEV), R.to(DEV), act=act, out=D, preact=Z)
+    gb.device_status()
+    plan = gb.last_plan()
+    assert ("z_store=tma" in plan) == (z_off == 0) and ("d_store=tma" in plan) == (d_off == 0), plan
+    ref_d, ref_z = oracle.linear_preact(bits(A), bits(B), bits(bias), bits(R), act)
+    assert_close(bits(D), ref_d, f"D {spec}")
+    assert_close(bits(Z), ref_z, f"Z {spec}")
+
+
+def test_preact_integer_exact_and_k_zero():
+    M, N, K = 200, 300, 64
+    A, B = int_tensor((M, K), 150), int_tensor((N, K), 151)
+    bias = int_tensor((N,), 152, -5, 5)
+    D, Z = gb.linear_preact(A.to(DEV), B.to(DEV), bias.to(DEV), act="relu")
+    gb.device_status()
+    ref_d, ref_z = oracle.linear_preact(bits(A), bits(B), bits(bias), None, "relu")
+    assert_bitexact(bits(D), ref_d, "D")
+    assert_bitexact(bits(Z), ref_z, "Z")
+    # K = 0: Z is the bias broadcast over rows
+    D0, Z0 = gb.linear_preact(torch.empty((M, 0), dtype=torch.bfloat16, device=DEV),
+                              torch.empty((N, 0), dtype=torch.bfloat16, device=DEV), bias.to(DEV), act="gelu_tanh")
+    gb.device_status()
+    assert torch.equal(Z0.view(torch.int16), bias.to(DEV).view(torch.int16)[None, :].expand(M, N))

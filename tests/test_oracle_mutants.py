@@ -37,6 +37,10 @@ MUTANTS = [
     ("ffn_swap_gate", "float v = act_f32(ORACLE_ACT_SILU, a1) * a3;", "float v = act_f32(ORACLE_ACT_SILU, a3) * a1;", 0),
     ("ffn_same_weight", "float a3 = dot_f32(X + m * ldx, W3 + n * ldw3, K);", "float a3 = dot_f32(X + m * ldx, W1 + n * ldw1, K);", 0),
     ("ffn_f64_swap", "Y[m * ldy + n] = act_f64(ORACLE_ACT_SILU, a1) * a3;", "Y[m * ldy + n] = act_f64(ORACLE_ACT_SILU, a3) * a1;", 0),
+    ("preact_after_act", "            Z[m * ldz + n] = f32_to_bf16(v);\n            v = act_f32(act, v);",
+     "            v = act_f32(act, v);\n            Z[m * ldz + n] = f32_to_bf16(v);", 0),
+    ("preact_no_bias", "            if (bias) v = v + bf16_to_f32(bias[n]);\n            Z[m * ldz + n] = f32_to_bf16(v);",
+     "            Z[m * ldz + n] = f32_to_bf16(v);\n            if (bias) v = v + bf16_to_f32(bias[n]);", 0),
     ("f64_dot_drop", "for (int64_t k = 0; k < K; ++k) {\n        double p", "for (int64_t k = 1; k < K; ++k) {\n        double p", 0),
 ]
 
