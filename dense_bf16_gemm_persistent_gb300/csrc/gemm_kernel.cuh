@@ -121,7 +121,8 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     int32_t kb_per_split;
     float* ws;
     uint32_t* ws_cnt;
-    int32_t stages;  // depth of the operand ring (<= the variant's maximum)
+    int32_t stages;       // depth of the operand ring (<= the variant's maximum)
+    int32_t l2_prefetch;  // k-blocks ahead of the ring to prefetch into L2 (0: none)
 };
 
 struct SharedCtl {
@@ -544,6 +545,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const bool reverse = p.zigzag && (local & 1);
                     const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
                     const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
+                    // L2 prefetches only for boxes wholly inside A and B (K is a multiple of
+                    // 64 then too, since kp < nkb covers whole k-blocks below K rounded up).
+                    const bool pf_rows_ok = p.l2_prefetch > 0 && a_row + kBM <= p.m &&
+                                            (NUM_B == 1 ? b_row + S::kBRows : nb * BN + BN) <= p.n &&
+                                            p.k % kBK == 0;
                     for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
                         const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
                         if (kk > 0 || it > 0) {
@@ -561,6 +567,20 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const uint32_t own_full = smem_addr(&full[s]);
                         if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
                         uint8_t* sb = st + S::kABytes;
+                        if (pf_rows_ok && kk + p.l2_prefetch < nkb) {
+                            // Pull a later k-block of this tile into L2, so the ring's loads
+                            // for it find their data in L2 instead of waiting on DRAM.
+                            const int32_t kp = kb0 + (reverse ? nkb - 1 - (kk + p.l2_prefetch) : kk + p.l2_prefetch);
+                            tma_prefetch_l2_2d(&p.tm_a, kp * kBK, a_row);
+                            if (NUM_B == 1) {
+                                tma_prefetch_l2_2d(&p.tm_b0, kp * kBK, b_row);
+                            } else if constexpr (PAIR) {
+                                tma_prefetch_l2_2d(leader ? &p.tm_b0 : &p.tm_b1, kp * kBK, nb * BN);
+                            } else {
+                                tma_prefetch_l2_2d(&p.tm_b0, kp * kBK, nb * BN);
+                                tma_prefetch_l2_2d(&p.tm_b1, kp * kBK, nb * BN);
+                            }
+                        }
                         if constexpr (PAIR) {
                             const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
                             tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);
@@ -659,6 +679,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         // pairs keeps up to two 32x32 R boxes in flight ahead of their use, so the
         // loads for the next tile overlap the current tile's MMAs.
         const bool r_tma = (NUM_B == 1) && (p.flags & kFlagRTma);
+        const bool express = p.splits == 1 && p.num_k_blocks > 0 && (p.flags & kFlagDTma) &&
+                             !(p.flags & (kFlagResidual | kFlagZ));
         // transpose buffer for unaligned R rows (the R boxes are unused then)
         uint8_t* tbuf_r = NUM_B == 1 ? rstage + e * 2 * kDStageBytes : nullptr;
         int32_t rc_w = unit, rc_c = g, rc_mb = -1, rc_nb = -1;
@@ -714,6 +736,81 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             const int32_t m = row0 + lane;
             const bool warp_rows = row0 < p.m;
             const uint32_t tcol = tmem_base + lane_base + b * kAccStride;
+            if (express) {
+                // Express path (no epilogue input, no second output, TMA-stored D, no
+                // split): a compact loop, so the hot epilogue code next to the MMA
+                // issuer stays small.
+#pragma unroll 1
+                for (int c = g; c < kChunks; c += kEpiGroups) {
+                    const int32_t n0 = nb * BN + c * kDChunk;
+                    const bool chunk_on = warp_rows && n0 < p.n;
+                    float v[32];
+                    if (chunk_on) {
+                        uint32_t r0[32];
+                        tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
+                        if (NUM_B == 2) {
+                            uint32_t r1[32];
+                            tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                        } else {
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                        }
+                    }
+                    if (c + kEpiGroups >= kChunks) {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), 0));
+                            else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                        }
+                    }
+                    if (!chunk_on) continue;
+                    if (NUM_B == 1) {
+                        if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
+                        switch (p.act) {
+                            case 1:
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                                break;
+                            case 2:
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                                break;
+                            case 3:
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                                break;
+                            default:
+                                break;
+                        }
+                    }
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                    uint8_t* buf = dstage + (e * 2 + (dcount & 1u)) * kDStageBytes;
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this box has read it
+                    __syncwarp();
+                    const uint32_t row_addr = smem_addr(buf) + lane * 64;
+                    const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
+                                     packed[4 * u + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tm_d, smem_addr(buf), n0, row0);
+                        bulk_commit_group();
+                    }
+                    ++dcount;
+                }
+                continue;
+            }
+
             const bool split_mode = p.splits > 1;
             // this slab's rows of the tile's fp32 accumulator (split-K only)
             float* acc_ws = p.ws + static_cast<int64_t>(tile) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
