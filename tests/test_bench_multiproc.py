@@ -55,3 +55,32 @@ def test_reference_arm_rank_nonzero_exits_without_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """The reference arm (the CPU oracle on a bounded sample) prints one JSON line with
+    the keys the benchmark contract asks for."""
+    import json
+
+    import bench
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-step-s", "0.3",
+                       "--workload", "ragged:127,96,512"]) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["config"]["workload"] == "ragged_residual_127x96x512"
+
+
+def test_workload_names_and_bytes():
+    import bench
+    wl = bench.workload("mlp_gelu")
+    assert bench.flops_per_step(wl) == 2.0 * 8192 * 14336 * 4096
+    assert bench.algorithmic_bytes(wl) == 2.0 * (8192 * 4096 + 14336 * 4096 + 14336 + 8192 * 14336)
+    rg = bench.workload("ragged:127,96,64")
+    assert rg["residual"] and rg["split_k"] == "auto" and bench.needs_l2_flush(rg)
+    assert not bench.needs_l2_flush(wl)
