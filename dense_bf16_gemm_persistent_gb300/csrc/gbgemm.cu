@@ -53,7 +53,6 @@ struct Config {
     int pair = -1;       // -1 = heuristic, 0 = single CTAs, 1 = CTA pairs
     int stages = 0;      // 0 = the deepest ring that fits
     int epi = 0;         // epilogue warpgroups: 0 = heuristic, 1 or 2
-    int prefetch = -1;   // L2 prefetch distance in k-blocks: -1 = heuristic, 0 = off
 };
 
 std::mutex g_cfg_mu;
@@ -417,7 +416,6 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         int st = cfg.stages > 0 ? std::min(cfg.stages, deepest) : deepest;
         prm.stages = std::max(2, st);
     }
-    prm.l2_prefetch = cfg.prefetch >= 0 ? cfg.prefetch : 0;
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
     if (pr.k > 0) {
@@ -453,11 +451,10 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
 
     char plan[360];
     snprintf(plan, sizeof plan,
-             "kernel=%s pair=%d epi=%d tile=%dx%dx%d stages=%d prefetch=%d grid=%lld tiles=%d k_blocks=%d splits=%d "
+             "kernel=%s pair=%d epi=%d tile=%dx%dx%d stages=%d grid=%lld tiles=%d k_blocks=%d splits=%d "
              "group=%d zigzag=%d "
              "d_store=%s r_load=%s z_store=%s",
              pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kEpi, V::kTileM, bn, gb::kBK, prm.stages,
-             prm.l2_prefetch,
              static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, d_tma ? "tma" : "st.transposed",
              pr.r ? (r_tma ? "tma" : (flags & gb::kFlagRVec) ? "ld.v4" : "ld.transposed") : "none",
@@ -739,7 +736,6 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "pair" && v >= -1 && v <= 1) c.pair = static_cast<int>(v);
             else if (key == "stages" && v >= 0 && v <= 16) c.stages = static_cast<int>(v);
             else if (key == "epi" && v >= 0 && v <= 2) c.epi = static_cast<int>(v);
-            else if (key == "prefetch" && v >= -1 && v <= 64) c.prefetch = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

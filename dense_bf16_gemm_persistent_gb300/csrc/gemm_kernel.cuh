@@ -121,8 +121,7 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     int32_t kb_per_split;
     float* ws;
     uint32_t* ws_cnt;
-    int32_t stages;       // depth of the operand ring (<= the variant's maximum)
-    int32_t l2_prefetch;  // k-blocks ahead of the ring to prefetch into L2 (0: none)
+    int32_t stages;  // depth of the operand ring (<= the variant's maximum)
 };
 
 struct SharedCtl {
@@ -545,11 +544,6 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const bool reverse = p.zigzag && (local & 1);
                     const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
                     const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
-                    // L2 prefetches only for boxes wholly inside A and B (K is a multiple of
-                    // 64 then too, since kp < nkb covers whole k-blocks below K rounded up).
-                    const bool pf_rows_ok = p.l2_prefetch > 0 && a_row + kBM <= p.m &&
-                                            (NUM_B == 1 ? b_row + S::kBRows : nb * BN + BN) <= p.n &&
-                                            p.k % kBK == 0;
                     for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
                         const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
                         if (kk > 0 || it > 0) {
@@ -567,20 +561,6 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const uint32_t own_full = smem_addr(&full[s]);
                         if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
                         uint8_t* sb = st + S::kABytes;
-                        if (pf_rows_ok && kk + p.l2_prefetch < nkb) {
-                            // Pull a later k-block of this tile into L2, so the ring's loads
-                            // for it find their data in L2 instead of waiting on DRAM.
-                            const int32_t kp = kb0 + (reverse ? nkb - 1 - (kk + p.l2_prefetch) : kk + p.l2_prefetch);
-                            tma_prefetch_l2_2d(&p.tm_a, kp * kBK, a_row);
-                            if (NUM_B == 1) {
-                                tma_prefetch_l2_2d(&p.tm_b0, kp * kBK, b_row);
-                            } else if constexpr (PAIR) {
-                                tma_prefetch_l2_2d(leader ? &p.tm_b0 : &p.tm_b1, kp * kBK, nb * BN);
-                            } else {
-                                tma_prefetch_l2_2d(&p.tm_b0, kp * kBK, nb * BN);
-                                tma_prefetch_l2_2d(&p.tm_b1, kp * kBK, nb * BN);
-                            }
-                        }
                         if constexpr (PAIR) {
                             const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
                             tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);

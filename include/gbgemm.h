@@ -228,9 +228,7 @@ GB_API const char* gb_last_error(void);
  * -1 = auto; the 128-wide linear tile always runs on single CTAs), stages
  * (depth of the operand ring, >= 2; 0 = the deepest that fits in shared
  * memory, which is one less when an epilogue input needs staging boxes), epi
- * (epilogue warpgroups: 1 or 2; 0 = auto: two for epilogue-bound shapes),
- * prefetch (k-blocks ahead of the operand ring that the producer also pulls
- * into L2 with TMA prefetches; 0 = off, -1 = auto).
+ * (epilogue warpgroups: 1 or 2; 0 = auto: two for epilogue-bound shapes).
  * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
  */
 GB_API gb_status_t gb_set_config(const char* spec);
