@@ -53,6 +53,7 @@ struct Config {
     int pair = -1;       // -1 = heuristic, 0 = single CTAs, 1 = CTA pairs
     int stages = 0;      // 0 = the deepest ring that fits
     int epi = 0;         // epilogue warpgroups: 0 = heuristic, 1 or 2
+    int boxes = 0;       // staging boxes per epilogue warp (D, and R by TMA): 0 = heuristic, 2..8
 };
 
 std::mutex g_cfg_mu;
@@ -190,10 +191,11 @@ struct Variant {
         static bool ready[64] = {};
         static int units[64] = {};
         auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR, EPI>;
-        const uint32_t smem_max = S::smem_bytes(STAGES, false);
-        if (S::smem_bytes(2, NUM_B == 1) > info.smem_optin)
-            return fail(GB_ERR_UNSUPPORTED, "kernel needs %u bytes of shared memory, device allows %zu",
-                        S::smem_bytes(2, NUM_B == 1), info.smem_optin);
+        const uint32_t smem_max = S::smem_bytes(STAGES, 2, 0);
+        const uint32_t smem_min = S::smem_bytes(2, 2, NUM_B == 1 ? 2 : 0);
+        if (smem_min > info.smem_optin)
+            return fail(GB_ERR_UNSUPPORTED, "kernel needs %u bytes of shared memory, device allows %zu", smem_min,
+                        info.smem_optin);
         std::lock_guard<std::mutex> lk(mu);
         if (!ready[dev]) {
             const int attr_bytes = static_cast<int>(info.smem_optin);
@@ -225,11 +227,25 @@ struct Variant {
         return GB_OK;
     }
 
-    // The deepest ring (<= STAGES, >= 2) that fits next to the staging boxes.
-    static int max_stages(bool r_boxes, size_t smem_optin) {
-        int st = STAGES;
-        while (st > 2 && S::smem_bytes(st, r_boxes) > smem_optin) --st;
-        return st;
+    // Shared memory of one launch: the operand ring and the epilogue warps' box
+    // queues.  Long-K work items want the deepest ring (the MMAs must never wait
+    // for operands) and two boxes per warp; work items of at most 4 k-blocks are
+    // bound by the epilogue's global traffic, so they take a 3-stage ring and spend
+    // the rest on deeper D/R queues (more bytes in flight per SM).  `r_mode`: 0 no
+    // R boxes, 1 two boxes as the transpose buffer of unaligned R rows, 2 a queue
+    // of R boxes loaded by TMA.  Boxes shrink first, then the ring, down to 2 each.
+    struct Layout {
+        int stages, d_boxes, r_boxes;
+    };
+    static Layout choose_layout(int kb_per_item, int r_mode, const Config& cfg, size_t smem_optin) {
+        const bool short_k = kb_per_item <= 4;
+        int st = cfg.stages > 0 ? std::min(cfg.stages, STAGES) : (short_k ? std::min(3, STAGES) : STAGES);
+        st = std::max(2, st);
+        int boxes = cfg.boxes > 0 ? cfg.boxes : (short_k ? gb::kMaxBoxes : 2);
+        auto r_of = [&](int b) { return r_mode == 2 ? b : (r_mode == 1 ? 2 : 0); };
+        while (boxes > 2 && S::smem_bytes(st, boxes, r_of(boxes)) > smem_optin) --boxes;
+        while (st > 2 && S::smem_bytes(st, boxes, r_of(boxes)) > smem_optin) --st;
+        return Layout{st, boxes, r_of(boxes)};
     }
 
     static gb_status_t launch(const GemmParams& p, int units, cudaStream_t stream) {
@@ -238,7 +254,7 @@ struct Variant {
         cudaLaunchAttribute attr[1];
         cfg.gridDim = dim3(units * S::kCG, 1, 1);
         cfg.blockDim = dim3(S::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = S::smem_bytes(p.stages, NUM_B == 1 && (p.flags & gb::kFlagResidual));
+        cfg.dynamicSmemBytes = S::smem_bytes(p.stages, p.d_boxes, p.r_boxes);
         cfg.stream = stream;
         if (PAIR) {
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -412,9 +428,11 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.ldz = pr.ldz;
     prm.flags = flags;
     {
-        const int deepest = V::max_stages(!pr.ffn && pr.r, info.smem_optin);
-        int st = cfg.stages > 0 ? std::min(cfg.stages, deepest) : deepest;
-        prm.stages = std::max(2, st);
+        const int r_mode = r_tma ? 2 : (!pr.ffn && pr.r && !(flags & gb::kFlagRVec)) ? 1 : 0;
+        const auto lay = V::choose_layout(prm.kb_per_split, r_mode, cfg, info.smem_optin);
+        prm.stages = lay.stages;
+        prm.d_boxes = lay.d_boxes;
+        prm.r_boxes = lay.r_boxes;
     }
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
@@ -451,10 +469,11 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
 
     char plan[360];
     snprintf(plan, sizeof plan,
-             "kernel=%s pair=%d epi=%d tile=%dx%dx%d stages=%d grid=%lld tiles=%d k_blocks=%d splits=%d "
-             "group=%d zigzag=%d "
+             "kernel=%s pair=%d epi=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d k_blocks=%d "
+             "splits=%d group=%d zigzag=%d "
              "d_store=%s r_load=%s z_store=%s",
              pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kEpi, V::kTileM, bn, gb::kBK, prm.stages,
+             prm.d_boxes, prm.r_boxes,
              static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, d_tma ? "tma" : "st.transposed",
              pr.r ? (r_tma ? "tma" : (flags & gb::kFlagRVec) ? "ld.v4" : "ld.transposed") : "none",
@@ -736,6 +755,7 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "pair" && v >= -1 && v <= 1) c.pair = static_cast<int>(v);
             else if (key == "stages" && v >= 0 && v <= 16) c.stages = static_cast<int>(v);
             else if (key == "epi" && v >= 0 && v <= 2) c.epi = static_cast<int>(v);
+            else if (key == "boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.boxes = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

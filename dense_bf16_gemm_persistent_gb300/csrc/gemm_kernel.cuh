@@ -71,6 +71,10 @@ constexpr int kTmemCols = 512;    // two accumulator buffers of 256 columns
 constexpr int kAccStride = 256;
 constexpr int kDChunk = 32;       // epilogue chunk: 32 columns
 constexpr int kDStageBytes = 32 * kDChunk * 2;  // one warp's 32x32 bf16 staging box
+// Each epilogue warp owns a queue of D staging boxes (stores in flight) and, with
+// an epilogue input, a queue of R boxes (loads in flight); the depths are chosen
+// at launch, from 2 up to this.
+constexpr int kMaxBoxes = 8;
 
 enum : uint32_t {
     kFlagBias = 1u,
@@ -121,7 +125,9 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     int32_t kb_per_split;
     float* ws;
     uint32_t* ws_cnt;
-    int32_t stages;  // depth of the operand ring (<= the variant's maximum)
+    int32_t stages;   // depth of the operand ring (<= the variant's maximum)
+    int32_t d_boxes;  // D staging boxes per epilogue warp, 2..kMaxBoxes
+    int32_t r_boxes;  // R boxes per epilogue warp: 2..kMaxBoxes with an epilogue input (linear), else 0
 };
 
 struct SharedCtl {
@@ -311,16 +317,17 @@ __device__ __forceinline__ void add_rows_transposed(const GemmParams& p, float (
     __syncwarp();
 }
 
-// Store one 32x32 bf16 chunk of an output: by TMA from this warp's next staging
-// box (two boxes alternate; a box is rewritten only after the store that used it
-// has read it -- so several outputs share the boxes), or through the
-// shared-memory transpose when the output's rows are not 16-byte aligned.
+// Store one 32x32 bf16 chunk of an output: by TMA from the next box of this
+// warp's queue of d_boxes staging boxes (a box is rewritten only after the store
+// that used it has read it -- so several outputs share the queue), or through
+// the shared-memory transpose when the output's rows are not 16-byte aligned.
+// `dbox` is this warp's first box, `dslot` the queue position (wraps).
 __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorMap* tm, uint16_t* out, int64_t ld,
                                             bool by_tma, const uint32_t (&packed)[16], int32_t row0, int32_t n0,
-                                            int valid, int lane, int e, uint8_t* dstage, uint32_t& dcount) {
+                                            int valid, int lane, uint8_t* dbox, int32_t& dslot) {
     if (by_tma) {
-        uint8_t* buf = dstage + (e * 2 + (dcount & 1u)) * kDStageBytes;
-        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+        uint8_t* buf = dbox + dslot * kDStageBytes;
+        if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
         __syncwarp();
         // 64-byte rows, 16-byte units XOR-swizzled with (row / 2) % 4 (TMA 64B swizzle).
         const uint32_t row_addr = smem_addr(buf) + lane * 64;
@@ -335,9 +342,9 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorM
             tma_store_2d(tm, smem_addr(buf), n0, row0);
             bulk_commit_group();
         }
-        ++dcount;
+        if (++dslot == p.d_boxes) dslot = 0;
     } else {
-        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, dstage + e * 2 * kDStageBytes);
+        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, dbox);
     }
 }
 
@@ -346,10 +353,10 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorM
 template <int NUM_B>
 // `rbox` is the shared-memory address of this chunk's R box when R came by TMA
 // (0: read R from global memory); `tbuf_r` is this warp's transpose buffer for an
-// R whose rows are not 16-byte aligned; `e` indexes this warp's staging boxes.
-// Warp-collective.
+// R whose rows are not 16-byte aligned; `dbox`/`dslot` are this warp's D staging
+// queue and its position.  Warp-collective.
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32], int32_t m, int32_t row0,
-                                             int32_t n0, int lane, int e, uint8_t* dstage, uint32_t& dcount,
+                                             int32_t n0, int lane, uint8_t* dbox, int32_t& dslot,
                                              uint32_t rbox, uint8_t* tbuf_r) {
     const int valid = min(32, p.n - n0);
     if (NUM_B == 1) {
@@ -358,7 +365,7 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
             uint32_t zp[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) zp[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-            store_chunk(p, &p.tm_z, p.z, p.ldz, p.flags & kFlagZTma, zp, row0, n0, valid, lane, e, dstage, dcount);
+            store_chunk(p, &p.tm_z, p.z, p.ldz, p.flags & kFlagZTma, zp, row0, n0, valid, lane, dbox, dslot);
         }
         switch (p.act) {
             case 1:
@@ -390,7 +397,7 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
     uint32_t packed[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-    store_chunk(p, &p.tm_d, p.d, p.ldd, p.flags & kFlagDTma, packed, row0, n0, valid, lane, e, dstage, dcount);
+    store_chunk(p, &p.tm_d, p.d, p.ldd, p.flags & kFlagDTma, packed, row0, n0, valid, lane, dbox, dslot);
 }
 
 // 32 floats added into global memory with vector fp32 reductions (performed in L2).
@@ -442,13 +449,11 @@ struct KernelShape {
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTxBytes = kCG * kStageBytes;  // bytes the leader's full barrier waits for
-    static constexpr uint32_t kDStageTotal = kEpiWarps * 2 * kDStageBytes;
-    static constexpr uint32_t kRStageTotal = NUM_B == 1 ? kEpiWarps * 2 * kDStageBytes : 0;  // R boxes (linear)
-    static constexpr uint32_t kBarBytes = 2 * STAGES * 8 + 2 * kEpiWarps * 8;  // ring + 2 R barriers per warp
-    // Layout: [ring: stages x stage][D boxes][R boxes, only with an epilogue input][barriers][control].
-    static constexpr uint32_t smem_bytes(int stages, bool r_boxes) {
-        return 1024 /* alignment slack */ + stages * kStageBytes + kDStageTotal + (r_boxes ? kRStageTotal : 0) +
-               kBarBytes + sizeof(SharedCtl);
+    static constexpr uint32_t kBarBytes = 2 * STAGES * 8 + kMaxBoxes * kEpiWarps * 8;  // ring + R barriers
+    // Layout: [ring: stages x stage][D boxes: warps x d_boxes][R boxes: warps x r_boxes][barriers][control].
+    static constexpr uint32_t smem_bytes(int stages, int d_boxes, int r_boxes) {
+        return 1024 /* alignment slack */ + stages * kStageBytes +
+               static_cast<uint32_t>(kEpiWarps * (d_boxes + r_boxes)) * kDStageBytes + kBarBytes + sizeof(SharedCtl);
     }
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kMmaN);
     static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * kCG;  // epilogue warps of every CTA in the pair
@@ -457,8 +462,8 @@ struct KernelShape {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(kBRows % 8 == 0 && kBRows <= 256 && kMmaN % 16 == 0, "B operand rows");
     static_assert(NUM_B == 1 || BN == kBRows || 2 * BN == kBRows, "FFN: one product per CTA or both stacked");
-    static_assert(smem_bytes(STAGES, false) <= 232448, "the deepest ring fits without R boxes");
-    static_assert(smem_bytes(2, true) <= 232448, "a two-stage ring fits with R boxes");
+    static_assert(smem_bytes(STAGES, 2, 0) <= 232448, "the deepest ring fits with two D boxes per warp");
+    static_assert(smem_bytes(2, 2, NUM_B == 1 ? 2 : 0) <= 232448, "a two-stage ring fits with two D and R boxes");
 };
 
 template <int BN, int NUM_B, int STAGES, bool PAIR, int EPI>
@@ -471,14 +476,13 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t stages = static_cast<uint32_t>(p.stages);
-    const bool r_boxes = (NUM_B == 1) && (p.flags & kFlagResidual);
     uint8_t* ring = smem;
     uint8_t* dstage = smem + stages * S::kStageBytes;
-    uint8_t* rstage = dstage + S::kDStageTotal;
-    uint64_t* full = reinterpret_cast<uint64_t*>(rstage + (r_boxes ? S::kRStageTotal : 0u));
+    uint8_t* rstage = dstage + kEpiWarps * p.d_boxes * kDStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(rstage + kEpiWarps * p.r_boxes * kDStageBytes);
     uint64_t* empty = full + STAGES;
-    uint64_t* rbar = empty + STAGES;  // two per epilogue warp
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(rbar + 2 * kEpiWarps);
+    uint64_t* rbar = empty + STAGES;  // kMaxBoxes per epilogue warp
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(rbar + kMaxBoxes * kEpiWarps);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -499,7 +503,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             mbar_init(smem_addr(&ctl->acc_empty[b]), S::kAccEmptyArrivals);
         }
         mbar_init(smem_addr(&ctl->drain), 1);
-        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(smem_addr(&rbar[i]), 1);
+        for (int i = 0; i < kMaxBoxes * kEpiWarps; ++i) mbar_init(smem_addr(&rbar[i]), 1);
         ctl->abort = 0;
         fence_mbar_init();
     }
@@ -652,19 +656,23 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const int32_t slab_row = static_cast<int32_t>(rank) * kBM + q * 32 + lane;  // row within the tile
         constexpr int64_t kPartFloats = static_cast<int64_t>(S::kTileM) * BN;       // one partial accumulator
-        uint32_t dcount = 0;
+        uint8_t* dbox = dstage + e * p.d_boxes * kDStageBytes;  // this warp's D staging queue
+        int32_t dslot = 0;
         int32_t local = 0;
 
         // R by TMA (linear, no split): a cursor over this warp's future (tile, chunk)
-        // pairs keeps up to two 32x32 R boxes in flight ahead of their use, so the
-        // loads for the next tile overlap the current tile's MMAs.
+        // pairs keeps up to r_boxes 32x32 R boxes in flight ahead of their use, so
+        // the loads for the next tile overlap the current tile's MMAs.
         const bool r_tma = (NUM_B == 1) && (p.flags & kFlagRTma);
         const bool express = p.splits == 1 && p.num_k_blocks > 0 && (p.flags & kFlagDTma) &&
                              !(p.flags & (kFlagResidual | kFlagZ));
-        // transpose buffer for unaligned R rows (the R boxes are unused then)
-        uint8_t* tbuf_r = NUM_B == 1 ? rstage + e * 2 * kDStageBytes : nullptr;
+        // this warp's R boxes; also the transpose buffer for unaligned R rows (the
+        // boxes are unused then)
+        uint8_t* rbox0 = rstage + e * p.r_boxes * kDStageBytes;
+        uint8_t* tbuf_r = NUM_B == 1 ? rbox0 : nullptr;
         int32_t rc_w = unit, rc_c = g, rc_mb = -1, rc_nb = -1;
-        uint32_t r_issued = 0, r_used = 0, r_phase = 0;
+        uint32_t r_issued = 0, r_used = 0, r_phase = 0;  // r_phase: one parity bit per box
+        int32_t r_islot = 0, r_uslot = 0;                 // queue positions of the next load and the next use
         auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
             while (rc_w < num_work) {
                 if (rc_mb < 0) tile_coords(rc_w, p, rc_mb, rc_nb);
@@ -681,14 +689,14 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         };
         auto r_issue = [&]() {
             if (!r_tma || !r_find()) return;
-            const uint32_t buf = r_issued & 1u;
             if (lane == 0) {
-                const uint32_t bar = smem_addr(&rbar[e * 2 + buf]);
+                const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_islot]);
                 mbar_arrive_expect_tx(bar, kDStageBytes);
-                tma_load_2d(smem_addr(rstage + (e * 2 + buf) * kDStageBytes), &p.tm_r, bar,
-                            rc_nb * BN + rc_c * kDChunk, rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32);
+                tma_load_2d(smem_addr(rbox0 + r_islot * kDStageBytes), &p.tm_r, bar, rc_nb * BN + rc_c * kDChunk,
+                            rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32);
             }
             ++r_issued;
+            if (++r_islot == p.r_boxes) r_islot = 0;
             rc_c += kEpiGroups;
             if (rc_c >= kChunks) {
                 rc_c = g;
@@ -696,8 +704,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 rc_mb = -1;
             }
         };
-        r_issue();
-        r_issue();
+        if (r_tma)
+            for (int i = 0; i < p.r_boxes; ++i) r_issue();
 
         for (int32_t w = unit; w < num_work; w += units, ++local) {
             const uint32_t b = local & 1;
@@ -771,8 +779,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     uint32_t packed[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                    uint8_t* buf = dstage + (e * 2 + (dcount & 1u)) * kDStageBytes;
-                    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this box has read it
+                    uint8_t* buf = dbox + dslot * kDStageBytes;
+                    if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
                     __syncwarp();
                     const uint32_t row_addr = smem_addr(buf) + lane * 64;
                     const uint32_t sw = (lane >> 1) & 3u;
@@ -786,7 +794,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         tma_store_2d(&p.tm_d, smem_addr(buf), n0, row0);
                         bulk_commit_group();
                     }
-                    ++dcount;
+                    if (++dslot == p.d_boxes) dslot = 0;
                 }
                 continue;
             }
@@ -841,23 +849,23 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 if (!chunk_on || split_mode) continue;
                 uint32_t rbox = 0;
                 if (r_tma) {
-                    const uint32_t buf = r_used & 1u;
-                    const uint32_t bar = smem_addr(&rbar[e * 2 + buf]);
-                    const uint32_t par = (r_phase >> buf) & 1u;
+                    const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
+                    const uint32_t par = (r_phase >> r_uslot) & 1u;
                     bool rok = true;
-                    if (lane == 0) rok = wait_bar(bar, par, abort_flag, tmo, kRoleEpilogue, 0x200u | buf);
+                    if (lane == 0) rok = wait_bar(bar, par, abort_flag, tmo, kRoleEpilogue, 0x200u | r_uslot);
                     rok = __shfl_sync(0xffffffffu, rok, 0);
                     if (!rok) break;
                     while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
                     }
-                    r_phase ^= 1u << buf;
-                    rbox = smem_addr(rstage + (e * 2 + buf) * kDStageBytes);
+                    r_phase ^= 1u << r_uslot;
+                    rbox = smem_addr(rbox0 + r_uslot * kDStageBytes);
                 }
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, e, dstage, dcount, rbox, tbuf_r);
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r);
                 if (r_tma) {
-                    __syncwarp();  // every lane has read the box: refill its buffer
+                    __syncwarp();  // every lane has read the box: refill it
                     fence_proxy_async_smem();
                     ++r_used;
+                    if (++r_uslot == p.r_boxes) r_uslot = 0;
                     r_issue();
                 }
             }
@@ -889,13 +897,17 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = silu(v[j]) * v3[j];
                 }
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, e, dstage, dcount, 0u, tbuf_r);
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, 0u, tbuf_r);
             }
         }
         if (lane == 0) {
-            // R boxes still in flight after an early stop: wait (bounded) for them to land.
-            for (uint32_t i = r_used; i < r_issued; ++i)
-                drain_bar(smem_addr(&rbar[e * 2 + (i & 1u)]), (r_phase >> (i & 1u)) & 1u, tmo);
+            // R boxes still in flight after an early stop (at most r_boxes, from the use
+            // position on): wait (bounded) for them to land.
+            int32_t slot = r_uslot;
+            for (uint32_t i = r_used; i < r_issued; ++i) {
+                drain_bar(smem_addr(&rbar[e * kMaxBoxes + slot]), (r_phase >> slot) & 1u, tmo);
+                if (++slot == p.r_boxes) slot = 0;
+            }
             bulk_wait_group<0>();
         }
         __syncwarp();

@@ -112,6 +112,20 @@ __device__ __forceinline__ void bulk_wait_group_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// The same with a run-time bound n (clamped to [0, 7]).
+__device__ __forceinline__ void bulk_wait_group_read_at_most(int n) {
+    switch (n) {
+        case 0: bulk_wait_group_read<0>(); break;
+        case 1: bulk_wait_group_read<1>(); break;
+        case 2: bulk_wait_group_read<2>(); break;
+        case 3: bulk_wait_group_read<3>(); break;
+        case 4: bulk_wait_group_read<4>(); break;
+        case 5: bulk_wait_group_read<5>(); break;
+        case 6: bulk_wait_group_read<6>(); break;
+        default: if (n < 0) bulk_wait_group_read<0>(); else bulk_wait_group_read<7>(); break;
+    }
+}
+
 // Wait until at most N bulk groups are pending at all (writes complete).
 template <int N>
 __device__ __forceinline__ void bulk_wait_group() {

@@ -187,7 +187,8 @@ def test_ffn_integer_bit_exact_when_gate_is_relu_like():
                                   "pair=1,grid=2", "pair=1,persistent=0", "pair=0,grid=5,group=2",
                                   "pair=1,group=1,grid=6", "stages=2", "stages=3,pair=1,grid=3",
                                   "stages=4,pair=0", "stages=16", "epi=1", "epi=2", "epi=1,pair=0,grid=3",
-                                  "epi=2,pair=1,grid=2,stages=3"])
+                                  "epi=2,pair=1,grid=2,stages=3", "boxes=2", "boxes=8,grid=3",
+                                  "boxes=5,stages=6", "boxes=3,epi=1,pair=0"])
 def test_config_overrides_give_identical_bits(spec):
     """Tile size, grid, swizzle and persistence change which CTA computes a tile but not
     the per-element accumulation order within the tile: identical bits."""
@@ -260,6 +261,49 @@ def test_residual_by_tma(spec, M, N):
     got = run_linear(A, B, bias, R, "gelu_tanh")
     assert "r_load=tma" in gb.last_plan(), gb.last_plan()
     assert_close(got, ref_linear(A, B, bias, R, "gelu_tanh"), f"{spec} {M}x{N}")
+
+
+@pytest.mark.parametrize("spec", ["boxes=2", "boxes=3", "boxes=8", "boxes=8,stages=2", "boxes=5,grid=3",
+                                  "boxes=8,epi=1", "boxes=4,epi=2,pair=0,grid=2", "boxes=7,pair=1,grid=2"])
+@pytest.mark.parametrize("K", [64, 1024])
+def test_box_queue_depths(spec, K):
+    """Per-warp queues of D staging boxes and TMA-loaded R boxes, 2 to 8 deep, with
+    the ring shortened to make room: a small grid makes every warp's queues wrap
+    many times across tiles.  The queue depth changes no arithmetic: identical bits
+    to the default plan, and the oracle's result within tolerance."""
+    M, N = 700, 1160
+    A = inputs.randn_bf16((M, K), seed=140)
+    B = inputs.randn_bf16((N, K), seed=141, std=1.0 / np.sqrt(K))
+    bias = inputs.randn_bf16((N,), seed=142, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=143)
+    base = run_linear(A, B, bias, R, "gelu_tanh")
+    gb.set_config(spec)
+    got = run_linear(A, B, bias, R, "gelu_tanh")
+    plan = gb.last_plan()
+    d_boxes, r_boxes = (int(v) for v in plan.split("boxes=")[1].split()[0].split("/"))
+    want = int(spec.split("boxes=")[1].split(",")[0])
+    assert "r_load=tma" in plan and d_boxes == r_boxes and 2 <= d_boxes <= want, plan
+    assert_bitexact(got, base, plan)
+    assert_close(got, ref_linear(A, B, bias, R, "gelu_tanh"), plan)
+    # second output and no epilogue input: D and Z share the D queue
+    D, Z = gb.linear_preact(A.to(DEV), B.to(DEV), bias.to(DEV), None, act="relu")
+    gb.device_status()
+    assert_close(bits(D), ref_linear(A, B, bias, None, "relu"), "D " + gb.last_plan())
+    assert_close(bits(Z), ref_linear(A, B, bias, None, "none"), "Z " + gb.last_plan())
+
+
+def test_short_k_plan_takes_deep_queues():
+    """Work items of at most 4 k-blocks get a 3-stage ring and the deepest queues that
+    fit; long-K items keep the deepest ring and two boxes per warp."""
+    A = inputs.randn_bf16((512, 4096), seed=150)
+    B = inputs.randn_bf16((512, 4096), seed=151, std=1.0 / 64)
+    R = inputs.randn_bf16((512, 512), seed=152)
+    run_linear(A[:, :64].contiguous(), B[:, :64].contiguous(), None, R)
+    short = gb.last_plan()
+    assert "stages=3" in short and "boxes=2/" not in short, short
+    run_linear(A, B, None, R)
+    long = gb.last_plan()
+    assert "boxes=2/2" in long and "stages=3 " not in long, long
 
 
 def test_residual_by_tma_aliasing_d():
