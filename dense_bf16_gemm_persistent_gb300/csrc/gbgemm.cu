@@ -54,6 +54,8 @@ struct Config {
     int stages = 0;      // 0 = the deepest ring that fits
     int epi = 0;         // epilogue warpgroups: 0 = heuristic, 1 or 2
     int boxes = 0;       // staging boxes per epilogue warp (D, and R by TMA): 0 = heuristic, 2..8
+    int pingpong = -1;   // 1: the two epilogue warpgroups alternate tiles (implies epi=2; no effect with
+                         // split-K); 0: they share every tile; -1 = auto (alternate on short-K work items)
 };
 
 std::mutex g_cfg_mu;
@@ -437,6 +439,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         prm.d_boxes = lay.d_boxes;
         prm.r_boxes = lay.r_boxes;
     }
+    // Ping-pong (two epilogue warpgroups alternating tiles): on by default for work
+    // items of at most 4 k-blocks, where the epilogue is the whole cost (measured on
+    // GB300: +9-13 % on the K = 64 residual shapes); off for long K, where sharing
+    // every tile's chunks is 2.5-7.5 % faster.
+    const bool pp_auto = prm.kb_per_split <= 4;
+    prm.pingpong = (V::kEpi == 2 && splits == 1 && (cfg.pingpong == 1 || (cfg.pingpong < 0 && pp_auto))) ? 1 : 0;
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
     if (pr.k > 0) {
@@ -472,10 +480,11 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
 
     char plan[360];
     snprintf(plan, sizeof plan,
-             "kernel=%s pair=%d epi=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d k_blocks=%d "
-             "splits=%d group=%d zigzag=%d "
+             "kernel=%s pair=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
+             "k_blocks=%d splits=%d group=%d zigzag=%d "
              "d_store=%s r_load=%s z_store=%s",
-             pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kEpi, V::kTileM, bn, gb::kBK, prm.stages,
+             pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kEpi, prm.pingpong, V::kTileM, bn, gb::kBK,
+             prm.stages,
              prm.d_boxes, prm.r_boxes,
              static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, d_tma ? "tma" : "st.transposed",
@@ -539,8 +548,11 @@ gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitR
     const bool d_rows_aligned = aligned16(pr.d) && pr.ldd % 8 == 0;
     const int64_t tiles_est = cdiv(pr.m, pair ? 2 * gb::kBM : gb::kBM) * cdiv(pr.n, bn);
     const bool few_tiles_split = sr.allowed && 2 * tiles_est <= info.sms;
-    const int epi = cfg.epi > 0 ? cfg.epi
-                                : ((kb <= 16 || few_tiles_split || !d_rows_aligned || pr.r || pr.z) ? 2 : 1);
+    if (cfg.pingpong == 1 && cfg.epi == 1)
+        return fail(GB_ERR_INVALID_ARG, "pingpong=1 needs two epilogue warpgroups (epi=2)");
+    const int epi = cfg.pingpong == 1 ? 2
+                    : cfg.epi > 0 ? cfg.epi
+                                  : ((kb <= 16 || few_tiles_split || !d_rows_aligned || pr.r || pr.z) ? 2 : 1);
     return epi == 2 ? dispatch<2>(pr, cfg, bn, pair, dev, info, timeout_ns, inject, stream, sr)
                     : dispatch<1>(pr, cfg, bn, pair, dev, info, timeout_ns, inject, stream, sr);
 }
@@ -759,6 +771,7 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "stages" && v >= 0 && v <= 16) c.stages = static_cast<int>(v);
             else if (key == "epi" && v >= 0 && v <= 2) c.epi = static_cast<int>(v);
             else if (key == "boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.boxes = static_cast<int>(v);
+            else if (key == "pingpong" && v >= -1 && v <= 1) c.pingpong = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

@@ -128,6 +128,10 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     int32_t stages;   // depth of the operand ring (<= the variant's maximum)
     int32_t d_boxes;  // D staging boxes per epilogue warp, 2..kMaxBoxes
     int32_t r_boxes;  // R boxes per epilogue warp: 2..kMaxBoxes with an epilogue input (linear), else 0
+    // Ping-pong (two epilogue warpgroups, no split): warpgroup g takes every work item
+    // of local parity g -- always TMEM buffer g -- and all of its chunks, instead of
+    // both warpgroups sharing every tile's chunks.
+    int32_t pingpong;
 };
 
 struct SharedCtl {
@@ -492,6 +496,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     const int32_t unit = PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
     const int32_t units = PAIR ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
     const int32_t num_work = p.num_tiles * p.splits;
+    // ping-pong takes effect with two epilogue warpgroups and no split only
+    const bool pingpong = kEpiGroups == 2 && p.pingpong != 0 && p.splits == 1;
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < stages; ++s) {
@@ -500,7 +506,10 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&ctl->acc_full[b]), 1);
-            mbar_init(smem_addr(&ctl->acc_empty[b]), S::kAccEmptyArrivals);
+            // every epilogue warp of the pair frees a buffer; with ping-pong only the
+            // warpgroup that owns it
+            mbar_init(smem_addr(&ctl->acc_empty[b]), pingpong ? S::kAccEmptyArrivals / kEpiGroups
+                                                              : S::kAccEmptyArrivals);
         }
         mbar_init(smem_addr(&ctl->drain), 1);
         for (int i = 0; i < kMaxBoxes * kEpiWarps; ++i) mbar_init(smem_addr(&rbar[i]), 1);
@@ -651,7 +660,12 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         // ------------------------------------------------------------ epilogue (every CTA)
         const int e = warp - kEpiWarp0;  // epilogue warp index: staging buffers, counters
         const int q = e & 3;              // == warp % 4: this warp's TMEM lane quadrant
-        const int g = e >> 2;             // chunk phase: chunks g, g + kEpiGroups, ...
+        const int g = e >> 2;             // this warp's warpgroup among the epilogue warpgroups
+        // Chunks of a tile this warp stores: g, g + kEpiGroups, ... when the warpgroups
+        // share every tile; all of them, on every other tile, with ping-pong.
+        const bool pp = pingpong;
+        const int c0 = pp ? 0 : g;
+        const int cstep = pp ? 1 : kEpiGroups;
         constexpr int kChunks = BN / kDChunk;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const int32_t slab_row = static_cast<int32_t>(rank) * kBM + q * 32 + lane;  // row within the tile
@@ -670,18 +684,24 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         // boxes are unused then)
         uint8_t* rbox0 = rstage + e * p.r_boxes * kDStageBytes;
         uint8_t* tbuf_r = NUM_B == 1 ? rbox0 : nullptr;
-        int32_t rc_w = unit, rc_c = g, rc_mb = -1, rc_nb = -1;
+        int32_t rc_w = unit, rc_local = 0, rc_c = c0, rc_mb = -1, rc_nb = -1;
         uint32_t r_issued = 0, r_used = 0, r_phase = 0;  // r_phase: one parity bit per box
         int32_t r_islot = 0, r_uslot = 0;                 // queue positions of the next load and the next use
         auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
             while (rc_w < num_work) {
+                if (pp && (rc_local & 1) != g) {  // the other warpgroup's work item
+                    rc_w += units;
+                    ++rc_local;
+                    continue;
+                }
                 if (rc_mb < 0) tile_coords(rc_w, p, rc_mb, rc_nb);
                 const int32_t r0 = rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;
                 if (rc_c < kChunks && r0 < p.m && rc_nb * BN + rc_c * kDChunk < p.n) return true;
-                rc_c += kEpiGroups;
+                rc_c += cstep;
                 if (rc_c >= kChunks) {
-                    rc_c = g;
+                    rc_c = c0;
                     rc_w += units;
+                    ++rc_local;
                     rc_mb = -1;
                 }
             }
@@ -697,10 +717,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             }
             ++r_issued;
             if (++r_islot == p.r_boxes) r_islot = 0;
-            rc_c += kEpiGroups;
+            rc_c += cstep;
             if (rc_c >= kChunks) {
-                rc_c = g;
+                rc_c = c0;
                 rc_w += units;
+                ++rc_local;
                 rc_mb = -1;
             }
         };
@@ -708,6 +729,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             for (int i = 0; i < p.r_boxes; ++i) r_issue();
 
         for (int32_t w = unit; w < num_work; w += units, ++local) {
+            if (pp && (local & 1) != g) continue;  // the other warpgroup's tile
             const uint32_t b = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
             bool ok = true;
@@ -729,7 +751,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 // split): a compact loop, so the hot epilogue code next to the MMA
                 // issuer stays small.
 #pragma unroll 1
-                for (int c = g; c < kChunks; c += kEpiGroups) {
+                for (int c = c0; c < kChunks; c += cstep) {
                     const int32_t n0 = nb * BN + c * kDChunk;
                     const bool chunk_on = warp_rows && n0 < p.n;
                     float v[32];
@@ -748,7 +770,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
                         }
                     }
-                    if (c + kEpiGroups >= kChunks) {
+                    if (c + cstep >= kChunks) {
                         tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) {
@@ -804,7 +826,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             float* acc_ws = p.ws + static_cast<int64_t>(tile) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
 
 #pragma unroll 1
-            for (int c = g; c < kChunks; c += kEpiGroups) {
+            for (int c = c0; c < kChunks; c += cstep) {
                 const int32_t n0 = nb * BN + c * kDChunk;
                 const bool chunk_on = warp_rows && n0 < p.n;
                 float v[32];
@@ -837,7 +859,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                 }
-                if (c + kEpiGroups >= kChunks) {
+                if (c + cstep >= kChunks) {
                     // This warp's TMEM reads of this buffer are done: hand it back to the MMA issuer.
                     tc_fence_before_sync();
                     __syncwarp();
@@ -882,7 +904,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             if (arrived != static_cast<uint32_t>(p.splits - 1)) continue;
             __threadfence();
 #pragma unroll 1
-            for (int c = g; c < kChunks; c += kEpiGroups) {
+            for (int c = c0; c < kChunks; c += cstep) {
                 const int32_t n0 = nb * BN + c * kDChunk;
                 if (n0 >= p.n) break;
                 float v[32];

@@ -226,9 +226,15 @@ GB_API const char* gb_last_error(void);
  * group (tile-swizzle group size along M, >= 1), zigzag (0, 1, or -1 = auto),
  * pair (1 = CTA pairs with 256-row tiles, 0 = single CTAs with 128-row tiles,
  * -1 = auto; the 128-wide linear tile always runs on single CTAs), stages
- * (depth of the operand ring, >= 2; 0 = the deepest that fits in shared
- * memory, which is one less when an epilogue input needs staging boxes), epi
- * (epilogue warpgroups: 1 or 2; 0 = auto: two for epilogue-bound shapes).
+ * (depth of the operand ring, >= 2; 0 = auto: the deepest that fits for
+ * long K, 3 for work items of at most 4 k-blocks), boxes (D staging boxes and
+ * TMA-loaded R boxes per epilogue warp, 2..8; 0 = auto: 2 for long K, the
+ * deepest that fits for short K; boxes shrink before the ring does), epi
+ * (epilogue warpgroups: 1 or 2; 0 = auto: two for epilogue-bound shapes),
+ * pingpong (1 = the two epilogue warpgroups alternate whole tiles, each owning
+ * one TMEM accumulator buffer, instead of sharing every tile's chunks; implies
+ * epi=2, GB_ERR_INVALID_ARG with epi=1 at the call, no effect with split-K;
+ * 0 = never; -1 = auto: on for work items of at most 4 k-blocks).
  * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
  */
 GB_API gb_status_t gb_set_config(const char* spec);

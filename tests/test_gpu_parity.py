@@ -188,7 +188,8 @@ def test_ffn_integer_bit_exact_when_gate_is_relu_like():
                                   "pair=1,group=1,grid=6", "stages=2", "stages=3,pair=1,grid=3",
                                   "stages=4,pair=0", "stages=16", "epi=1", "epi=2", "epi=1,pair=0,grid=3",
                                   "epi=2,pair=1,grid=2,stages=3", "boxes=2", "boxes=8,grid=3",
-                                  "boxes=5,stages=6", "boxes=3,epi=1,pair=0"])
+                                  "boxes=5,stages=6", "boxes=3,epi=1,pair=0", "pingpong=1", "pingpong=1,grid=3",
+                                  "pingpong=1,pair=0,grid=2"])
 def test_config_overrides_give_identical_bits(spec):
     """Tile size, grid, swizzle and persistence change which CTA computes a tile but not
     the per-element accumulation order within the tile: identical bits."""
@@ -292,6 +293,64 @@ def test_box_queue_depths(spec, K):
     assert_close(bits(Z), ref_linear(A, B, bias, None, "none"), "Z " + gb.last_plan())
 
 
+@pytest.mark.parametrize("spec", ["pingpong=1", "pingpong=1,grid=3", "pingpong=1,pair=0,grid=5", "pingpong=1,boxes=8",
+                                  "pingpong=1,pair=1,grid=2,stages=2", "pingpong=0,epi=2", "pingpong=0,grid=3"])
+@pytest.mark.parametrize("K", [64, 640])
+def test_pingpong_all_epilogues(spec, K):
+    """Ping-pong on and off: the two epilogue warpgroups alternate whole tiles (each owns
+    one TMEM buffer) or share every tile's chunks.  Same per-element arithmetic either
+    way, so identical bits to the default plan for bias+GELU+R (R by TMA), unaligned
+    rows (transposes), the second output Z and the FFN; and the oracle's result within
+    tolerance."""
+    M, N = 520, 776
+    A = inputs.randn_bf16((M, K), seed=160)
+    B = inputs.randn_bf16((N, K), seed=161, std=1.0 / np.sqrt(K))
+    B3 = inputs.randn_bf16((N, K), seed=162, std=1.0 / np.sqrt(K))
+    bias = inputs.randn_bf16((N,), seed=163, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=164)
+    Ad, Bd, B3d, biasd, Rd = (t.to(DEV) for t in (A, B, B3, bias, R))
+
+    def all_outputs():
+        out = {"lin": bits(gb.linear(Ad, Bd, biasd, Rd, act="gelu_tanh"))}
+        Dodd = torch.zeros((M, N + 1), dtype=torch.bfloat16, device=DEV)[:, 1:]  # rows not 16-byte aligned
+        Rodd = torch.zeros((M, N + 1), dtype=torch.bfloat16, device=DEV)[:, 1:]
+        Rodd.copy_(Rd)
+        gb.linear(Ad, Bd, biasd, Rodd, act="silu", out=Dodd)
+        out["odd"] = bits(Dodd)
+        D, Z = gb.linear_preact(Ad, Bd, biasd, None, act="relu")
+        out["D"], out["Z"] = bits(D), bits(Z)
+        out["ffn"] = bits(gb.ffn_gated(Ad, Bd, B3d))
+        gb.device_status()
+        return out
+
+    base = all_outputs()
+    gb.set_config(spec)
+    got = all_outputs()
+    plan = gb.last_plan()
+    assert f"pingpong={spec[9]}" in plan and "epi=2" in plan, plan
+    for k in base:
+        assert_bitexact(got[k], base[k], f"{spec} {k}")
+    assert_close(got["lin"], ref_linear(A, B, bias, R, "gelu_tanh"), spec)
+    assert_close(got["odd"], ref_linear(A, B, bias, R, "silu"), spec)
+    assert_close(got["Z"], ref_linear(A, B, bias, None, "none"), spec)
+    assert_close(got["ffn"], oracle.ffn_gated(bits(A), bits(B), bits(B3)), spec)
+
+
+def test_pingpong_is_ignored_by_split_k_and_refused_with_one_warpgroup():
+    M, N, K = 127, 96, 4096
+    A = inputs.randn_bf16((M, K), seed=170)
+    B = inputs.randn_bf16((N, K), seed=171, std=1.0 / 64)
+    R = inputs.randn_bf16((M, N), seed=172)
+    gb.set_config("pingpong=1")
+    got = run_linear(A, B, None, R, split_k="auto")
+    plan = gb.last_plan()
+    assert "pingpong=0" in plan and int(plan.split("splits=")[1].split()[0]) > 1, plan
+    assert_close(got, ref_linear(A, B, None, R), plan)
+    gb.set_config("pingpong=1,epi=1")
+    with pytest.raises(gb.GBError):
+        run_linear(A, B)
+
+
 def test_short_k_plan_takes_deep_queues():
     """Work items of at most 4 k-blocks get a 3-stage ring and the deepest queues that
     fit; long-K items keep the deepest ring and two boxes per warp."""
@@ -300,10 +359,10 @@ def test_short_k_plan_takes_deep_queues():
     R = inputs.randn_bf16((512, 512), seed=152)
     run_linear(A[:, :64].contiguous(), B[:, :64].contiguous(), None, R)
     short = gb.last_plan()
-    assert "stages=3" in short and "boxes=2/" not in short, short
+    assert "stages=3" in short and "boxes=2/" not in short and "pingpong=1" in short, short
     run_linear(A, B, None, R)
     long = gb.last_plan()
-    assert "boxes=2/2" in long and "stages=3 " not in long, long
+    assert "boxes=2/2" in long and "stages=3 " not in long and "pingpong=0" in long, long
 
 
 def test_residual_by_tma_aliasing_d():
