@@ -439,12 +439,6 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         prm.d_boxes = lay.d_boxes;
         prm.r_boxes = lay.r_boxes;
     }
-    // Ping-pong (two epilogue warpgroups alternating tiles): on by default for work
-    // items of at most 4 k-blocks, where the epilogue is the whole cost (measured on
-    // GB300: +9-13 % on the K = 64 residual shapes); off for long K, where sharing
-    // every tile's chunks is 2.5-7.5 % faster.
-    const bool pp_auto = prm.kb_per_split <= 4;
-    prm.pingpong = (V::kEpi == 2 && splits == 1 && (cfg.pingpong == 1 || (cfg.pingpong < 0 && pp_auto))) ? 1 : 0;
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
     if (pr.k > 0) {
@@ -477,6 +471,14 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     }
     if (units > work) units = work;
     if (units < 1) units = 1;
+
+    // Ping-pong (two epilogue warpgroups alternating tiles): on by default for work
+    // items of at most 4 k-blocks, where the epilogue is the whole cost (measured on
+    // GB300: +9-13 % on the K = 64 residual shapes), if every unit gets at least 4 of
+    // them (with fewer, one warpgroup would idle); off for long K, where sharing
+    // every tile's chunks is 2.5-7.5 % faster.
+    const bool pp_auto = prm.kb_per_split <= 4 && work >= 4 * units;
+    prm.pingpong = (V::kEpi == 2 && splits == 1 && (cfg.pingpong == 1 || (cfg.pingpong < 0 && pp_auto))) ? 1 : 0;
 
     char plan[360];
     snprintf(plan, sizeof plan,

@@ -352,17 +352,27 @@ def test_pingpong_is_ignored_by_split_k_and_refused_with_one_warpgroup():
 
 
 def test_short_k_plan_takes_deep_queues():
-    """Work items of at most 4 k-blocks get a 3-stage ring and the deepest queues that
-    fit; long-K items keep the deepest ring and two boxes per warp."""
+    """Work items of at most 4 k-blocks get a 3-stage ring, the deepest queues that fit
+    and, with at least 4 work items per unit, the ping-pong schedule; long-K items keep
+    the deepest ring, two boxes per warp and the shared schedule."""
     A = inputs.randn_bf16((512, 4096), seed=150)
     B = inputs.randn_bf16((512, 4096), seed=151, std=1.0 / 64)
     R = inputs.randn_bf16((512, 512), seed=152)
     run_linear(A[:, :64].contiguous(), B[:, :64].contiguous(), None, R)
     short = gb.last_plan()
-    assert "stages=3" in short and "boxes=2/" not in short and "pingpong=1" in short, short
+    assert "stages=3" in short and "boxes=2/" not in short and "pingpong=0" in short, short  # 4 tiles only
     run_linear(A, B, None, R)
     long = gb.last_plan()
     assert "boxes=2/2" in long and "stages=3 " not in long and "pingpong=0" in long, long
+    # 16 x 20 tiles of 256 x 256 on at most 76 CTA pairs: ping-pong (plan only)
+    Ab = torch.zeros((4096, 64), dtype=torch.bfloat16, device=DEV)
+    Bb = torch.zeros((5120, 64), dtype=torch.bfloat16, device=DEV)
+    Rb = torch.zeros((4096, 5120), dtype=torch.bfloat16, device=DEV)
+    D = gb.linear(Ab, Bb, None, Rb)
+    gb.device_status()
+    big = gb.last_plan()
+    assert "pingpong=1" in big and "stages=3" in big, big
+    assert torch.equal(D.view(torch.int16), Rb.view(torch.int16))
 
 
 def test_residual_by_tma_aliasing_d():
