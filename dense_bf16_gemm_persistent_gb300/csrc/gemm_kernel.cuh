@@ -269,6 +269,17 @@ __device__ __forceinline__ void add_bf16_box_row(float (&v)[32], uint32_t box, i
     }
 }
 
+// Write this lane's row of a 32x32 bf16 box, 64-byte swizzled for the TMA store.
+__device__ __forceinline__ void stage_box_row(uint32_t box, const float (&v)[32], int lane) {
+    const uint32_t row_addr = box + lane * 64;
+    const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        st_shared_v4(row_addr + ((u ^ sw) << 4), pack_bf16x2(v[8 * u], v[8 * u + 1]),
+                     pack_bf16x2(v[8 * u + 2], v[8 * u + 3]), pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
+                     pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+}
+
 // Rows of D or R that are not 16-byte aligned (e.g. N = 4099): go through a
 // per-warp shared-memory transpose with a 68-byte row stride (conflict-free), so
 // every global access instruction covers one contiguous 64-byte row segment
@@ -680,12 +691,17 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         const bool r_tma = (NUM_B == 1) && (p.flags & kFlagRTma);
         const bool express = p.splits == 1 && p.num_k_blocks > 0 && (p.flags & kFlagDTma) &&
                              !(p.flags & (kFlagResidual | kFlagZ));
+        // Paired path (R by TMA, D by TMA, no second output, no split): two chunks per
+        // step, so the fixed cost of a step (waits, fence, warp syncs, branches) is
+        // paid once per 64 columns and the two chunks' chains overlap.
+        const bool paired = r_tma && p.splits == 1 && p.num_k_blocks > 0 && (p.flags & kFlagDTma) &&
+                            !(p.flags & kFlagZ);
         // this warp's R boxes; also the transpose buffer for unaligned R rows (the
         // boxes are unused then)
         uint8_t* rbox0 = rstage + e * p.r_boxes * kDStageBytes;
         uint8_t* tbuf_r = NUM_B == 1 ? rbox0 : nullptr;
         int32_t rc_w = unit, rc_local = 0, rc_c = c0, rc_mb = -1, rc_nb = -1;
-        uint32_t r_issued = 0, r_used = 0, r_phase = 0;  // r_phase: one parity bit per box
+        uint32_t r_pending = 0, r_phase = 0;  // R boxes issued and not yet used; one parity bit per box
         int32_t r_islot = 0, r_uslot = 0;                 // queue positions of the next load and the next use
         auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
             while (rc_w < num_work) {
@@ -715,7 +731,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 tma_load_2d(smem_addr(rbox0 + r_islot * kDStageBytes), &p.tm_r, bar, rc_nb * BN + rc_c * kDChunk,
                             rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32);
             }
-            ++r_issued;
+            ++r_pending;
             if (++r_islot == p.r_boxes) r_islot = 0;
             rc_c += cstep;
             if (rc_c >= kChunks) {
@@ -820,6 +836,109 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 }
                 continue;
             }
+            if constexpr (NUM_B == 1) {
+                if (paired) {
+                    // This warp's chunks of the tile come in pairs (c, c + cstep): kChunks /
+                    // cstep is even for every variant.  The two chunks are computed one after
+                    // the other (one chunk's registers), but share one wait for two free D
+                    // boxes, one proxy fence and one warp sync before their two stores.
+                    // Chunk b is on only if chunk a is.
+                    bool rok = true;
+#pragma unroll 1
+                    for (int c = c0; c < kChunks; c += 2 * cstep) {
+                        const bool last = c + 2 * cstep >= kChunks;
+                        const int nchunks = !(warp_rows && nb * BN + c * kDChunk < p.n) ? 0
+                                            : (nb * BN + (c + cstep) * kDChunk < p.n ? 2 : 1);
+                        if (nchunks > 0) {
+                            // two D boxes free: the stores that last used them have read them
+                            if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 2);
+                            __syncwarp();
+                        }
+                        uint32_t box_a = 0;
+#pragma unroll 1
+                        for (int i = 0; i < 2; ++i) {
+                            const int ci = c + i * cstep;
+                            const int32_t n0 = nb * BN + ci * kDChunk;
+                            float v[32];
+                            if (i < nchunks) {
+                                uint32_t r0[32];
+                                tmem_ld_32x32b_x32(tcol + ci * kDChunk, r0);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                            }
+                            if (last && i == 1) {  // this warp's last TMEM reads of the buffer are done
+                                tc_fence_before_sync();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), 0));
+                                    else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                                }
+                            }
+                            if (i >= nchunks) continue;
+                            if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
+                            switch (p.act) {
+                                case 1:
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                                    break;
+                                case 2:
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                                    break;
+                                case 3:
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                                    break;
+                                default:
+                                    break;
+                            }
+                            // this chunk's R box: the one at the use position of the queue
+                            const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
+                            const uint32_t par = (r_phase >> r_uslot) & 1u;
+                            if (lane == 0) rok = wait_bar(bar, par, abort_flag, tmo, kRoleEpilogue, 0x200u | r_uslot);
+                            rok = __shfl_sync(0xffffffffu, rok, 0);
+                            if (!rok) break;
+                            while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
+                            }
+                            r_phase ^= 1u << r_uslot;
+                            add_bf16_box_row(v, smem_addr(rbox0 + r_uslot * kDStageBytes), lane);
+                            --r_pending;
+                            if (++r_uslot == p.r_boxes) r_uslot = 0;
+                            const uint32_t box = smem_addr(dbox + dslot * kDStageBytes);
+                            if (++dslot == p.d_boxes) dslot = 0;
+                            stage_box_row(box, v, lane);
+                            if (i == 0) {
+                                box_a = box;
+                                continue;
+                            }
+                            // both chunks staged: one proxy fence orders this lane's staging writes
+                            // and R box reads before the TMA stores and the refills of the boxes
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&p.tm_d, box_a, n0 - cstep * kDChunk, row0);
+                                bulk_commit_group();
+                                tma_store_2d(&p.tm_d, box, n0, row0);
+                                bulk_commit_group();
+                            }
+                        }
+                        if (!rok) break;
+                        if (nchunks == 1) {  // chunk a alone (b is past N)
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&p.tm_d, box_a, nb * BN + c * kDChunk, row0);
+                                bulk_commit_group();
+                            }
+                        }
+#pragma unroll 1
+                        for (int i = 0; i < nchunks; ++i) r_issue();
+                    }
+                    if (!rok) break;
+                    continue;
+                }
+            }
 
             const bool split_mode = p.splits > 1;
             // this slab's rows of the tile's fp32 accumulator (split-K only)
@@ -886,7 +1005,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 if (r_tma) {
                     __syncwarp();  // every lane has read the box: refill it
                     fence_proxy_async_smem();
-                    ++r_used;
+                    --r_pending;
                     if (++r_uslot == p.r_boxes) r_uslot = 0;
                     r_issue();
                 }
@@ -926,7 +1045,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             // R boxes still in flight after an early stop (at most r_boxes, from the use
             // position on): wait (bounded) for them to land.
             int32_t slot = r_uslot;
-            for (uint32_t i = r_used; i < r_issued; ++i) {
+            for (uint32_t i = 0; i < r_pending; ++i) {
                 drain_bar(smem_addr(&rbar[e * kMaxBoxes + slot]), (r_phase >> slot) & 1u, tmo);
                 if (++slot == p.r_boxes) slot = 0;
             }
