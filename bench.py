@@ -417,7 +417,7 @@ def run_ours(args, wl: dict):
         ev_done = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
 
-        def run_pipeline(n: int):
+        def run_pipeline(n: int, compute: bool = True):
             for i in range(n):
                 bi = i % 2
                 if i >= 2:
@@ -429,7 +429,8 @@ def run_ours(args, wl: dict):
                 s_comp.wait_event(ev_in[bi])
                 if i >= 2:
                     s_comp.wait_event(ev_out[bi])     # copy-out i-2 has read dev_out[bi]
-                steps_b[bi]()
+                if compute:
+                    steps_b[bi]()
                 ev_done[bi].record(s_comp)
                 s_out.wait_event(ev_done[bi])
                 with torch.cuda.stream(s_out):
@@ -451,9 +452,25 @@ def run_ours(args, wl: dict):
         torch.cuda.synchronize()
         barrier(dist, device)
         gb.device_status()
-        e2e_val, _ = aggregate_replicas(fl * n_e2e / 1e12, e0.elapsed_time(e1) / 1e3, dist, device)
+        e2e_ms = e0.elapsed_time(e1)
+        e2e_val, _ = aggregate_replicas(fl * n_e2e / 1e12, e2e_ms / 1e3, dist, device)
+        # The same pipeline with the copies alone (a separate, reported measurement, not
+        # part of the e2e number): the host link's ceiling for this step's bytes.
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        c0.record(s_in)
+        last = run_pipeline(n_e2e, compute=False)
+        s_in.wait_event(last)
+        s_in.wait_event(ev_out[n_e2e % 2])
+        c1.record(s_in)
+        torch.cuda.synchronize()
+        copy_ms = c0.elapsed_time(c1) / n_e2e
         e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": n_e2e, "pipelined": "3 streams, double-buffered device inputs and outputs"}
+               "steps": n_e2e, "pipelined": "3 streams, double-buffered device inputs and outputs",
+               "ms_per_step": e2e_ms / n_e2e,
+               "copies_only_ms_per_step": copy_ms,
+               "link_gbs_copies_only": (h2d + d2h) / (copy_ms / 1e3) / 1e9,
+               "note": "copies_only: the same pipeline without the GEMM call, timed separately"}
 
     if rank != 0:
         if dist is not None:
