@@ -472,7 +472,11 @@ struct KernelShape {
     }
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kMmaN);
     static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * kCG;  // epilogue warps of every CTA in the pair
-    static constexpr int kSlabs = kEpiWarps * kCG;                     // split-K counters per tile
+    // split-K counters per tile: one per epilogue warp of every CTA of the tile, laid out
+    // for the most epilogue warps any variant of this tile shape has (two warpgroups), so
+    // the workspace size does not depend on which epilogue layout a call picks
+    static constexpr int kSlabs = 8 * kCG;
+    static_assert(kEpiWarps <= 8, "split-K counter layout");
     static_assert(kMmaN <= kAccStride, "accumulator buffer holds at most 256 columns");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(kBRows % 8 == 0 && kBRows <= 256 && kMmaN % 16 == 0, "B operand rows");

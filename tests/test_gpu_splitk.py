@@ -135,3 +135,33 @@ def test_workspace_checks():
     assert st == 1 and b"workspace" in L.gb_last_error()
     # no split needed -> no workspace needed
     assert gb.splitk_workspace_bytes(8192, 8192, 4096, 0) == 0
+
+
+@pytest.mark.parametrize("splits", [0, 2, 3])
+@pytest.mark.parametrize("form", ["plain", "bias_gelu", "residual", "residual_bias_silu", "unaligned_d"])
+def test_queried_workspace_covers_every_epilogue(form, splits):
+    """The size query knows only M, N, K and the split count, while a call may pick
+    another epilogue layout (an epilogue input or unaligned rows take two epilogue
+    warpgroups, no input one).  A workspace of exactly the queried size must do for
+    every epilogue form.  80 tiles of 256 x 256 and K = 1280: without an epilogue input
+    the plan takes one epilogue warpgroup, with one it takes two."""
+    M, N, K = 1280, 4096, 1280
+    A = inputs.randn_bf16((M, K), seed=200, device=DEV)
+    B = inputs.randn_bf16((N, K), seed=201, std=1.0 / np.sqrt(K), device=DEV)
+    bias = inputs.randn_bf16((N,), seed=202, std=0.1, device=DEV) if "bias" in form else None
+    R = inputs.randn_bf16((M, N), seed=203, device=DEV) if "residual" in form else None
+    act = {"bias_gelu": "gelu_tanh", "residual_bias_silu": "silu"}.get(form, "none")
+    ws = torch.empty(gb.splitk_workspace_bytes(M, N, K, splits), dtype=torch.uint8, device=DEV)
+    if form == "unaligned_d":
+        Dbig = torch.zeros((M, N + 1), dtype=torch.bfloat16, device=DEV)
+        D = Dbig[:, 1:]
+        gb.linear(A, B, bias, R, act=act, out=D, split_k=splits or "auto", workspace=ws)
+    else:
+        D = gb.linear(A, B, bias, R, act=act, split_k=splits or "auto", workspace=ws)
+    gb.device_status()
+    plan = gb.last_plan()
+    r, c = inputs.sample_indices(M, N, seed=204)
+    rr, cc = torch.from_numpy(r).to(DEV), torch.from_numpy(c).to(DEV)
+    ref = oracle.linear(bits(A[rr]), bits(B[cc]), None if bias is None else bits(bias)[c],
+                        None if R is None else bits(R[rr][:, cc]), act)
+    assert_close(bits(D[rr][:, cc]), ref, f"{form} {plan}")
