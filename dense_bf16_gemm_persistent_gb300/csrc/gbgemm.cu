@@ -367,14 +367,20 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.num_tiles = static_cast<int32_t>(tiles);
 
     // Split-K: only with a workspace.  Auto: when the tiles would leave more than
-    // half of the scheduling units idle, cut K so that tiles x splits fills them,
-    // keeping at least 4 k-blocks per split.
+    // half of the scheduling units idle (and, unless K has at least 256 k-blocks,
+    // more than three quarters), cut K so that tiles x splits fills them, keeping at
+    // least 4 k-blocks per split and at most 64 splits.
     int splits = 1;
     if (sr.allowed && prm.num_k_blocks > 1) {
         if (sr.splits > 0) {
             splits = sr.splits;
-        } else if (prm.num_k_blocks >= 8 && 2 * tiles <= max_units) {
-            splits = static_cast<int>(std::min<int64_t>(max_units / tiles, prm.num_k_blocks / 4));
+        } else if (prm.num_k_blocks >= 8 && 2 * tiles <= max_units &&
+                   (4 * tiles <= max_units || prm.num_k_blocks >= 256)) {
+            // The fp32 partial sums cost about as much as a short K range saves: measured on
+            // GB300, a tile set that already fills a quarter of the units runs faster unsplit
+            // at K = 4096 (8191x96: 32.8 against 36.9 us) but split at K = 65536 (204 against
+            // 323 us); beyond 64 splits the reductions outweigh the shorter K ranges.
+            splits = static_cast<int>(std::min<int64_t>({max_units / tiles, prm.num_k_blocks / 4, 64}));
         }
         splits = std::max(1, std::min(splits, prm.num_k_blocks));
     }

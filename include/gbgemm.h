@@ -144,8 +144,9 @@ GB_API gb_status_t gb_gemm_ffn_gated(const void* X, int64_t ldx, const void* W1,
  * additions across ranges is not fixed, so two calls may differ by rounding;
  * results equal a sequential fp32 sum up to rounding, like every other call
  * (inputs whose partial sums are exact give identical bits).
- *   splits     <= 0: chosen automatically (1 when the tiles already fill the
- *              GPU); otherwise clamped to [1, number of 64-wide k-blocks].
+ *   splits     <= 0: chosen automatically (1 when the tiles fill half of the
+ *              GPU, or a quarter of it with fewer than 256 64-wide k-blocks; at
+ *              most 64); otherwise clamped to [1, number of 64-wide k-blocks].
  *   workspace  device memory owned by the caller, 256-byte aligned, at least
  *              gb_splitk_workspace_bytes() bytes (may be NULL when that is 0):
  *              one fp32 accumulator tile per output tile plus the counters.
