@@ -170,13 +170,47 @@ class ClockSampler:
                 "samples": len(inside), "window": "timed region (+-1 s) at 100 ms sampling"}
 
 
+def code_tokens(text: str) -> str:
+    """C++/CUDA source with comments removed and whitespace collapsed (string and
+    character literals kept verbatim): what the compiler sees, not how it is annotated."""
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments and layout ignored), so that recorded
+    counters stay attached to the code they were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_bf16_gemm_persistent_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

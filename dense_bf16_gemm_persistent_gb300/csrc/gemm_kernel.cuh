@@ -13,14 +13,18 @@
 //                       double-buffered fp32 accumulator and tcgen05.commit
 //                       to release each stage once (section "Syncing issues":
 //                       one commit per stage, one per tile).
-//   * warps 4..11    -- epilogue, two warpgroups: tcgen05.ld of 32-column
-//                       chunks, bias, activation, epilogue input (prefetched by
-//                       TMA), bf16 rounding, and a chunked TMA store whose
-//                       shared-memory wait is delayed until the buffer is reused
-//                       (sections "Epilogue inputs" and "TMA store and
-//                       stmatrix").
-//   * registers move from the control warpgroup to the epilogue warpgroups
-//     with setmaxnreg after the role split (section "Register usage/spilling").
+//   * warps 4..7 or 4..11 -- epilogue, one or two warpgroups (template EPI):
+//                       tcgen05.ld of 32-column chunks, bias, activation,
+//                       epilogue input (prefetched by TMA into a per-warp box
+//                       queue), bf16 rounding, and chunked TMA stores from a
+//                       per-warp queue of staging boxes, each reused only after
+//                       its store has read it (sections "Epilogue inputs" and
+//                       "TMA store and stmatrix").  Two warpgroups either share
+//                       every tile's chunks or alternate tiles (ping-pong, one
+//                       TMEM buffer each; section "ping-pong").
+//   * with two epilogue warpgroups, registers move from the control warpgroup
+//     to them with setmaxnreg after the role split (section "Register
+//     usage/spilling").
 //   * all barriers are initialised once, outside the persistent tile loop, and
 //     the ring position comes from a k-block counter that runs on across
 //     tiles (section "Syncing persistent matmuls").
