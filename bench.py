@@ -203,20 +203,21 @@ def code_tokens(text: str) -> str:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code (comments and layout ignored), so that recorded
-    counters stay attached to the code they were taken on."""
+    """Hash of the device code (the kernel headers, comments and layout ignored). Recorded
+    counters stay attached to the code they were taken on; together with the launch plan
+    (recorded beside them) this pins the launch they describe."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_bf16_gemm_persistent_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith(".cuh"):
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode() + b"\0" + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, plan: str | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+    current device code and (when the record names one) the same launch plan; else None."""
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     try:
         kv = {}
@@ -226,6 +227,8 @@ def recorded_traffic(workload: str):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
         if kv.get("source_sha256") != kernel_source_hash():
+            return None
+        if "plan" in kv and plan is not None and kv["plan"] != plan.strip():
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -518,7 +521,7 @@ def run_ours(args, wl: dict):
     peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     alg_bytes = algorithmic_bytes(wl)
-    traffic = recorded_traffic(wl["name"])
+    traffic = recorded_traffic(wl["name"], plan)
     if fl / alg_bytes >= peak * 1e12 / (hbm * 1e9):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                     "traffic": traffic,

@@ -1,5 +1,5 @@
-"""bench.py helpers that need no GPU: the kernel-source hash that keeps recorded ncu
-traffic attached to the code it was measured on."""
+"""bench.py helpers that need no GPU: the device-code hash and launch plan that keep
+recorded ncu traffic attached to the launch it was measured on."""
 import os
 import shutil
 
@@ -25,5 +25,11 @@ def test_recorded_traffic_follows_the_code(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w") == 1234.0
     (csrc / "k.cuh").write_text("// a new comment\n__global__ void k() {\n  int x = 1;\n}\n")
     assert bench.recorded_traffic("w") == 1234.0          # comments and layout: same code
+    (csrc / "host.cu").write_text("int host_side_planner = 1;\n")
+    assert bench.recorded_traffic("w") == 1234.0          # host code is pinned by the plan instead
+    (tmp_path / "profiles" / "traffic_w.txt").write_text(
+        f"dram_bytes_per_launch: 1234\nsource_sha256: {h}\nplan: tile=256x256x64 stages=6\n")
+    assert bench.recorded_traffic("w", "tile=256x256x64 stages=6") == 1234.0
+    assert bench.recorded_traffic("w", "tile=256x256x64 stages=5") is None   # another launch
     (csrc / "k.cuh").write_text("__global__ void k() { int x = 2; }\n")
-    assert bench.recorded_traffic("w") is None            # changed code: counters no longer apply
+    assert bench.recorded_traffic("w", "tile=256x256x64 stages=6") is None   # changed device code
