@@ -15,7 +15,7 @@ from tests.gpu_util import assert_close, bits
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-N_CASES = 96
+N_CASES = 256
 MAX_MACS = 1 << 27  # keeps every oracle call well under a second
 
 CONFIG_ITEMS = ["pair=0", "pair=1", "epi=1", "epi=2", "pingpong=1", "pingpong=0", "boxes=2", "boxes=5",
