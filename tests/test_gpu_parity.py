@@ -351,6 +351,23 @@ def test_pingpong_is_ignored_by_split_k_and_refused_with_one_warpgroup():
         run_linear(A, B)
 
 
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("rem", [1, 8, 17, 100, 128, 129, 240, 255])
+def test_ragged_last_tile_column(pair, rem):
+    """A ragged last tile column at every width boundary (one column, a box, half a pair's
+    B rows, one past half, all but one): bit-exact on integer inputs and against the oracle
+    on random ones, with full tile columns before it on the same accumulator buffers."""
+    gb.set_config(f"pair={pair},grid=2")
+    M, N, K = 300, 512 + rem, 200
+    Ai, Bi = int_tensor((M, K), 180), int_tensor((N, K), 181)
+    Ri = int_tensor((M, N), 182, -4, 4)
+    assert_bitexact(run_linear(Ai, Bi, None, Ri), ref_linear(Ai, Bi, None, Ri), f"int rem={rem}")
+    A = inputs.randn_bf16((M, K), seed=183)
+    B = inputs.randn_bf16((N, K), seed=184, std=1.0 / np.sqrt(K))
+    bias = inputs.randn_bf16((N,), seed=185, std=0.1)
+    assert_close(run_linear(A, B, bias, None, "gelu_tanh"), ref_linear(A, B, bias, None, "gelu_tanh"), f"rem={rem}")
+
+
 def test_short_k_plan_takes_deep_queues():
     """Work items of at most 4 k-blocks get a 3-stage ring, the deepest queues that fit
     and, with at least 4 work items per unit, the ping-pong schedule; long-K items keep
