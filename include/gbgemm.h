@@ -25,9 +25,10 @@
  *
  * Ownership.  All pointers are DEVICE pointers owned by the caller and must
  * stay valid until the work queued on `stream` has finished.  The library
- * allocates no device memory: it keeps only a host-side cache of TMA
- * descriptors and a per-device 32-bit status word in its own static device
- * memory.
+ * allocates no device memory at run time: it keeps a host-side cache of TMA
+ * descriptors, and its own static device memory holds only a 32-bit status
+ * word and the scratch array of gb_gemm_linear_splitk_noalloc (both part of
+ * the loaded module).
  *
  * Synchronisation.  Calls only validate, plan and enqueue on `stream` (a
  * cudaStream_t; NULL means the legacy default stream) and return at once.
