@@ -122,6 +122,25 @@ def test_strided_views_and_offset_d():
     assert torch.all(Dbig[:, :3] == 0) and torch.all(Dbig[:, 3 + N:] == 0)
 
 
+@pytest.mark.parametrize("spec", ["", "epi=1", "epi=2", "pair=0,grid=3", "pingpong=1"])
+@pytest.mark.parametrize("with_r", [False, True])
+def test_bias_only_2_byte_aligned(spec, with_r):
+    """A bias that starts 2 bytes past a 16-byte boundary takes the scalar bias loads
+    (the vector loads need 16-byte alignment): express, paired and general epilogues."""
+    gb.set_config(spec or None)
+    M, N, K = 300, 520, 192
+    A = inputs.randn_bf16((M, K), seed=195)
+    B = inputs.randn_bf16((N, K), seed=196, std=1.0 / np.sqrt(K))
+    bias_big = inputs.randn_bf16((N + 1,), seed=197, std=0.1)
+    bias = bias_big[1:]
+    R = inputs.randn_bf16((M, N), seed=198) if with_r else None
+    bias_dev = bias_big.to(DEV)[1:]
+    assert bias_dev.data_ptr() % 16 == 2
+    D = gb.linear(A.to(DEV), B.to(DEV), bias_dev, None if R is None else R.to(DEV), act="gelu_tanh")
+    gb.device_status()
+    assert_close(bits(D), ref_linear(A, B, bias.contiguous(), R, "gelu_tanh"), f"{spec} R={with_r}")
+
+
 def test_d_aliases_r():
     M, N, K = 260, 384, 96
     A = inputs.randn_bf16((M, K), seed=50)

@@ -165,3 +165,20 @@ def test_queried_workspace_covers_every_epilogue(form, splits):
     ref = oracle.linear(bits(A[rr]), bits(B[cc]), None if bias is None else bits(bias)[c],
                         None if R is None else bits(R[rr][:, cc]), act)
     assert_close(bits(D[rr][:, cc]), ref, f"{form} {plan}")
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_split_k_with_d_aliasing_r(splits):
+    """D == R through the split-K entry point: the last split of each slab reads R and
+    writes D for the same elements, after every partial is in."""
+    M, N, K = 127, 200, 8192
+    A = inputs.randn_bf16((M, K), seed=210)
+    B = inputs.randn_bf16((N, K), seed=211, std=1.0 / np.sqrt(K))
+    bias = inputs.randn_bf16((N,), seed=212, std=0.1)
+    R = inputs.randn_bf16((M, N), seed=213)
+    ref = oracle.linear(bits(A), bits(B), bits(bias), bits(R), "silu")
+    RD = R.to(DEV).clone()
+    gb.linear(A.to(DEV), B.to(DEV), bias.to(DEV), RD, act="silu", out=RD, split_k=splits or "auto")
+    gb.device_status()
+    assert int(gb.last_plan().split("splits=")[1].split()[0]) > 1, gb.last_plan()
+    assert_close(bits(RD), ref, f"split-K D == R, splits={splits}")
