@@ -141,6 +141,32 @@ def test_bias_only_2_byte_aligned(spec, with_r):
     assert_close(bits(D), ref_linear(A, B, bias.contiguous(), R, "gelu_tanh"), f"{spec} R={with_r}")
 
 
+@pytest.mark.parametrize("spec", ["", "epi=1", "pair=0,grid=3", "pingpong=1", "boxes=8"])
+@pytest.mark.parametrize("K", [64, 520])
+def test_unaligned_r_with_aligned_d(spec, K):
+    """R rows only 2-byte aligned (R read through the shared-memory transpose) while D
+    rows are 16-byte aligned (D stored by TMA), and the reverse."""
+    gb.set_config(spec or None)
+    M, N = 300, 520
+    A = inputs.randn_bf16((M, K), seed=200)
+    B = inputs.randn_bf16((N, K), seed=201, std=1.0 / np.sqrt(K))
+    Rbig = inputs.randn_bf16((M, N + 1), seed=202)
+    R = Rbig[:, 1:]
+    Rd = Rbig.to(DEV)[:, 1:]
+    D = gb.linear(A.to(DEV), B.to(DEV), None, Rd, act="relu")
+    gb.device_status()
+    plan = gb.last_plan()
+    assert "r_load=ld.transposed" in plan and "d_store=tma" in plan, plan
+    ref = ref_linear(A, B, None, R.contiguous(), "relu")
+    assert_close(bits(D), ref, f"{spec} {plan}")
+    Dbig = torch.zeros((M, N + 1), dtype=torch.bfloat16, device=DEV)
+    gb.linear(A.to(DEV), B.to(DEV), None, R.contiguous().to(DEV), act="relu", out=Dbig[:, 1:])
+    gb.device_status()
+    plan = gb.last_plan()
+    assert "r_load=tma" in plan and "d_store=st.transposed" in plan, plan
+    assert_close(bits(Dbig[:, 1:]), ref, f"{spec} {plan}")
+
+
 def test_d_aliases_r():
     M, N, K = 260, 384, 96
     A = inputs.randn_bf16((M, K), seed=50)
