@@ -182,3 +182,18 @@ def test_split_k_with_d_aliasing_r(splits):
     gb.device_status()
     assert int(gb.last_plan().split("splits=")[1].split()[0]) > 1, gb.last_plan()
     assert_close(bits(RD), ref, f"split-K D == R, splits={splits}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 65536), (1, 1, 8), (2, 3, 40000), (1, 200, 16384)])
+def test_tiny_outputs_long_k(M, N, K):
+    """One or a few output elements over a long K: a single tile split into many K ranges
+    (the automatic count caps at 64), all reducing into the same slab; and integer inputs
+    bit-exact."""
+    (A, B, b, r), ref = _lin(M, N, K, seed=220, bias=True, R=True, act="relu")
+    D = gb.linear(A, B, b, r, act="relu", split_k="auto")
+    gb.device_status()
+    assert_close(bits(D), ref, f"{M}x{N}x{K} {gb.last_plan()}")
+    Ai, Bi = int_tensor((M, K), 221, -1, 1), int_tensor((N, K), 222, -1, 1)
+    Di = gb.linear(Ai.to(DEV), Bi.to(DEV), split_k="auto")
+    gb.device_status()
+    assert_bitexact(bits(Di), oracle.linear(bits(Ai), bits(Bi)), f"int {M}x{N}x{K}")
