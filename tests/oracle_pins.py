@@ -105,6 +105,24 @@ def check_acc_error_bound(o) -> None:
         assert np.allclose(y, exact, rtol=1e-12, atol=1e-12 * absum.max())
 
 
+def check_fp32_sequential_sum(o) -> None:
+    """The sum is a recursive binary32 sum in ascending k, not a more exact or reordered
+    one.  2^24 + 1 rounds back to 2^24 in binary32 (a tie, to even), so
+    [2^24, 1, -2^24] . [1, 1, 1] is 0 summed in that order; the exact value is 1, and
+    so is the descending-order sum (-2^24 + 1 = -16777215 exactly, + 2^24 = 1)."""
+    A = lib_round_bf16(np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)], [1.0, 2.0 ** 24, -(2.0 ** 24)]], dtype=np.float32))
+    B = lib_round_bf16(np.ones((1, 3), dtype=np.float32))
+    acc = o.acc_f32(A, B)
+    assert float(acc[0, 0]) == 0.0, float(acc[0, 0])   # the 1 is absorbed
+    assert float(acc[1, 0]) == 0.0, float(acc[1, 0])   # 1 + 2^24 rounds to 2^24 as well
+    np.testing.assert_array_equal(o.linear(A, B), lib_round_bf16(np.zeros((2, 1), dtype=np.float32)))
+    # many small terms after a large one are each absorbed
+    row = np.concatenate([[2.0 ** 24], np.ones(50), [-(2.0 ** 24)]]).astype(np.float32)[None, :]
+    A2 = lib_round_bf16(row)
+    B2 = lib_round_bf16(np.ones((1, row.shape[1]), dtype=np.float32))
+    assert float(o.acc_f32(A2, B2)[0, 0]) == 0.0
+
+
 def check_integer_exact(o) -> None:
     """Small-integer operands: every partial sum is an exact integer in fp32, so the
     result is the exact integer product rounded once to bf16 -- bit for bit."""
@@ -284,12 +302,19 @@ def check_ffn(o) -> None:
 
 
 def check_leading_dims(o) -> None:
-    """Strided views (leading dimension > K) give the same bits as packed copies."""
+    """Strided views (leading dimension > row length: A, B and the epilogue input R)
+    give the same bits as packed copies."""
     rng = np.random.default_rng(18)
     Abig = rand_bf16(rng, (10, 70))
     Bbig = rand_bf16(rng, (6, 80))
     A, B = Abig[:, 3:53], Bbig[:, 10:60]
     np.testing.assert_array_equal(o.linear(A, B), o.linear(np.ascontiguousarray(A), np.ascontiguousarray(B)))
+    Rbig = rand_bf16(rng, (10, 15))
+    R = Rbig[:, 4:10]                                   # leading dimension 15 > N = 6
+    bias = rand_bf16(rng, (6,), 0.1)
+    np.testing.assert_array_equal(o.linear(A, B, bias=bias, R=R, act="silu"),
+                                  o.linear(np.ascontiguousarray(A), np.ascontiguousarray(B), bias=bias,
+                                           R=np.ascontiguousarray(R), act="silu"))
 
 
 def check_preact_output(o) -> None:
@@ -314,7 +339,8 @@ def check_preact_output(o) -> None:
     np.testing.assert_array_equal(D2, Z2)
 
 
-ALL_CHECKS = [check_f32_to_bf16, check_f64_to_bf16, check_acc_error_bound, check_integer_exact,
+ALL_CHECKS = [check_f32_to_bf16, check_f64_to_bf16, check_acc_error_bound, check_fp32_sequential_sum,
+              check_integer_exact,
               check_transpose_and_index, check_identity_b, check_zero_bias_and_linearity,
               check_bias_broadcast_and_residual, check_k_zero, check_activation_closed_forms,
               check_activation_vs_library, check_epilogue_order, check_ffn, check_leading_dims,

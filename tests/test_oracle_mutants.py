@@ -42,6 +42,11 @@ MUTANTS = [
     ("preact_no_bias", "            if (bias) v = v + bf16_to_f32(bias[n]);\n            Z[m * ldz + n] = f32_to_bf16(v);",
      "            Z[m * ldz + n] = f32_to_bf16(v);\n            if (bias) v = v + bf16_to_f32(bias[n]);", 0),
     ("f64_dot_drop", "for (int64_t k = 0; k < K; ++k) {\n        double p", "for (int64_t k = 1; k < K; ++k) {\n        double p", 0),
+    ("acc_in_double", "    float acc = 0.0f;\n    for (int64_t k = 0; k < K; ++k) {\n        float p",
+     "    double acc = 0.0;\n    for (int64_t k = 0; k < K; ++k) {\n        float p", 0),
+    ("sum_descending", "for (int64_t k = 0; k < K; ++k) {\n        float p", "for (int64_t k = K - 1; k >= 0; --k) {\n        float p", 0),
+    ("lda_ignored", "float v = dot_f32(A + m * lda, B + n * ldb, K);", "float v = dot_f32(A + m * K, B + n * ldb, K);", 0),
+    ("ldr_ignored", "if (R) v = v + bf16_to_f32(R[m * ldr + n]);", "if (R) v = v + bf16_to_f32(R[m * N + n]);", 0),
 ]
 
 
