@@ -44,6 +44,9 @@ WORKLOADS = {
                   name="plain_256x384x512"),
     "mlp_noepi": dict(M=8192, N=14336, K=4096, kind="linear", act="none", bias=False, residual=False,
                       name="linear_noepi_8192x14336x4096"),
+    # the MLP linear storing also its pre-activation Z = bf16(X.W^T + bias) (second output)
+    "mlp_preact": dict(M=8192, N=14336, K=4096, kind="linear", act="gelu_tanh", bias=True, residual=False,
+                       preact=True, name="mlp_preact_8192x14336x4096"),
     "int64": dict(M=65536, N=4096, K=65536, kind="linear", act="none", bias=False, residual=False,
                   name="int64_65536x4096x65536"),
 }
@@ -256,9 +259,10 @@ def make_inputs(wl: dict, device):
 
 
 def algorithmic_bytes(wl: dict) -> float:
-    """One read of every input and one write of D (bf16)."""
+    """One read of every input and one write of D (and of Z, the pre-activation, when
+    the workload stores it), all bf16."""
     M, N, K = wl["M"], wl["N"], wl["K"]
-    b = M * K + N * K * (2 if wl["kind"] == "ffn" else 1) + M * N
+    b = M * K + N * K * (2 if wl["kind"] == "ffn" else 1) + M * N * (2 if wl.get("preact") else 1)
     if wl.get("bias"):
         b += N
     if wl.get("residual"):
@@ -275,6 +279,11 @@ def step_fn(wl: dict, t: dict, out, workspace=None, stream=None):
     import dense_bf16_gemm_persistent_gb300 as gb
     if wl["kind"] == "ffn":
         return lambda: gb.ffn_gated(t["X"], t["W1"], t["W3"], out=out, stream=stream)
+    if wl.get("preact"):
+        import torch
+        z = torch.empty_like(out)
+        return lambda: gb.linear_preact(t["A"], t["B"], t.get("bias"), t.get("R"), act=t["act"], out=out,
+                                        preact=z, stream=stream)
     split = wl.get("split_k")
     return lambda: gb.linear(t["A"], t["B"], t.get("bias"), t.get("R"), act=t["act"], out=out, split_k=split,
                              workspace=workspace, stream=stream)
@@ -300,7 +309,8 @@ def oracle_sample_run(wl: dict, h: dict, rows: int):
         return time.perf_counter() - t0, 4.0 * rows * N * K, oracle.num_threads()
     R = h.get("R")
     t0 = time.perf_counter()
-    oracle.linear(h["A"][:rows], h["B"], h.get("bias"), None if R is None else R[:rows], h["act"])
+    run = oracle.linear_preact if wl.get("preact") else oracle.linear
+    run(h["A"][:rows], h["B"], h.get("bias"), None if R is None else R[:rows], h["act"])
     return time.perf_counter() - t0, 2.0 * rows * N * K, oracle.num_threads()
 
 
@@ -357,7 +367,7 @@ def config_of(wl: dict) -> dict:
     elif wl.get("residual"):
         epi = "acc + R"
     elif wl.get("bias"):
-        epi = f"{wl['act']}(acc + bias)"
+        epi = f"{wl['act']}(acc + bias)" + (", and Z = acc + bias" if wl.get("preact") else "")
     else:
         epi = "none"
     cfg = {"workload": wl["name"], "M": wl["M"], "N": wl["N"], "K": wl["K"], "epilogue": epi,

@@ -552,15 +552,17 @@ gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitR
     // long-K shapes, with or without an aligned epilogue input (K >= 4096); two are up
     // to 1.4x faster on short K (<= 16 k-blocks), on split-K plans over few tiles, and
     // with rows that go through the shared-memory transposes (N = 4099: two win by 12 %
-    // at K = 4096; at K = 65536 the two were within run-to-run noise).  A second output
-    // doubles the stores: two.
+    // at K = 4096; at K = 65536 the two were within run-to-run noise).  An epilogue input
+    // or a second output needs two below 64 k-blocks; above, one was faster (MLP with its
+    // pre-activation stored, 8192x14336x4096: 1538 against 1515 TFLOP/s).
     const int64_t kb = cdiv(pr.k, gb::kBK);
     const bool d_rows_aligned = aligned16(pr.d) && pr.ldd % 8 == 0;
     const bool r_rows_aligned = !pr.r || (aligned16(pr.r) && pr.ldr % 8 == 0);
+    const bool z_rows_aligned = !pr.z || (aligned16(pr.z) && pr.ldz % 8 == 0);
     const int64_t tiles_est = cdiv(pr.m, pair ? 2 * gb::kBM : gb::kBM) * cdiv(pr.n, bn);
     const bool few_tiles_split = sr.allowed && 2 * tiles_est <= info.sms;
-    const bool heavy_epilogue = kb <= 16 || few_tiles_split || pr.z ||
-                                !d_rows_aligned || !r_rows_aligned || (pr.r && kb < 64);
+    const bool heavy_epilogue = kb <= 16 || few_tiles_split || !d_rows_aligned || !r_rows_aligned ||
+                                !z_rows_aligned || ((pr.r || pr.z) && kb < 64);
     if (cfg.pingpong == 1 && cfg.epi == 1)
         return fail(GB_ERR_INVALID_ARG, "pingpong=1 needs two epilogue warpgroups (epi=2)");
     const int epi = cfg.pingpong == 1 ? 2 : cfg.epi > 0 ? cfg.epi : (heavy_epilogue ? 2 : 1);

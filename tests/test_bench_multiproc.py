@@ -84,3 +84,7 @@ def test_workload_names_and_bytes():
     rg = bench.workload("ragged:127,96,64")
     assert rg["residual"] and rg["split_k"] == "auto" and bench.needs_l2_flush(rg)
     assert not bench.needs_l2_flush(wl)
+    pre = bench.workload("mlp_preact")
+    assert bench.flops_per_step(pre) == bench.flops_per_step(wl)
+    assert bench.algorithmic_bytes(pre) == bench.algorithmic_bytes(wl) + 2.0 * 8192 * 14336   # Z written too
+    assert "Z = acc + bias" in bench.config_of(pre)["epilogue"]
