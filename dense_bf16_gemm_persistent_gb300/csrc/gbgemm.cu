@@ -595,6 +595,7 @@ void* g_scratch_addr[64] = {};
 // code the array's name is only a host-side stand-in, so the address is looked
 // up once per device (with that device current) and cached.
 gb_status_t static_scratch_address(int dev, void** out) {
+    if (dev < 0 || dev >= 64) return fail(GB_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
         void* ptr = nullptr;
@@ -705,29 +706,18 @@ gb_status_t gb_gemm_linear_splitk_noalloc(const void* A, int64_t lda, const void
     void* scratch = nullptr;
     if ((st = static_scratch_address(dev, &scratch)) != GB_OK) return st;
 
+    // Every split count above 1 needs the same scratch (one fp32 accumulator tile per
+    // output tile, plus counters), so a plan that does not fit can only run unsplit.
     size_t need = 0;
     if ((st = splitk_bytes_for(pr, splits, &need)) != GB_OK) return st;
     if (need > kStaticScratchBytes) {
-        if (splits > 0)
+        if (splits > 1)
             return fail(GB_ERR_UNSUPPORTED,
-                        "split-K with %d splits needs %zu bytes of scratch, more than the %zu-byte static scratch "
-                        "of gb_gemm_linear_splitk_noalloc; use fewer splits or gb_gemm_linear_splitk",
-                        splits, need, kStaticScratchBytes);
-        // Automatic split count: the largest one whose partials fit the static scratch.
-        const int kb = static_cast<int>(cdiv(pr.k, gb::kBK));
-        int lo = 1, hi = kb;
-        while (lo < hi) {
-            const int mid = lo + (hi - lo + 1) / 2;
-            size_t b = 0;
-            if ((st = splitk_bytes_for(pr, mid, &b)) != GB_OK) return st;
-            if (b <= kStaticScratchBytes) lo = mid;
-            else hi = mid - 1;
-        }
-        splits = lo;
-        if ((st = splitk_bytes_for(pr, splits, &need)) != GB_OK) return st;
-        if (need > kStaticScratchBytes)
-            return fail(GB_ERR_UNSUPPORTED, "problem needs %zu bytes of split-K scratch, more than the %zu-byte static "
-                        "scratch", need, kStaticScratchBytes);
+                        "split-K of this problem needs %zu bytes of scratch, more than the %zu-byte static scratch "
+                        "of gb_gemm_linear_splitk_noalloc, for any split count above 1; use splits=1 or "
+                        "gb_gemm_linear_splitk with a workspace",
+                        need, kStaticScratchBytes);
+        splits = 1;  // automatic: the partials do not fit, so the call runs unsplit
     }
     SplitReq sr;
     sr.allowed = true;

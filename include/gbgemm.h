@@ -186,10 +186,13 @@ GB_API gb_status_t gb_splitk_workspace_bytes(int ffn, int64_t M, int64_t N, int6
  * for example a framework whose own caching allocator must own every device
  * allocation, or a serving runtime that reserves all memory at start-up and may
  * not allocate while it handles requests.
- *   splits  > 0: used as given (clamped as in gb_gemm_linear_splitk); if its
- *           partials do not fit the static scratch the call returns
- *           GB_ERR_UNSUPPORTED with the bytes needed and allowed.
- *           <= 0: automatic, lowered if needed until the partials fit.
+ *   splits  > 0: used as given (clamped as in gb_gemm_linear_splitk).  Every
+ *           split count above 1 needs the same scratch (one fp32 tile per
+ *           output tile plus counters); if that does not fit the static
+ *           scratch the call returns GB_ERR_UNSUPPORTED with the bytes needed
+ *           and allowed (splits = 1 always fits: it needs none).
+ *           <= 0: automatic; when the automatic plan's partials do not fit,
+ *           the call runs unsplit (splits = 1) instead.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current and caches it; make that first
  * call before any stream capture.  Every call on a device shares the one array,

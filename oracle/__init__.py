@@ -75,10 +75,23 @@ class Oracle:
         lib.oracle_act_f64_array.argtypes = [ctypes.c_int, p, p, i64]
         lib.oracle_f32_to_bf16_array.argtypes = [p, p, i64]
         lib.oracle_f64_to_bf16_array.argtypes = [p, p, i64]
+        lib.oracle_dact_f32.argtypes = [p, i64, p, i64, p, i64, ctypes.c_int, p, i64, i64, i64, i64]
+        lib.oracle_dact_f64.argtypes = [p, i64, p, i64, p, i64, ctypes.c_int, p, i64, i64, i64, i64]
+        lib.oracle_dact_f32_array.argtypes = [ctypes.c_int, p, p, i64]
+        lib.oracle_dact_f64_array.argtypes = [ctypes.c_int, p, p, i64]
+        lib.oracle_linear_entries_f32.argtypes = [p, p, i64, p, p, ctypes.c_int, p, i64]
+        lib.oracle_linear_entries_f64.argtypes = [p, p, i64, p, p, ctypes.c_int, p, i64]
+        lib.oracle_ffn_entries_f32.argtypes = [p, p, p, i64, p, i64]
+        lib.oracle_ffn_entries_f64.argtypes = [p, p, p, i64, p, i64]
+        lib.oracle_dact_entries_f32.argtypes = [p, p, i64, p, ctypes.c_int, p, i64]
+        lib.oracle_dact_entries_f64.argtypes = [p, p, i64, p, ctypes.c_int, p, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
         for name in ("oracle_linear_f32", "oracle_linear_f64", "oracle_linear_preact_f32", "oracle_ffn_f32",
-                     "oracle_ffn_f64",
+                     "oracle_ffn_f64", "oracle_dact_f32", "oracle_dact_f64",
                      "oracle_acc_f32", "oracle_act_f32_array", "oracle_act_f64_array",
+                     "oracle_dact_f32_array", "oracle_dact_f64_array",
+                     "oracle_linear_entries_f32", "oracle_linear_entries_f64", "oracle_ffn_entries_f32",
+                     "oracle_ffn_entries_f64", "oracle_dact_entries_f32", "oracle_dact_entries_f64",
                      "oracle_f32_to_bf16_array", "oracle_f64_to_bf16_array"):
             getattr(lib, name).restype = None
         self.lib = lib
@@ -152,6 +165,87 @@ class Oracle:
         self.lib.oracle_ffn_f64(px, ldx, p1, ld1, p3, ld3, Y.ctypes.data, N, M, N, K)
         return Y
 
+    def dact(self, dY, W, Z, act: str = "none"):
+        """D[M,K] = bf16( (dY.W) * act'(Z) ): dY [M,N], W [N,K] (the forward weight), Z [M,K];
+        the fp32 sum runs over n in ascending order; bf16 bits out."""
+        M, N = dY.shape
+        if W.ndim != 2 or W.shape[0] != N:
+            raise ValueError("W must have shape (N, K)")
+        K = W.shape[1]
+        if Z.shape != (M, K):
+            raise ValueError("Z must have shape (M, K)")
+        D = np.empty((M, K), dtype=np.uint16)
+        py, ldy = _mat(dY, "dY")
+        pw, ldw = _mat(W, "W")
+        pz, ldz = _mat(Z, "Z")
+        self.lib.oracle_dact_f32(py, ldy, pw, ldw, pz, ldz, ACT[act], D.ctypes.data, K, M, N, K)
+        return D
+
+    def dact_f64(self, dY, W, Z, act: str = "none"):
+        M, N = dY.shape
+        K = W.shape[1]
+        if W.shape[0] != N or Z.shape != (M, K):
+            raise ValueError("shapes: dY (M,N), W (N,K), Z (M,K)")
+        Y = np.empty((M, K), dtype=np.float64)
+        py, ldy = _mat(dY, "dY")
+        pw, ldw = _mat(W, "W")
+        pz, ldz = _mat(Z, "Z")
+        self.lib.oracle_dact_f64(py, ldy, pw, ldw, pz, ldz, ACT[act], Y.ctypes.data, K, M, N, K)
+        return Y
+
+    @staticmethod
+    def _rows(x, name, P=None, K=None):
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        if x.ndim != 2 or (P is not None and x.shape[0] != P) or (K is not None and x.shape[1] != K):
+            raise ValueError(f"{name}: expected shape ({P}, {K}), got {x.shape}")
+        return x
+
+    @staticmethod
+    def _vals(x, name, P):
+        if x is None:
+            return None, 0
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        if x.shape != (P,):
+            raise ValueError(f"{name}: expected shape ({P},)")
+        return x, x.ctypes.data
+
+    def linear_entries(self, Arows, Brows, bias=None, R=None, act: str = "none", f64: bool = False):
+        """Single entries of linear(): entry p = row p of Arows with row p of Brows, plus the
+        entry's bias and R values (each of shape (P,), or None)."""
+        A = self._rows(Arows, "Arows")
+        P, K = A.shape
+        B = self._rows(Brows, "Brows", P, K)
+        bias, pbias = self._vals(bias, "bias", P)
+        R, pr = self._vals(R, "R", P)
+        out = np.empty(P, dtype=np.float64 if f64 else np.uint16)
+        fn = self.lib.oracle_linear_entries_f64 if f64 else self.lib.oracle_linear_entries_f32
+        fn(A.ctypes.data, B.ctypes.data, K, pbias, pr, ACT[act], out.ctypes.data, P)
+        return out
+
+    def ffn_entries(self, Xrows, W1rows, W3rows, f64: bool = False):
+        X = self._rows(Xrows, "Xrows")
+        P, K = X.shape
+        W1 = self._rows(W1rows, "W1rows", P, K)
+        W3 = self._rows(W3rows, "W3rows", P, K)
+        out = np.empty(P, dtype=np.float64 if f64 else np.uint16)
+        fn = self.lib.oracle_ffn_entries_f64 if f64 else self.lib.oracle_ffn_entries_f32
+        fn(X.ctypes.data, W1.ctypes.data, W3.ctypes.data, K, out.ctypes.data, P)
+        return out
+
+    def dact_entries(self, dYrows, Wcols, Z, act: str = "none", f64: bool = False):
+        """Single entries of dact(): entry p = row p of dYrows with column p of W gathered as
+        row p of Wcols (both length N), times act' of the entry's Z value (shape (P,))."""
+        Y = self._rows(dYrows, "dYrows")
+        P, N = Y.shape
+        W = self._rows(Wcols, "Wcols", P, N)
+        Z, pz = self._vals(Z, "Z", P)
+        if Z is None:
+            raise ValueError("Z is required")
+        out = np.empty(P, dtype=np.float64 if f64 else np.uint16)
+        fn = self.lib.oracle_dact_entries_f64 if f64 else self.lib.oracle_dact_entries_f32
+        fn(Y.ctypes.data, W.ctypes.data, N, pz, ACT[act], out.ctypes.data, P)
+        return out
+
     def acc_f32(self, A, B):
         """Raw fp32 accumulator A.B^T (ascending k, no FMA), no epilogue."""
         M, N, K = self._dims(A, B)
@@ -171,6 +265,19 @@ class Oracle:
         x = np.ascontiguousarray(x, dtype=np.float64)
         y = np.empty_like(x)
         self.lib.oracle_act_f64_array(ACT[act], x.ctypes.data, y.ctypes.data, x.size)
+        return y
+
+    def dact_f32_values(self, act: str, x):
+        """act'(x) in fp32 (the derivative the dact epilogue multiplies by)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty_like(x)
+        self.lib.oracle_dact_f32_array(ACT[act], x.ctypes.data, y.ctypes.data, x.size)
+        return y
+
+    def dact_f64_values(self, act: str, x):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        y = np.empty_like(x)
+        self.lib.oracle_dact_f64_array(ACT[act], x.ctypes.data, y.ctypes.data, x.size)
         return y
 
     def f32_to_bf16(self, x):
@@ -216,6 +323,26 @@ def ffn_gated(X, W1, W3):
 
 def ffn_gated_f64(X, W1, W3):
     return default().ffn_gated_f64(X, W1, W3)
+
+
+def dact(dY, W, Z, act: str = "none"):
+    return default().dact(dY, W, Z, act)
+
+
+def dact_f64(dY, W, Z, act: str = "none"):
+    return default().dact_f64(dY, W, Z, act)
+
+
+def linear_entries(Arows, Brows, bias=None, R=None, act: str = "none", f64: bool = False):
+    return default().linear_entries(Arows, Brows, bias, R, act, f64)
+
+
+def ffn_entries(Xrows, W1rows, W3rows, f64: bool = False):
+    return default().ffn_entries(Xrows, W1rows, W3rows, f64)
+
+
+def dact_entries(dYrows, Wcols, Z, act: str = "none", f64: bool = False):
+    return default().dact_entries(dYrows, Wcols, Z, act, f64)
 
 
 def acc_f32(A, B):

@@ -24,10 +24,25 @@
  *              optional second output (pre-activation): Z[m][n] = bf16_rne(acc + bias)
  *   ffn    :   a1 = acc(X, W1);  a3 = acc(X, W3);
  *              D[m][n] = bf16_rne( silu(a1) * a3 )
+ *   dact   :   the activation-gradient product of a linear layer's backward pass
+ *              (the consumer of the stored pre-activation Z):
+ *              g[m][k] = sum_{n=0}^{N-1} f32(dY[m][n]) * f32(W[n][k])   (fp32, ascending n)
+ *              D[m][k] = bf16_rne( g[m][k] * act'(f32(Z[m][k])) )
+ *              with W the layer's [N,K] weight as the forward pass uses it.
  *
  *   act: 0 none, 1 GELU (tanh form, Hendrycks & Gimpel 2016:
  *        0.5 x (1 + tanh( sqrt(2/pi) (x + 0.044715 x^3) ))),
  *        2 SiLU (x / (1 + e^-x)), 3 ReLU (max(x, 0)).
+ *   act' (derivatives, by the chain rule on the forms above):
+ *        none 1;  ReLU 1 if x > 0 else 0;
+ *        SiLU s (1 + x (1 - s)) with s = 1 / (1 + e^-x);
+ *        GELU 0.5 (1 + t) + 0.5 x (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
+ *             with t = tanh( sqrt(2/pi) (x + 0.044715 x^3) ).
+ *
+ * The *_entries functions evaluate the same definitions at a list of single
+ * output entries, given each entry's operand rows gathered by the caller (row i
+ * of A with row j of B; for dact row m of dY with column k of W): the checks of
+ * outputs too large for the full oracle sample independent (i, j) pairs.
  *
  * Readings where the pages are silent: the activation is applied before the
  * epilogue input is added (act(acc + bias) + R); every epilogue step is fp32
@@ -126,6 +141,42 @@ static inline double act_f64(int act, double x) {
     }
 }
 
+static inline float dact_f32(int act, float x) {
+    switch (act) {
+    case ORACLE_ACT_NONE: return 1.0f;
+    case ORACLE_ACT_GELU_TANH: {
+        const float c = 0.7978845608028654f; /* sqrt(2/pi) */
+        const float a = 0.044715f;
+        float t = tanhf(c * (x + a * x * x * x));
+        return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * c * (1.0f + 3.0f * a * x * x);
+    }
+    case ORACLE_ACT_SILU: {
+        float sg = 1.0f / (1.0f + expf(-x));
+        return sg * (1.0f + x * (1.0f - sg));
+    }
+    case ORACLE_ACT_RELU: return x > 0.0f ? 1.0f : 0.0f;
+    default: return NAN;
+    }
+}
+
+static inline double dact_f64(int act, double x) {
+    switch (act) {
+    case ORACLE_ACT_NONE: return 1.0;
+    case ORACLE_ACT_GELU_TANH: {
+        const double c = 0.79788456080286535588; /* sqrt(2/pi) */
+        const double a = 0.044715;
+        double t = tanh(c * (x + a * x * x * x));
+        return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * a * x * x);
+    }
+    case ORACLE_ACT_SILU: {
+        double sg = 1.0 / (1.0 + exp(-x));
+        return sg * (1.0 + x * (1.0 - sg));
+    }
+    case ORACLE_ACT_RELU: return x > 0.0 ? 1.0 : 0.0;
+    default: return NAN;
+    }
+}
+
 float oracle_act_f32(int act, float x) { return act_f32(act, x); }
 double oracle_act_f64(int act, double x) { return act_f64(act, x); }
 
@@ -135,6 +186,14 @@ void oracle_act_f32_array(int act, const float* x, float* y, int64_t n) {
 
 void oracle_act_f64_array(int act, const double* x, double* y, int64_t n) {
     for (int64_t i = 0; i < n; ++i) y[i] = act_f64(act, x[i]);
+}
+
+void oracle_dact_f32_array(int act, const float* x, float* y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = dact_f32(act, x[i]);
+}
+
+void oracle_dact_f64_array(int act, const double* x, double* y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = dact_f64(act, x[i]);
 }
 
 void oracle_f32_to_bf16_array(const float* x, uint16_t* y, int64_t n) {
@@ -151,6 +210,25 @@ static float dot_f32(const uint16_t* a, const uint16_t* b, int64_t K) {
     float acc = 0.0f;
     for (int64_t k = 0; k < K; ++k) {
         float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k]);
+        acc = acc + p;
+    }
+    return acc;
+}
+
+/* The same sum with the second operand read at a stride (a column of a row-major matrix). */
+static float dot_f32_strided(const uint16_t* a, const uint16_t* b, int64_t stride, int64_t K) {
+    float acc = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+        float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k * stride]);
+        acc = acc + p;
+    }
+    return acc;
+}
+
+static double dot_f64_strided(const uint16_t* a, const uint16_t* b, int64_t stride, int64_t K) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = (double)bf16_to_f32(a[k]) * (double)bf16_to_f32(b[k * stride]);
         acc = acc + p;
     }
     return acc;
@@ -251,6 +329,105 @@ void oracle_ffn_f64(const uint16_t* X, int64_t ldx, const uint16_t* W1, int64_t 
             double a3 = dot_f64(X + m * ldx, W3 + n * ldw3, K);
             Y[m * ldy + n] = act_f64(ORACLE_ACT_SILU, a1) * a3;
         }
+    }
+}
+
+/* ---- activation gradient: D = bf16( (dY.W) * act'(Z) ) ---------------------------- */
+
+/* dY [M,N], W [N,K] (the forward weight), Z [M,K]: the contraction runs over n. */
+void oracle_dact_f32(const uint16_t* dY, int64_t lddy, const uint16_t* W, int64_t ldw,
+                     const uint16_t* Z, int64_t ldz, int act,
+                     uint16_t* D, int64_t ldd, int64_t M, int64_t N, int64_t K) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) {
+            float g = dot_f32_strided(dY + m * lddy, W + k, ldw, N);
+            float v = g * dact_f32(act, bf16_to_f32(Z[m * ldz + k]));
+            D[m * ldd + k] = f32_to_bf16(v);
+        }
+    }
+}
+
+void oracle_dact_f64(const uint16_t* dY, int64_t lddy, const uint16_t* W, int64_t ldw,
+                     const uint16_t* Z, int64_t ldz, int act,
+                     double* Y, int64_t ldy, int64_t M, int64_t N, int64_t K) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) {
+            double g = dot_f64_strided(dY + m * lddy, W + k, ldw, N);
+            Y[m * ldy + k] = g * dact_f64(act, (double)bf16_to_f32(Z[m * ldz + k]));
+        }
+    }
+}
+
+/* ---- single entries: the definitions above at P listed output entries ----------------- */
+
+/* Entry p of linear: row p of A (length K) with row p of B; bias and R are the
+ * entry's own values (NULL: none).  out[p] = bf16(act(dot + bias[p]) + R[p]). */
+void oracle_linear_entries_f32(const uint16_t* A, const uint16_t* B, int64_t K,
+                               const uint16_t* bias, const uint16_t* R, int act,
+                               uint16_t* out, int64_t P) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        float v = dot_f32(A + p * K, B + p * K, K);
+        if (bias) v = v + bf16_to_f32(bias[p]);
+        v = act_f32(act, v);
+        if (R) v = v + bf16_to_f32(R[p]);
+        out[p] = f32_to_bf16(v);
+    }
+}
+
+void oracle_linear_entries_f64(const uint16_t* A, const uint16_t* B, int64_t K,
+                               const uint16_t* bias, const uint16_t* R, int act,
+                               double* out, int64_t P) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        double v = dot_f64(A + p * K, B + p * K, K);
+        if (bias) v = v + (double)bf16_to_f32(bias[p]);
+        v = act_f64(act, v);
+        if (R) v = v + (double)bf16_to_f32(R[p]);
+        out[p] = v;
+    }
+}
+
+/* Entry p of the FFN fusion: row p of X with row p of W1 and row p of W3. */
+void oracle_ffn_entries_f32(const uint16_t* X, const uint16_t* W1, const uint16_t* W3, int64_t K,
+                            uint16_t* out, int64_t P) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        float a1 = dot_f32(X + p * K, W1 + p * K, K);
+        float a3 = dot_f32(X + p * K, W3 + p * K, K);
+        out[p] = f32_to_bf16(act_f32(ORACLE_ACT_SILU, a1) * a3);
+    }
+}
+
+void oracle_ffn_entries_f64(const uint16_t* X, const uint16_t* W1, const uint16_t* W3, int64_t K,
+                            double* out, int64_t P) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        double a1 = dot_f64(X + p * K, W1 + p * K, K);
+        double a3 = dot_f64(X + p * K, W3 + p * K, K);
+        out[p] = act_f64(ORACLE_ACT_SILU, a1) * a3;
+    }
+}
+
+/* Entry p of dact: row p of dY (length N) with column p of W gathered as a row
+ * (length N), and the entry's Z value. */
+void oracle_dact_entries_f32(const uint16_t* dY, const uint16_t* Wcol, int64_t N,
+                             const uint16_t* Z, int act, uint16_t* out, int64_t P) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        float g = dot_f32(dY + p * N, Wcol + p * N, N);
+        out[p] = f32_to_bf16(g * dact_f32(act, bf16_to_f32(Z[p])));
+    }
+}
+
+void oracle_dact_entries_f64(const uint16_t* dY, const uint16_t* Wcol, int64_t N,
+                             const uint16_t* Z, int act, double* out, int64_t P) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        double g = dot_f64(dY + p * N, Wcol + p * N, N);
+        out[p] = g * dact_f64(act, (double)bf16_to_f32(Z[p]));
     }
 }
 

@@ -339,9 +339,163 @@ def check_preact_output(o) -> None:
     np.testing.assert_array_equal(D2, Z2)
 
 
+# ---- activation gradient (backward pass consumer of the pre-activation) --------------------
+
+def check_dact_closed_forms(o) -> None:
+    """act'(0) = 1/2 for GELU and SiLU; ReLU' is the step with 0 at 0; the identity's
+    derivative is 1; GELU' and SiLU' tend to 1 for large x and to 0 for very negative x."""
+    z = np.array([0.0], np.float32)
+    assert o.dact_f32_values("gelu_tanh", z)[0] == 0.5
+    assert o.dact_f32_values("silu", z)[0] == 0.5
+    np.testing.assert_array_equal(o.dact_f32_values("relu", np.array([-2.0, -0.0, 0.0, 1e-30, 3.0], np.float32)),
+                                  np.array([0, 0, 0, 1, 1], np.float32))
+    np.testing.assert_array_equal(o.dact_f32_values("none", np.array([-5.0, 0.0, 7.0], np.float32)),
+                                  np.ones(3, np.float32))
+    big = np.array([12.0, 30.0, 80.0], np.float32)
+    np.testing.assert_array_equal(o.dact_f32_values("gelu_tanh", big), np.ones(3, np.float32))
+    np.testing.assert_array_equal(o.dact_f32_values("silu", np.array([40.0, 80.0], np.float32)),
+                                  np.ones(2, np.float32))
+    assert np.all(np.abs(o.dact_f32_values("gelu_tanh", -big)) <= 1e-30)
+    assert np.all(np.abs(o.dact_f32_values("silu", np.array([-40.0, -80.0], np.float32))) < 1e-15)
+    # silu'(x) + silu'(-x) = 1 and gelu'(x) + gelu'(-x) = 1 (derivatives of x - f(-x) = f(x))
+    x = np.linspace(-10, 10, 2001)
+    for act in ("silu", "gelu_tanh"):
+        np.testing.assert_allclose(o.dact_f64_values(act, x) + o.dact_f64_values(act, -x), 1.0, rtol=0, atol=1e-12)
+
+
+def check_dact_vs_autograd(o) -> None:
+    """act' against torch autograd of torch's own float64 activations at 10^4 points,
+    and against central finite differences of the oracle's float64 activations."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal(9000) * 4.0, np.linspace(-20, 20, 1000)])
+    x = x[np.abs(x) > 1e-3]  # keep ReLU's kink out of the finite differences
+    fns = {"gelu_tanh": lambda t: torch.nn.functional.gelu(t, approximate="tanh"),
+           "silu": torch.nn.functional.silu, "relu": torch.relu, "none": lambda t: t * 1.0}
+    for act, fn in fns.items():
+        t = torch.from_numpy(x.copy()).requires_grad_(True)
+        fn(t).sum().backward()
+        want = t.grad.numpy()
+        np.testing.assert_allclose(o.dact_f64_values(act, x), want, rtol=1e-12, atol=1e-13)
+        got32 = o.dact_f32_values(act, x.astype(np.float32)).astype(np.float64)
+        want32 = o.dact_f64_values(act, x.astype(np.float32).astype(np.float64))
+        assert np.all(np.abs(got32 - want32) <= 1e-6 + 16 * U32 * np.abs(want32)), act
+        h = 1e-5
+        fd = (o.act_f64(act, x + h) - o.act_f64(act, x - h)) / (2 * h)
+        assert np.all(np.abs(o.dact_f64_values(act, x) - fd) <= 1e-8 * (1 + np.abs(x))), act
+
+
+def check_dact_integer_exact(o) -> None:
+    """Small-integer dY and W: the sum over n is an exact integer, so with the ReLU
+    derivative (0 or 1, from the sign of integer Z, including Z = 0) or the identity's,
+    D is that integer masked and rounded once -- bit for bit."""
+    rng = np.random.default_rng(22)
+    for M, N, K in [(1, 1, 1), (5, 64, 7), (17, 33, 9), (12, 40, 31)]:
+        dY, dy = int_bf16(rng, (M, N))
+        W, w = int_bf16(rng, (N, K))
+        Z, zv = int_bf16(rng, (M, K), -3, 3)
+        g = dy @ w
+        np.testing.assert_array_equal(o.dact(dY, W, Z, "none"), lib_round_bf16(g.astype(np.float32)))
+        # the mask multiplies: a negative sum times 0 is -0, as in IEEE arithmetic
+        mask = (zv > 0).astype(np.float32)
+        np.testing.assert_array_equal(o.dact(dY, W, Z, "relu"), lib_round_bf16(g.astype(np.float32) * mask))
+
+
+def check_dact_index_and_transpose(o) -> None:
+    """D[m,k] = m + 16 k exactly: dY[m,0] = m, dY[m,1] = 1, W[0,k] = 1, W[1,k] = 16 k;
+    a W read as [K,N], or a swapped row/column index, cannot give it."""
+    M, N, K = 9, 6, 7
+    dy = np.zeros((M, N), np.float32)
+    dy[:, 0] = np.arange(M)
+    dy[:, 1] = 1.0
+    w = np.zeros((N, K), np.float32)
+    w[0, :] = 1.0
+    w[1, :] = 16.0 * np.arange(K)
+    Z = lib_round_bf16(np.ones((M, K), np.float32))
+    want = np.arange(M)[:, None] + 16 * np.arange(K)[None, :]
+    for act in ("relu", "none"):
+        np.testing.assert_array_equal(o.dact(lib_round_bf16(dy), lib_round_bf16(w), Z, act),
+                                      lib_round_bf16(want.astype(np.float32)))
+
+
+def check_dact_identity_and_order(o) -> None:
+    """W = I: D = bf16(dY * act'(Z)) within one rounding of the float64 product; and the
+    sum over n is a binary32 sum in ascending n (2^24 + 1 is absorbed)."""
+    rng = np.random.default_rng(23)
+    M, K = 13, 24
+    dY = rand_bf16(rng, (M, K))
+    Z = rand_bf16(rng, (M, K), 2.0)
+    W = lib_round_bf16(np.eye(K, dtype=np.float32))
+    z = torch.from_numpy(f32_of(Z).astype(np.float64)).requires_grad_(True)
+    torch.nn.functional.gelu(z, approximate="tanh").sum().backward()
+    ref = f32_of(dY).astype(np.float64) * z.grad.numpy()
+    got = f32_of(o.dact(dY, W, Z, "gelu_tanh")).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+    np.testing.assert_allclose(o.dact_f64(dY, W, Z, "gelu_tanh"), ref, rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(o.dact(dY, W, Z, "relu"),
+                                  lib_round_bf16(f32_of(dY) * (f32_of(Z) > 0).astype(np.float32)))
+    dy = lib_round_bf16(np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)]], np.float32))
+    ones = lib_round_bf16(np.ones((3, 1), np.float32))
+    one = lib_round_bf16(np.ones((1, 1), np.float32))
+    assert int(o.dact(dy, ones, one, "none")[0, 0]) == 0
+    assert o.dact_f64(dy, ones, one, "none")[0, 0] == 1.0
+
+
+# ---- single entries (sampled checks of large outputs) -----------------------------------------
+
+def check_entries(o) -> None:
+    """The per-entry evaluators against exact integer arithmetic at independent
+    (i, j) pairs (linear with bias/ReLU/R, dact with ReLU), the FFN at integer silu
+    points, and every float64 twin against numpy/torch float64."""
+    rng = np.random.default_rng(24)
+    M, N, K, P = 11, 13, 40, 300
+    A, a = int_bf16(rng, (M, K))
+    B, b = int_bf16(rng, (N, K))
+    bias, bv = int_bf16(rng, (N,), -3, 3)
+    R, rv = int_bf16(rng, (M, N), -3, 3)
+    i = rng.integers(0, M, P)
+    j = rng.integers(0, N, P)
+    exact = (a @ b.T + bv[None, :])[i, j]
+    np.testing.assert_array_equal(o.linear_entries(A[i], B[j], bias[j], R[i, j], "relu"),
+                                  lib_round_bf16((np.maximum(exact, 0) + rv[i, j]).astype(np.float32)))
+    np.testing.assert_array_equal(o.linear_entries(A[i], B[j]), lib_round_bf16((a @ b.T)[i, j].astype(np.float32)))
+    # dact: row i of dY with column j of W
+    Wt, w = int_bf16(rng, (K, N))           # W [K_contract=K, N_out=N]
+    Z, zv = int_bf16(rng, (M, N), -3, 3)
+    g = (a @ w)[i, j]
+    np.testing.assert_array_equal(o.dact_entries(A[i], np.ascontiguousarray(Wt.T)[j], Z[i, j], "relu"),
+                                  lib_round_bf16(g.astype(np.float32) * (zv[i, j] > 0).astype(np.float32)))
+    # FFN: X.W3 = 1, X.W1 = integer n - 8
+    x = np.zeros((M, K), np.float32)
+    x[:, 0] = 1.0
+    w1 = np.zeros((N, K), np.float32)
+    w1[:, 0] = np.arange(N) - 8.0
+    w3 = np.zeros((N, K), np.float32)
+    w3[:, 0] = 1.0
+    X, W1, W3 = lib_round_bf16(x), lib_round_bf16(w1), lib_round_bf16(w3)
+    silu = torch.nn.functional.silu(torch.from_numpy((np.arange(N) - 8.0)[j])).numpy()
+    got = f32_of(o.ffn_entries(X[i], W1[j], W3[j])).astype(np.float64)
+    assert np.all(np.abs(got - silu) <= 2.0 ** -8 * np.abs(silu) + 1e-30)
+    # float64 twins on random operands
+    Ar, Br, Cr = rand_bf16(rng, (P, K)), rand_bf16(rng, (P, K), 0.2), rand_bf16(rng, (P, K), 0.2)
+    af, bf, cf = (f32_of(v).astype(np.float64) for v in (Ar, Br, Cr))
+    dot_ab, dot_ac = (af * bf).sum(1), (af * cf).sum(1)
+    bz = rand_bf16(rng, (P,))
+    t = torch.from_numpy(dot_ab + f32_of(bz).astype(np.float64))
+    np.testing.assert_allclose(o.linear_entries(Ar, Br, bz, None, "gelu_tanh", f64=True),
+                               torch.nn.functional.gelu(t, approximate="tanh").numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(o.ffn_entries(Ar, Br, Cr, f64=True),
+                               torch.nn.functional.silu(torch.from_numpy(dot_ab)).numpy() * dot_ac,
+                               rtol=1e-12, atol=1e-13)
+    zt = torch.from_numpy(f32_of(bz).astype(np.float64)).requires_grad_(True)
+    torch.nn.functional.silu(zt).sum().backward()
+    np.testing.assert_allclose(o.dact_entries(Ar, Br, bz, "silu", f64=True), dot_ab * zt.grad.numpy(),
+                               rtol=1e-12, atol=1e-13)
+
+
 ALL_CHECKS = [check_f32_to_bf16, check_f64_to_bf16, check_acc_error_bound, check_fp32_sequential_sum,
               check_integer_exact,
               check_transpose_and_index, check_identity_b, check_zero_bias_and_linearity,
               check_bias_broadcast_and_residual, check_k_zero, check_activation_closed_forms,
               check_activation_vs_library, check_epilogue_order, check_ffn, check_leading_dims,
-              check_preact_output]
+              check_preact_output, check_dact_closed_forms, check_dact_vs_autograd, check_dact_integer_exact,
+              check_dact_index_and_transpose, check_dact_identity_and_order, check_entries]

@@ -47,6 +47,41 @@ MUTANTS = [
     ("sum_descending", "for (int64_t k = 0; k < K; ++k) {\n        float p", "for (int64_t k = K - 1; k >= 0; --k) {\n        float p", 0),
     ("lda_ignored", "float v = dot_f32(A + m * lda, B + n * ldb, K);", "float v = dot_f32(A + m * K, B + n * ldb, K);", 0),
     ("ldr_ignored", "if (R) v = v + bf16_to_f32(R[m * ldr + n]);", "if (R) v = v + bf16_to_f32(R[m * N + n]);", 0),
+    # activation gradient
+    ("dact_w_row_not_column", "float g = dot_f32_strided(dY + m * lddy, W + k, ldw, N);",
+     "float g = dot_f32_strided(dY + m * lddy, W + (k % N) * ldw, 1, N < K ? N : K);", 0),
+    ("dact_dy_row", "float g = dot_f32_strided(dY + m * lddy, W + k, ldw, N);",
+     "float g = dot_f32_strided(dY + (m / 2) * lddy, W + k, ldw, N);", 0),
+    ("dact_z_index", "float v = g * dact_f32(act, bf16_to_f32(Z[m * ldz + k]));",
+     "float v = g * dact_f32(act, bf16_to_f32(Z[m * ldz]));", 0),
+    ("dact_no_derivative", "float v = g * dact_f32(act, bf16_to_f32(Z[m * ldz + k]));",
+     "float v = g * act_f32(act, bf16_to_f32(Z[m * ldz + k]));", 0),
+    ("dact_strided_drop_last", "for (int64_t k = 0; k < K; ++k) {\n        float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k * stride]);",
+     "for (int64_t k = 0; k + 1 < K; ++k) {\n        float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k * stride]);", 0),
+    ("dact_sum_in_double", "    float acc = 0.0f;\n    for (int64_t k = 0; k < K; ++k) {\n        float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k * stride]);",
+     "    double acc = 0.0;\n    for (int64_t k = 0; k < K; ++k) {\n        float p = bf16_to_f32(a[k]) * bf16_to_f32(b[k * stride]);", 0),
+    ("dgelu_half", "return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t)", "return (1.0f + t) + 0.5f * x * (1.0f - t * t)", 0),
+    ("dgelu_sech2_sign", "0.5f * x * (1.0f - t * t)", "0.5f * x * (1.0f + t * t)", 0),
+    ("dgelu_cubic_factor", "c * (1.0f + 3.0f * a * x * x)", "c * (1.0f + a * x * x)", 0),
+    ("dgelu_f64_cubic_factor", "c * (1.0 + 3.0 * a * x * x)", "c * (1.0 + a * x * x)", 0),
+    ("dsilu_form", "return sg * (1.0f + x * (1.0f - sg));", "return sg * (1.0f + x * sg);", 0),
+    ("dsilu_f64_form", "return sg * (1.0 + x * (1.0 - sg));", "return sg * (1.0 + x * sg);", 0),
+    ("drelu_at_zero", "case ORACLE_ACT_RELU: return x > 0.0f ? 1.0f : 0.0f;", "case ORACLE_ACT_RELU: return x >= 0.0f ? 1.0f : 0.0f;", 0),
+    ("dnone_zero", "case ORACLE_ACT_NONE: return 1.0f;", "case ORACLE_ACT_NONE: return 0.0f;", 0),
+    ("dact_f64_no_derivative", "Y[m * ldy + k] = g * dact_f64(act, (double)bf16_to_f32(Z[m * ldz + k]));",
+     "Y[m * ldy + k] = g;", 0),
+    # per-entry evaluators
+    ("entries_bias_dropped", "if (bias) v = v + bf16_to_f32(bias[p]);", "if (0) v = v + bf16_to_f32(bias[p]);", 0),
+    ("entries_residual_before_act", "        v = act_f32(act, v);\n        if (R) v = v + bf16_to_f32(R[p]);",
+     "        if (R) v = v + bf16_to_f32(R[p]);\n        v = act_f32(act, v);", 0),
+    ("entries_b_row", "float v = dot_f32(A + p * K, B + p * K, K);", "float v = dot_f32(A + p * K, B + (p / 2) * K, K);", 0),
+    ("entries_f64_act_dropped", "        v = act_f64(act, v);\n        if (R) v = v + (double)bf16_to_f32(R[p]);",
+     "        if (R) v = v + (double)bf16_to_f32(R[p]);", 0),
+    ("ffn_entries_swap", "out[p] = f32_to_bf16(act_f32(ORACLE_ACT_SILU, a1) * a3);",
+     "out[p] = f32_to_bf16(act_f32(ORACLE_ACT_SILU, a3) * a1);", 0),
+    ("ffn_entries_f64_swap", "out[p] = act_f64(ORACLE_ACT_SILU, a1) * a3;", "out[p] = act_f64(ORACLE_ACT_SILU, a3) * a1;", 0),
+    ("dact_entries_z_ignored", "out[p] = f32_to_bf16(g * dact_f32(act, bf16_to_f32(Z[p])));", "out[p] = f32_to_bf16(g);", 0),
+    ("dact_entries_f64_z_ignored", "out[p] = g * dact_f64(act, (double)bf16_to_f32(Z[p]));", "out[p] = g;", 0),
 ]
 
 
