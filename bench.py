@@ -5,6 +5,15 @@ the MLP-forward linear layer D = GELU_tanh(X W^T + bias) with X[8192,4096],
 W[14336,4096], bias[14336] (X ~ N(0,1), W and bias ~ N(0,0.02), bf16, fp32
 accumulation).  `--workload llama_ffn` times the Llama-FFN fusion instead.
 
+After the timed steps, the same run times every configuration once more (the
+plain matmul as a latency, the MLP linear, the Llama FFN, the 64-bit-indexing
+case, the stored pre-activation, the backward activation-gradient product and
+the skinny, short-K and unaligned ragged rows) and reports each under
+`per_shape`, with its median and minimum launch time, its roofline fraction,
+plan and sampled SM clock, and -- from the CPU-oracle leg -- its error on
+sampled entries.  `nominal_peak` is the tensor cores' dense bf16 rate per SM and
+clock measured by a tcgen05 probe, times SMs and clock.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints ONE JSON line on rank 0.  `value` is the device-timed throughput of the
@@ -49,7 +58,17 @@ WORKLOADS = {
                        preact=True, name="mlp_preact_8192x14336x4096"),
     "int64": dict(M=65536, N=4096, K=65536, kind="linear", act="none", bias=False, residual=False,
                   name="int64_65536x4096x65536"),
+    # the MLP layer's backward activation-gradient product D[M,K] = (dY[M,N] . W[N,K]) * gelu'(Z[M,K])
+    "mlp_dact": dict(M=8192, N=14336, K=4096, kind="dact", act="gelu_tanh", bias=False, residual=False,
+                     name="mlp_dact_8192x14336x4096"),
 }
+
+# Every configuration, timed after the main workload: plain matmul (latency), MLP linear,
+# Llama FFN, 64-bit indexing, the MLP with its stored pre-activation, the backward
+# activation-gradient product, and ragged rows (skinny and long K, short K, unaligned N).
+PER_SHAPE = ["plain", "mlp_gelu", "llama_ffn", "int64", "mlp_preact", "mlp_dact",
+             "ragged:127,96,65536", "ragged:8191,96,65536", "ragged:8191,12288,64",
+             "ragged:1000,4099,4096", "ragged:3001,4099,4096", "ragged:8191,4099,4096"]
 
 
 def workload(spec: str) -> dict:
@@ -240,11 +259,18 @@ def recorded_traffic(workload: str, plan: str | None = None):
 
 # ------------------------------------------------------------------ workloads
 
+def out_shape(wl: dict) -> tuple[int, int]:
+    """D is [M, N]; for the activation gradient the contraction runs over N and D is [M, K]."""
+    return (wl["M"], wl["K"]) if wl["kind"] == "dact" else (wl["M"], wl["N"])
+
+
 def make_inputs(wl: dict, device):
     from dense_bf16_gemm_persistent_gb300 import inputs
     M, N, K = wl["M"], wl["N"], wl["K"]
     if wl["kind"] == "ffn":
         return inputs.llama_ffn(device=device, M=M, N=N, K=K)
+    if wl["kind"] == "dact":
+        return inputs.mlp_dact(device=device, M=M, N=N, K=K)
     if wl["name"].startswith("ragged"):
         t = inputs.ragged(M, N, K, device=device)
     elif wl["name"].startswith("int64"):
@@ -262,6 +288,8 @@ def algorithmic_bytes(wl: dict) -> float:
     """One read of every input and one write of D (and of Z, the pre-activation, when
     the workload stores it), all bf16."""
     M, N, K = wl["M"], wl["N"], wl["K"]
+    if wl["kind"] == "dact":  # dY, W and Z read once, D written once
+        return 2.0 * (M * N + N * K + 2 * M * K)
     b = M * K + N * K * (2 if wl["kind"] == "ffn" else 1) + M * N * (2 if wl.get("preact") else 1)
     if wl.get("bias"):
         b += N
@@ -279,6 +307,8 @@ def step_fn(wl: dict, t: dict, out, workspace=None, stream=None):
     import dense_bf16_gemm_persistent_gb300 as gb
     if wl["kind"] == "ffn":
         return lambda: gb.ffn_gated(t["X"], t["W1"], t["W3"], out=out, stream=stream)
+    if wl["kind"] == "dact":
+        return lambda: gb.linear_dact(t["dY"], t["W"], t["Z"], act=t["act"], out=out, stream=stream)
     if wl.get("preact"):
         import torch
         z = torch.empty_like(out)
@@ -307,6 +337,10 @@ def oracle_sample_run(wl: dict, h: dict, rows: int):
         t0 = time.perf_counter()
         oracle.ffn_gated(h["X"][:rows], h["W1"], h["W3"])
         return time.perf_counter() - t0, 4.0 * rows * N * K, oracle.num_threads()
+    if wl["kind"] == "dact":
+        t0 = time.perf_counter()
+        oracle.dact(h["dY"][:rows], h["W"], h["Z"][:rows], h["act"])
+        return time.perf_counter() - t0, 2.0 * rows * N * K, oracle.num_threads()
     R = h.get("R")
     t0 = time.perf_counter()
     run = oracle.linear_preact if wl.get("preact") else oracle.linear
@@ -325,8 +359,9 @@ def calibrate_rows(wl: dict, target_s: float) -> tuple[int, dict]:
 def cpu_baseline(wl: dict, target_s: float = 12.0) -> dict:
     rows, h = calibrate_rows(wl, target_s)
     dt, fl, threads = oracle_sample_run(wl, h, rows)
+    cols = out_shape(wl)[1]
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{rows} full output rows ({rows}x{wl['N']} entries, K={wl['K']}) of {wl['name']}, "
+            "sample": f"{rows} full output rows ({rows}x{cols} entries) of {wl['name']}, "
                       f"{dt:.1f} s on {threads} host threads"}
 
 
@@ -364,6 +399,8 @@ def config_of(wl: dict) -> dict:
     ws = algorithmic_bytes(wl)
     if wl["kind"] == "ffn":
         epi = "silu(acc1) * acc3"
+    elif wl["kind"] == "dact":
+        epi = f"(dY.W) * {wl['act']}'(Z)"
     elif wl.get("residual"):
         epi = "acc + R"
     elif wl.get("bias"):
@@ -380,6 +417,170 @@ def config_of(wl: dict) -> dict:
 
 # ------------------------------------------------------------------ our arm
 
+def launch_stats(launch_ms: list[float]) -> dict:
+    ms = sorted(launch_ms)
+    return {"mean": sum(ms) / len(ms), "median": ms[len(ms) // 2], "min": ms[0], "max": ms[-1], "n": len(ms)}
+
+
+def roofline_of(wl: dict, launch_ms: float, peaks: dict, peak_src: str, traffic=None) -> dict:
+    """Achieved vs the measured peak of the kernel's bound (tensor or HBM), from the
+    arithmetic intensity of the workload against the ridge of the measured peaks."""
+    fl = flops_per_step(wl)
+    alg_bytes = algorithmic_bytes(wl)
+    achieved = fl / (launch_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    if fl / alg_bytes >= peak * 1e12 / (hbm * 1e9):
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
+                "frac_of_sustained": achieved / peak_sustained}
+    gbs = alg_bytes / (launch_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": traffic,
+            "peak_source": f"{peak_src} hbm_gbs (copy)", "tflops": achieved}
+
+
+def _bits(t):
+    from dense_bf16_gemm_persistent_gb300 import inputs
+    return inputs.to_bits(t)
+
+
+def sampled_accuracy(wl: dict, t: dict, out, n: int, seed: int) -> dict:
+    """The CPU oracle at n independent output entries of this run's D (outside every timed
+    region): max |err|, the library's tolerance |err| <= 2^-7 (|ref| + 1), and the bf16-ULP
+    histogram of D against the float64 result rounded once to bf16."""
+    import numpy as np
+    import torch
+    import oracle
+    from dense_bf16_gemm_persistent_gb300 import inputs
+    Mo, No = out_shape(wl)
+    i, j = inputs.sample_pairs(Mo, No, n=n, seed=seed)
+    dev = out.device
+    ti, tj = torch.from_numpy(i).to(dev), torch.from_numpy(j).to(dev)
+    got = _bits(out[ti, tj])
+    ref = np.empty(n, np.uint16)
+    ref64 = np.empty(n, np.float64)
+    chunk = 4096
+    for s0 in range(0, n, chunk):
+        ci, cj = ti[s0:s0 + chunk], tj[s0:s0 + chunk]
+        sl = slice(s0, s0 + ci.numel())
+        if wl["kind"] == "ffn":
+            args = (_bits(t["X"][ci]), _bits(t["W1"][cj]), _bits(t["W3"][cj]))
+            ref[sl] = oracle.ffn_entries(*args)
+            ref64[sl] = oracle.ffn_entries(*args, f64=True)
+        elif wl["kind"] == "dact":
+            args = (_bits(t["dY"][ci]), _bits(t["W"][:, cj].t().contiguous()), _bits(t["Z"][ci, cj]))
+            ref[sl] = oracle.dact_entries(*args, act=t["act"])
+            ref64[sl] = oracle.dact_entries(*args, act=t["act"], f64=True)
+        else:
+            bias = _bits(t["bias"][cj]) if t.get("bias") is not None else None
+            R = _bits(t["R"][ci, cj]) if t.get("R") is not None else None
+            A, B = _bits(t["A"][ci]), _bits(t["B"][cj])
+            ref[sl] = oracle.linear_entries(A, B, bias, R, t["act"])
+            ref64[sl] = oracle.linear_entries(A, B, bias, R, t["act"], f64=True)
+    g = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = (ref.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    err = np.abs(g - r)
+
+    def key(x):  # bf16 patterns in numeric order
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7fff), x & 0x7fff)
+    d = np.abs(key(got) - key(oracle.f64_to_bf16(ref64)))
+    hist = {str(k): int((d == k).sum()) for k in range(3)}
+    hist[">=3"] = int((d >= 3).sum())
+    return {"entries": int(n), "max_abs_err": float(np.nanmax(err)) if n else 0.0,
+            "tolerance_ok": bool(np.all(err <= 2.0 ** -7 * (np.abs(r) + 1.0))),
+            "within_1ulp_of_f64": float((d <= 1).mean()), "ulp_hist_vs_f64": hist,
+            "sample": f"{n} independent (i, j) entries, numpy default_rng({seed})"}
+
+
+def time_steps(step, steps: int, warmup: int, prewarm_s: float, flush, stream, local: int, dist=None, device=None):
+    """Pre-warm, W untimed steps, then K steps with an event pair around each launch on
+    the launching stream (an L2 flush between the pairs when the working set fits in L2),
+    with the SM clock sampled during the timed region."""
+    import torch
+    import dense_bf16_gemm_persistent_gb300 as gb
+    sampler = ClockSampler(local)
+    t_end = time.time() + prewarm_s
+    step()
+    torch.cuda.synchronize()
+    while time.time() < t_end:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+    for _ in range(warmup):
+        step()
+    gb.device_status()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    sampler.mark()
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    barrier(dist, device)
+    gb.device_status()
+    return [ev0[i].elapsed_time(ev1[i]) for i in range(steps)], sampler.stop()
+
+
+def measure_shape(spec: str, args, device, local: int, peaks: dict, peak_src: str) -> dict:
+    """One per_shape entry: the workload's own inputs, timed like the main step."""
+    import torch
+    import dense_bf16_gemm_persistent_gb300 as gb
+    wl = workload(spec)
+    t = make_inputs(wl, device)
+    out = torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device)
+    ws = None
+    if wl.get("split_k"):
+        ws = torch.empty(max(1, gb.splitk_workspace_bytes(wl["M"], wl["N"], wl["K"], 0)), dtype=torch.uint8,
+                         device=device)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device) if needs_l2_flush(wl) else None
+    steps = args.shape_steps if flops_per_step(wl) < 1e13 else max(3, args.shape_steps // 4)
+    launch_ms, clocks = time_steps(step_fn(wl, t, out, ws), steps, max(3, args.warmup), args.shape_prewarm_s, flush,
+                                   torch.cuda.current_stream(device), local)
+    st = launch_stats(launch_ms)
+    plan = gb.last_plan()
+    entry = {"workload": wl["name"], "M": wl["M"], "N": wl["N"], "K": wl["K"],
+             "epilogue": config_of(wl)["epilogue"], "ms_median": st["median"], "ms_min": st["min"],
+             "ms_mean": st["mean"], "launches": st["n"],
+             "tflops": flops_per_step(wl) / (st["median"] / 1e3) / 1e12,
+             "roofline": roofline_of(wl, st["median"], peaks, peak_src),
+             "plan": plan, "clocks": clocks, "l2": config_of(wl)["l2"]}
+    if wl.get("split_k"):
+        entry["entry_point"] = "gb_gemm_linear_splitk (automatic split count, caller workspace)"
+    if spec == "plain":
+        entry["latency_us"] = {"median": st["median"] * 1e3, "min": st["min"] * 1e3}
+    if not args.skip_cpu:
+        n = 16384 if wl["K"] <= 16384 else 4096
+        entry["accuracy"] = sampled_accuracy(wl, t, out, n, seed=7)
+    del t, out, ws, flush
+    torch.cuda.empty_cache()
+    return entry
+
+
+def nominal_peak(sms: int, sm_max_mhz: float, sm_load_mhz: float | None) -> dict:
+    """SMs x clock x the dense bf16 rate per SM and clock of the kernels' MMA shape,
+    pinned by the tcgen05 probe (one CTA pair alone, and every SM pair at once)."""
+    import dense_bf16_gemm_persistent_gb300 as gb
+    r1, c1 = gb.measure_mma_rate(cta_group=2, n=256, num_mma=16384, units=1)
+    ra, ca = gb.measure_mma_rate(cta_group=2, n=256, num_mma=16384, units=sms // 2)
+    d = {"probe": "tcgen05.mma.cta_group::2.kind::f16, M=256 N=256 K=16 bf16 -> fp32, back to back from shared "
+                  "memory (no loads, no epilogue), clock64 cycles",
+         "flops_per_clk_per_sm": r1, "cycles_per_mma": c1,
+         "flops_per_clk_per_sm_all_sms": ra, "cycles_per_mma_all_sms": ca,
+         "sms": sms, "sm_max_mhz": sm_max_mhz, "tflops_at_max_clock": r1 * sms * sm_max_mhz * 1e6 / 1e12}
+    if sm_load_mhz:
+        d["sm_mhz_under_load"] = sm_load_mhz
+        d["tflops_at_clock_under_load"] = r1 * sms * sm_load_mhz * 1e6 / 1e12
+    return d
+
+
 def run_ours(args, wl: dict):
     import torch
     world, rank, local = dist_env()
@@ -393,7 +594,7 @@ def run_ours(args, wl: dict):
     gb.set_config(args.config)
 
     t = make_inputs(wl, device)
-    out = torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16, device=device)
+    out = torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device)
     ws = None
     if wl.get("split_k"):
         ws = torch.empty(max(1, gb.splitk_workspace_bytes(wl["M"], wl["N"], wl["K"], 0)), dtype=torch.uint8,
@@ -403,39 +604,9 @@ def run_ours(args, wl: dict):
     fl = flops_per_step(wl)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device) if needs_l2_flush(wl) else None
 
-    # pre-warm (clocks to steady state) + W warm-up steps, all untimed
-    sampler = ClockSampler(local)
-    t_end = time.time() + args.prewarm_s
-    step()
-    torch.cuda.synchronize()
-    while time.time() < t_end:
-        for _ in range(10):
-            step()
-        torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        step()
-    gb.device_status()
-
-    # timed region: K steps; an event pair around each launch on the launching stream
-    # (an L2 flush, when the working set fits in L2, runs between the pairs).
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(dist, device)
-    torch.cuda.synchronize()
-    sampler.mark()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        ev0[i].record(stream)
-        step()
-        ev1[i].record(stream)
-    torch.cuda.synchronize()
-    sampler.mark()
-    barrier(dist, device)
-    launch_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    # timed region: K steps, an event pair around each launch on the launching stream
+    launch_ms, clocks = time_steps(step, args.steps, args.warmup, args.prewarm_s, flush, stream, local, dist, device)
     local_ms = sum(launch_ms)
-    gb.device_status()
-    clocks = sampler.stop()
     value, slowest_s = aggregate_replicas(fl * args.steps / 1e12, local_ms / 1e3, dist, device)
     plan = gb.last_plan()
 
@@ -447,12 +618,17 @@ def run_ours(args, wl: dict):
     # result drains.  Every step's copies are inside the timed region.
     e2e = None
     if not args.skip_e2e:
-        names = ["X", "W1", "W3"] if wl["kind"] == "ffn" else [k for k in ("A", "B", "bias", "R") if t.get(k) is not None]
+        if wl["kind"] == "ffn":
+            names = ["X", "W1", "W3"]
+        elif wl["kind"] == "dact":
+            names = ["dY", "W", "Z"]
+        else:
+            names = [k for k in ("A", "B", "bias", "R") if t.get(k) is not None]
         host = {k: t[k].cpu().pin_memory() for k in names}
         s_in, s_comp, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
         dev_in = [{k: torch.empty_like(t[k]) for k in names} for _ in range(2)]
-        dev_out = [torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16, device=device) for _ in range(2)]
-        host_out = [torch.empty((wl["M"], wl["N"]), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        dev_out = [torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device) for _ in range(2)]
+        host_out = [torch.empty(out_shape(wl), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         steps_b = []
         for bi in range(2):
             tin = dict(dev_in[bi])
@@ -518,6 +694,7 @@ def run_ours(args, wl: dict):
                "copies_only_ms_per_step": copy_ms,
                "link_gbs_copies_only": (h2d + d2h) / (copy_ms / 1e3) / 1e9,
                "note": "copies_only: the same pipeline without the GEMM call, timed separately"}
+        del host, dev_in, dev_out, host_out, steps_b
 
     if rank != 0:
         if dist is not None:
@@ -525,31 +702,18 @@ def run_ours(args, wl: dict):
         return 0
 
     peaks, peak_src = load_peaks()
-    avg_launch_ms = sum(launch_ms) / len(launch_ms)
-    achieved = fl / (avg_launch_ms / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    alg_bytes = algorithmic_bytes(wl)
+    st = launch_stats(launch_ms)
     traffic = recorded_traffic(wl["name"], plan)
-    if fl / alg_bytes >= peak * 1e12 / (hbm * 1e9):
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                    "traffic": traffic,
-                    "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
-                    "frac_of_sustained": achieved / peak_sustained}
-    else:
-        gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
-        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                    "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (copy)",
-                    "tflops": achieved}
-    roofline.update({"kernel": "gb::gemm_persistent_kernel", "avg_launch_ms": avg_launch_ms,
-                     "flops_per_launch": fl, "algorithmic_bytes_per_launch": alg_bytes,
+    roofline = roofline_of(wl, st["mean"], peaks, peak_src, traffic)
+    roofline.update({"kernel": "gb::gemm_persistent_kernel", "avg_launch_ms": st["mean"],
+                     "flops_per_launch": fl, "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
                      "clock_note": "timed after a pre-warm, so under the power cap (see clocks)"})
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": slowest_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(wl),
+        "launch_ms": st,
         "roofline": roofline,
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -558,6 +722,21 @@ def run_ours(args, wl: dict):
     }
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_s)
+        line["accuracy"] = sampled_accuracy(wl, t, out, 65536, seed=3)
+    del t, out, ws, flush
+    torch.cuda.empty_cache()
+    if world == 1 and args.per_shape != "none":
+        specs = PER_SHAPE if args.per_shape == "all" else [x for x in args.per_shape.split(";") if x]
+        line["per_shape"] = [measure_shape(sp, args, device, local, peaks, peak_src) for sp in specs]
+        gb.set_config(args.config)
+    if world == 1 and not args.skip_nominal:
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        sm_max = (clocks or {}).get("sm_max_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        line["nominal_peak"] = nominal_peak(sms, sm_max, (clocks or {}).get("sm_mhz"))
+        npk = line["nominal_peak"]
+        if "tflops_at_clock_under_load" in npk:
+            line["roofline"]["frac_of_nominal_at_clock"] = roofline["achieved"] / npk["tflops_at_clock_under_load"] \
+                if roofline["bound"] == "tensor" else None
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -578,6 +757,11 @@ def main(argv=None):
     ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of CPU-oracle work")
     ap.add_argument("--ref-step-s", type=float, default=4.0, help="reference arm: seconds per step")
     ap.add_argument("--config", default=None, help="tile-configuration override (gb_set_config syntax)")
+    ap.add_argument("--per-shape", default="all",
+                    help="'all' (every configuration, see PER_SHAPE), 'none', or workloads separated by ';'")
+    ap.add_argument("--shape-steps", type=int, default=20, help="timed launches per per_shape workload")
+    ap.add_argument("--shape-prewarm-s", type=float, default=0.3)
+    ap.add_argument("--skip-nominal", action="store_true", help="skip the tcgen05 rate probe")
     args = ap.parse_args(argv)
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps >= 1 and --warmup >= 0")

@@ -6,6 +6,7 @@ fallback of any kind, and every call raises if the library is missing.
 
     linear(A, B, bias=None, R=None, act="none")  ->  bf16(act(A @ B.T + bias) + R)
     ffn_gated(X, W1, W3)                         ->  bf16(silu(X @ W1.T) * (X @ W3.T))
+    linear_dact(dY, W, Z, act="none")            ->  bf16((dY @ W) * act'(Z))
 
 Tensors are torch CUDA bf16 tensors, 2-D with a contiguous last dimension
 (bias: contiguous 1-D).  Work is enqueued on ``torch.cuda.current_stream()``
@@ -20,7 +21,8 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libgbgemm.so")
+# GBGEMM_TRACE=1 loads the instrumented build (libgbgemm_trace.so, see gb_set_trace_buffer)
+LIB_PATH = os.path.join(_PKG, "libgbgemm_trace.so" if os.environ.get("GBGEMM_TRACE") == "1" else "libgbgemm.so")
 
 ACT = {"none": 0, "gelu_tanh": 1, "silu": 2, "relu": 3}
 STATUS = {0: "GB_OK", 1: "GB_ERR_INVALID_ARG", 2: "GB_ERR_UNSUPPORTED", 3: "GB_ERR_CUDA", 4: "GB_ERR_TIMEOUT"}
@@ -52,6 +54,7 @@ def lib() -> ctypes.CDLL:
         L.gb_gemm_ffn_gated.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p]
         L.gb_gemm_linear_preact.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, p, i64, i64, i64, i64,
                                             p]
+        L.gb_gemm_linear_dact.argtypes = [p, i64, p, i64, p, i64, ctypes.c_int, p, i64, i64, i64, i64, p]
         L.gb_gemm_linear_splitk.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64,
                                              ctypes.c_int, p, ctypes.c_size_t, p]
         L.gb_gemm_ffn_gated_splitk.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, ctypes.c_int, p,
@@ -68,13 +71,18 @@ def lib() -> ctypes.CDLL:
         L.gb_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         L.gb_set_fault_injection.argtypes = [ctypes.c_int]
         L.gb_last_plan.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+        L.gb_set_trace_buffer.argtypes = [p, ctypes.c_size_t]
+        L.gb_measure_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
         L.gb_version.argtypes = []
         L.gb_version.restype = ctypes.c_char_p
-        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_preact", "gb_gemm_linear_splitk",
+        for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_preact", "gb_gemm_linear_dact",
+                     "gb_gemm_linear_splitk",
                      "gb_gemm_ffn_gated_splitk",
                      "gb_splitk_workspace_bytes", "gb_gemm_linear_splitk_noalloc", "gb_static_scratch_bytes",
                      "gb_get_device_status", "gb_set_config",
-                     "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan"):
+                     "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan", "gb_set_trace_buffer",
+                     "gb_measure_mma_rate"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -177,6 +185,24 @@ def linear_preact(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = 
     return out, preact
 
 
+def linear_dact(dY: torch.Tensor, W: torch.Tensor, Z: torch.Tensor, act: str = "none",
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = bf16((dY @ W) * act'(Z)) on the GPU: dY [M,N], W [N,K] (the layer's weight as linear()
+    takes it), Z [M,K] (the stored pre-activation); D [M,K]."""
+    M, N = dY.shape
+    K = W.shape[1]
+    if act not in ACT:
+        raise ValueError(f"act must be one of {sorted(ACT)}")
+    py, ldy = _mat(dY, "dY", M, N)
+    pw, ldw = _mat(W, "W", N, K)
+    pz, ldz = _mat(Z, "Z", M, K)
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device)
+    pd, ldd = _mat(out, "out", M, K)
+    _check(lib().gb_gemm_linear_dact(py, ldy, pw, ldw, pz, ldz, ACT[act], pd, ldd, M, N, K, _stream(stream)))
+    return out
+
+
 def ffn_gated(X: torch.Tensor, W1: torch.Tensor, W3: torch.Tensor, out: torch.Tensor | None = None,
               stream=None, split_k=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """D = bf16(silu(X @ W1.T) * (X @ W3.T)) on the GPU (X [M,K], W1/W3 [N,K]); split_k as in linear()."""
@@ -213,6 +239,23 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_fault_injection(mode: int) -> None:
     _check(lib().gb_set_fault_injection(int(mode)))
+
+
+def measure_mma_rate(cta_group: int = 2, n: int = 256, alternate: bool = False, num_mma: int = 8192,
+                     units: int = 1) -> tuple[float, float]:
+    """(dense bf16 FLOP per SM per clock, cycles per MMA) of back-to-back tcgen05.mma (see the header)."""
+    rate, cyc = ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().gb_measure_mma_rate(int(cta_group), int(n), 1 if alternate else 0, int(num_mma), int(units),
+                                     ctypes.byref(rate), ctypes.byref(cyc)))
+    return rate.value, cyc.value
+
+
+def set_trace_buffer(buf: torch.Tensor | None) -> None:
+    """Trace records go to `buf` (a CUDA tensor) in a GB_TRACE build; None turns tracing off."""
+    if buf is None:
+        _check(lib().gb_set_trace_buffer(None, 0))
+    else:
+        _check(lib().gb_set_trace_buffer(buf.data_ptr(), buf.numel() * buf.element_size()))
 
 
 def last_plan() -> str:

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libgbgemm.so")
 LOG_DIR = os.path.join(PKG, "_build")
 SOURCES = ["gbgemm.cu"]
-HEADERS = ["gemm_kernel.cuh", "ptx.cuh"]
+HEADERS = ["gemm_kernel.cuh", "ptx.cuh", "probe.cuh"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v",
               "--diag-suppress", "177"]
@@ -23,10 +23,10 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "gbgemm.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
@@ -57,23 +57,30 @@ def _check_register_budgets(log: str) -> None:
                                f"the {need} its warpgroup register budgets need")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build libgbgemm.so next to this file; the -Xptxas -v report goes to _build/ptxas.log."""
-    if not force and not _stale():
-        return LIB
+TRACE_LIB = os.path.join(PKG, "libgbgemm_trace.so")
+
+
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Build libgbgemm.so next to this file; the -Xptxas -v report goes to _build/ptxas.log.
+    trace=True builds the instrumented libgbgemm_trace.so instead (-DGB_TRACE: the kernels
+    record where each role waited; see gb_set_trace_buffer)."""
+    out = TRACE_LIB if trace else LIB
+    if not force and not _stale(out):
+        return out
     os.makedirs(LOG_DIR, exist_ok=True)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-shared", "-o", tmp, *[os.path.join(CSRC, s) for s in SOURCES]]
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), *NVCC_FLAGS, *(["-DGB_TRACE"] if trace else []), "-shared", "-o", tmp,
+           *[os.path.join(CSRC, s) for s in SOURCES]]
     res = subprocess.run(cmd, capture_output=True, text=True)
-    with open(os.path.join(LOG_DIR, "ptxas.log"), "w") as f:
+    with open(os.path.join(LOG_DIR, "ptxas_trace.log" if trace else "ptxas.log"), "w") as f:
         f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stderr[-4000:]}")
     _check_register_budgets(res.stdout + res.stderr)
     if verbose:
         print(res.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

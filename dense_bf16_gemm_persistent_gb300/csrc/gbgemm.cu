@@ -16,6 +16,7 @@
 
 #include "../../include/gbgemm.h"
 #include "gemm_kernel.cuh"
+#include "probe.cuh"
 
 namespace {
 
@@ -56,12 +57,18 @@ struct Config {
     int boxes = 0;       // staging boxes per epilogue warp (D, and R by TMA): 0 = heuristic, 2..8
     int pingpong = -1;   // 1: the two epilogue warpgroups alternate tiles (implies epi=2; no effect with
                          // split-K); 0: they share every tile; -1 = auto (alternate on short-K work items)
+    // L2 eviction hints for the TMA traffic of A, B, R and D (and Z): -1 = default,
+    // 0 = none, 1 = evict first, 2 = evict last
+    int hint_a = -1, hint_b = -1, hint_r = -1, hint_d = -1;
 };
 
 std::mutex g_cfg_mu;
 Config g_cfg;
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
 int g_inject = 0;
+// Trace buffer (libraries built with GB_TRACE): device memory of the caller.
+unsigned long long* g_trace = nullptr;
+size_t g_trace_bytes = 0;
 
 Config current_config(uint64_t* timeout, int* inject) {
     std::lock_guard<std::mutex> lk(g_cfg_mu);
@@ -296,11 +303,14 @@ struct Problem {
     bool ffn;
     void* z = nullptr;  // optional second output (linear): the pre-activation
     int64_t ldz = 0;
+    // activation gradient: B is a row-major [k, n] matrix (MN-major operand) and the
+    // epilogue input r (the stored pre-activation) multiplies by act'(r)
+    bool dact = false;
 };
 
 gb_status_t validate(const Problem& pr) {
-    const char* an = pr.ffn ? "X" : "A";
-    const char* bn = pr.ffn ? "W1" : "B";
+    const char* an = pr.ffn ? "X" : pr.dact ? "dY" : "A";
+    const char* bn = pr.ffn ? "W1" : pr.dact ? "W" : "B";
     if (pr.m < 0 || pr.n < 0 || pr.k < 0)
         return fail(GB_ERR_INVALID_ARG, "negative size M=%" PRId64 " N=%" PRId64 " K=%" PRId64, pr.m, pr.n, pr.k);
     if (pr.act < GB_ACT_NONE || pr.act > GB_ACT_RELU) return fail(GB_ERR_INVALID_ARG, "unknown activation %d", pr.act);
@@ -309,14 +319,24 @@ gb_status_t validate(const Problem& pr) {
                     pr.n, pr.k);
     if (pr.m == 0 || pr.n == 0) return GB_OK;
     if (!pr.d) return fail(GB_ERR_INVALID_ARG, "D is null");
-    if (pr.ldd < pr.n) return fail(GB_ERR_INVALID_ARG, "ldd=%" PRId64 " < N=%" PRId64, pr.ldd, pr.n);
-    if (pr.r && pr.ldr < pr.n) return fail(GB_ERR_INVALID_ARG, "ldr=%" PRId64 " < N=%" PRId64, pr.ldr, pr.n);
+    // dims named as the caller sees them: for the activation gradient the output is
+    // [M, K] and the contraction runs over N
+    const char* nn = pr.dact ? "K" : "N";
+    const char* kn = pr.dact ? "N" : "K";
+    if (pr.dact && !pr.r) return fail(GB_ERR_INVALID_ARG, "Z is null");
+    if (pr.ldd < pr.n) return fail(GB_ERR_INVALID_ARG, "ldd=%" PRId64 " < %s=%" PRId64, pr.ldd, nn, pr.n);
+    if (pr.r && pr.ldr < pr.n)
+        return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < %s=%" PRId64, pr.dact ? "z" : "r", pr.ldr, nn, pr.n);
     if (pr.k > 0) {
         if (!pr.a) return fail(GB_ERR_INVALID_ARG, "%s is null", an);
         if (!pr.b0) return fail(GB_ERR_INVALID_ARG, "%s is null", bn);
         if (pr.ffn && !pr.b1) return fail(GB_ERR_INVALID_ARG, "W3 is null");
-        if (pr.lda < pr.k) return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < K=%" PRId64, pr.ffn ? "x" : "a", pr.lda, pr.k);
-        if (pr.ldb0 < pr.k)
+        if (pr.lda < pr.k)
+            return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < %s=%" PRId64, pr.ffn ? "x" : pr.dact ? "dy" : "a",
+                        pr.lda, kn, pr.k);
+        if (pr.dact && pr.ldb0 < pr.n)
+            return fail(GB_ERR_INVALID_ARG, "ldw=%" PRId64 " < K=%" PRId64, pr.ldb0, pr.n);
+        if (!pr.dact && pr.ldb0 < pr.k)
             return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < K=%" PRId64, pr.ffn ? "w1" : "b", pr.ldb0, pr.k);
         if (pr.ffn && pr.ldb1 < pr.k) return fail(GB_ERR_INVALID_ARG, "ldw3=%" PRId64 " < K=%" PRId64, pr.ldb1, pr.k);
         if (!aligned16(pr.a) || !aligned16(pr.b0) || (pr.ffn && !aligned16(pr.b1)))
@@ -426,9 +446,15 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.ldd = pr.ldd;
     prm.timeout_ns = timeout_ns;
     prm.inject = inject;
+    auto hint = [](int cfg_value, int dflt) { return static_cast<uint32_t>(cfg_value >= 0 ? cfg_value : dflt); };
+    prm.hint_a = hint(cfg.hint_a, 0);
+    prm.hint_b = hint(cfg.hint_b, 0);
+    prm.hint_r = hint(cfg.hint_r, 0);
+    prm.hint_d = hint(cfg.hint_d, 0);
     uint32_t flags = 0;
     if (!pr.ffn && pr.bias) flags |= gb::kFlagBias | (aligned16(pr.bias) ? gb::kFlagBiasVec : 0u);
     if (!pr.ffn && pr.r) flags |= gb::kFlagResidual | ((aligned16(pr.r) && pr.ldr % 8 == 0) ? gb::kFlagRVec : 0u);
+    if (pr.dact) flags |= gb::kFlagBMn | gb::kFlagDact;
     const bool d_tma = aligned16(pr.d) && pr.ldd % 8 == 0;
     if (d_tma) flags |= gb::kFlagDTma;
     const bool r_tma = !pr.ffn && pr.r && aligned16(pr.r) && pr.ldr % 8 == 0 && splits == 1;
@@ -451,9 +477,15 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         if ((st = make_tmap(&prm.tm_a, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             GB_OK)
             return st;
-        if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.k, pr.n, pr.ldb0 * 2, gb::kBK, b_rows,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
+        if (pr.dact) {
+            // B = W [k rows (contraction), n columns]: boxes of 64 columns x 64 rows
+            if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.n, pr.k, pr.ldb0 * 2, 64, gb::kBK,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
+                return st;
+        } else if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.k, pr.n, pr.ldb0 * 2, gb::kBK, b_rows,
+                                   CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK) {
             return st;
+        }
         if (pr.ffn && (st = make_tmap(&prm.tm_b1, pr.b1, pr.k, pr.n, pr.ldb1 * 2, gb::kBK, b_rows,
                                       CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
             return st;
@@ -491,7 +523,8 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
              "kernel=%s pair=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
              "k_blocks=%d splits=%d group=%d zigzag=%d "
              "d_store=%s r_load=%s z_store=%s",
-             pr.ffn ? "ffn_gated" : "linear", V::kPair ? 1 : 0, V::kEpi, prm.pingpong, V::kTileM, bn, gb::kBK,
+             pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : "linear", V::kPair ? 1 : 0, V::kEpi, prm.pingpong,
+             V::kTileM, bn, gb::kBK,
              prm.stages,
              prm.d_boxes, prm.r_boxes,
              static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
@@ -499,6 +532,11 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
              pr.r ? (r_tma ? "tma" : (flags & gb::kFlagRVec) ? "ld.v4" : "ld.transposed") : "none",
              pr.z ? (z_tma ? "tma" : "st.transposed") : "none");
     t_plan = plan;
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        const size_t need = static_cast<size_t>(units) * (V::kPair ? 2 : 1) * gb::kTraceWords * 8;
+        prm.trace = (g_trace && g_trace_bytes >= need) ? g_trace : nullptr;
+    }
     if (ws_needed) {  // counters and accumulators start at zero
         cudaError_t e = cudaMemsetAsync(prm.ws_cnt, 0, ws_needed, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(split-K workspace)");
@@ -618,9 +656,75 @@ gb_status_t splitk_bytes_for(const Problem& pr, int splits, size_t* bytes) {
     return run(pr, nullptr, sr);
 }
 
+// ---------------------------------------------------------------- tensor-core rate probe
+
+template <int CG, int N>
+gb_status_t probe_run(int units, int num_mma, int alternate, cudaStream_t stream) {
+    auto kern = gb::mma_rate_kernel<CG, N>;
+    const int smem = 200 * 1024;  // one CTA per SM: its 512 TMEM columns are free
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(probe)");
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(units * CG, 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, num_mma, alternate, static_cast<uint64_t>(1000000000ull));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(probe)");
+    return GB_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+gb_status_t gb_measure_mma_rate(int cta_group, int n, int alternate, int num_mma, int units,
+                                double* flops_per_clk_per_sm, double* cycles_per_mma) {
+    t_error.clear();
+    if (!flops_per_clk_per_sm || !cycles_per_mma) return fail(GB_ERR_INVALID_ARG, "output pointer is null");
+    if (cta_group != 1 && cta_group != 2) return fail(GB_ERR_INVALID_ARG, "cta_group must be 1 or 2");
+    if (n != 128 && n != 256) return fail(GB_ERR_INVALID_ARG, "n must be 128 or 256");
+    if (num_mma < 8 || num_mma > 65536) return fail(GB_ERR_INVALID_ARG, "num_mma must be in [8, 65536]");
+    int dev = 0;
+    DeviceInfo info;
+    gb_status_t st = device_info(&dev, &info);
+    if (st != GB_OK) return st;
+    const int max_units = std::min(gb::kProbeMaxUnits, info.sms / cta_group);
+    if (units < 1 || units > max_units)
+        return fail(GB_ERR_INVALID_ARG, "units must be in [1, %d] (one CTA per SM)", max_units);
+    static const unsigned long long zeros[gb::kProbeMaxUnits] = {};
+    cudaError_t e = cudaMemcpyToSymbol(gb::g_probe_cycles, zeros, sizeof zeros);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the probe results");
+    cudaStream_t stream = nullptr;
+    if (cta_group == 1)
+        st = n == 128 ? probe_run<1, 128>(units, num_mma, alternate, stream)
+                      : probe_run<1, 256>(units, num_mma, alternate, stream);
+    else
+        st = n == 128 ? probe_run<2, 128>(units, num_mma, alternate, stream)
+                      : probe_run<2, 256>(units, num_mma, alternate, stream);
+    if (st != GB_OK) return st;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize(probe)");
+    unsigned long long cyc[gb::kProbeMaxUnits];
+    if ((e = cudaMemcpyFromSymbol(cyc, gb::g_probe_cycles, sizeof cyc)) != cudaSuccess)
+        return cuda_fail(e, "reading the probe results");
+    std::sort(cyc, cyc + units);
+    if (cyc[0] == 0) return fail(GB_ERR_TIMEOUT, "a probe unit's wait for its MMAs ran out");
+    const double per_mma = static_cast<double>(cyc[units / 2]) / num_mma;
+    const double flops = 2.0 * 128.0 * cta_group * n * 16.0;
+    *cycles_per_mma = per_mma;
+    *flops_per_clk_per_sm = flops / per_mma / cta_group;
+    return GB_OK;
+}
+
 
 gb_status_t gb_gemm_linear(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, const void* R,
                            int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
@@ -635,6 +739,16 @@ gb_status_t gb_gemm_linear_preact(const void* A, int64_t lda, const void* B, int
     t_error.clear();
     if (!Z && M > 0 && N > 0) return fail(GB_ERR_INVALID_ARG, "Z is null");
     Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false, Z, ldz};
+    return run(pr, stream);
+}
+
+gb_status_t gb_gemm_linear_dact(const void* dY, int64_t lddy, const void* W, int64_t ldw, const void* Z,
+                                int64_t ldz, int act, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                                void* stream) {
+    t_error.clear();
+    // output [M, K], contraction over N: in the plan's terms n = K and k = N
+    Problem pr{dY, lddy, W, ldw, nullptr, 0, nullptr, Z, ldz, act, D, ldd, M, K, N, false};
+    pr.dact = true;
     return run(pr, stream);
 }
 
@@ -775,6 +889,10 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "epi" && v >= 0 && v <= 2) c.epi = static_cast<int>(v);
             else if (key == "boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.boxes = static_cast<int>(v);
             else if (key == "pingpong" && v >= -1 && v <= 1) c.pingpong = static_cast<int>(v);
+            else if (key == "hint_a" && v >= -1 && v <= 2) c.hint_a = static_cast<int>(v);
+            else if (key == "hint_b" && v >= -1 && v <= 2) c.hint_b = static_cast<int>(v);
+            else if (key == "hint_r" && v >= -1 && v <= 2) c.hint_r = static_cast<int>(v);
+            else if (key == "hint_d" && v >= -1 && v <= 2) c.hint_d = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;
@@ -804,6 +922,19 @@ gb_status_t gb_set_fault_injection(int mode) {
     std::lock_guard<std::mutex> lk(g_cfg_mu);
     g_inject = mode;
     return GB_OK;
+}
+
+gb_status_t gb_set_trace_buffer(void* buf, size_t bytes) {
+#ifdef GB_TRACE
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    g_trace = static_cast<unsigned long long*>(buf);
+    g_trace_bytes = buf ? bytes : 0;
+    return GB_OK;
+#else
+    (void)buf;
+    (void)bytes;
+    return fail(GB_ERR_UNSUPPORTED, "this library was built without GB_TRACE");
+#endif
 }
 
 const char* gb_version(void) { return "0.1.0"; }

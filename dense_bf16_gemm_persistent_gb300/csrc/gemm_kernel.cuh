@@ -89,7 +89,10 @@ enum : uint32_t {
     kFlagRTma = 32u,     // R loaded by TMA into shared memory, prefetched ahead of use
     kFlagZ = 64u,        // also store the pre-activation Z = bf16(acc + bias)
     kFlagZTma = 128u,    // Z stored by TMA (16-byte aligned rows)
+    kFlagBMn = 256u,     // B is MN-major: a row-major [K, N] matrix (contraction over its rows)
+    kFlagDact = 512u,    // the epilogue input multiplies: v *= act'(R) (activation gradient), no act
 };
+constexpr uint32_t kMnBoxBytes = 64 * kBK * 2;  // one MN-major B box: 64 columns x 64 contraction rows
 
 // Codes written to the device status word (low byte = gb_status_t).
 enum : uint32_t { kStatusTimeout = 4u };
@@ -136,6 +139,59 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     // of local parity g -- always TMEM buffer g -- and all of its chunks, instead of
     // both warpgroups sharing every tile's chunks.
     int32_t pingpong;
+    // L2 eviction hints (l2_policy codes: 0 none, 1 evict first, 2 evict last) for the
+    // TMA loads of A, of B (W1/W3), of R, and the TMA stores of D and Z.
+    uint32_t hint_a, hint_b, hint_r, hint_d;
+    // Timing trace (libraries built with GB_TRACE only): kTraceWords words per CTA.
+    unsigned long long* trace;
+};
+
+// Trace record of one CTA (GB_TRACE builds): where each role waited, in SM clock
+// cycles, and when the CTA started and finished, in %globaltimer nanoseconds.
+constexpr int kTraceWords = 32;
+enum : int {
+    kTrStartNs = 0,        // kernel entry
+    kTrSetupNs = 1,        // barriers initialised, TMEM allocated
+    kTrMmaFullCyc = 2,     // MMA issuer: cycles blocked on operand stages (full)
+    kTrMmaFullN = 3,
+    kTrMmaAccCyc = 4,      // MMA issuer: cycles blocked on a free accumulator (acc_empty)
+    kTrMmaAccN = 5,
+    kTrProdEmptyCyc = 6,   // producer: cycles blocked on a free stage (empty)
+    kTrProdEmptyN = 7,
+    kTrEpiFullCyc = 8,     // epilogue warp 0: cycles blocked on a finished accumulator
+    kTrEpiFullN = 9,
+    kTrEpiBodyCyc = 10,    // epilogue warp 0: cycles spent on its tiles after the wait
+    kTrMmaFirstNs = 11,    // MMA issuer: first MMA issued
+    kTrMmaLastNs = 12,     // MMA issuer: last accumulator committed
+    kTrEndNs = 13,         // epilogue warp 0 done
+    kTrMmaItems = 14,      // work items this CTA's MMA issuer ran
+    kTrMmaCyc = 15,        // MMA issuer: cycles from its first wait to its last commit
+    // epilogue warp 0, cycles per phase of its chunk loop (express and paired paths)
+    kTrEpDBox = 16,        // waiting for free D staging boxes
+    kTrEpTmemLd = 17,      // tcgen05.ld + wait::ld
+    kTrEpRWait = 18,       // waiting for the chunk's R box
+    kTrEpMath = 19,        // bias, activation, epilogue input, bf16 packing, staging stores
+    kTrEpStore = 20,       // proxy fence, warp sync, TMA store issue
+    kTrEpRIssue = 21,      // issuing the next R box loads
+    kTrEpSteps = 22,       // chunk steps
+};
+
+// Per-phase cycle counters of the first epilogue warp (GB_TRACE builds).
+#ifdef GB_TRACE
+#define GB_TR_T0(name) long long name = clock64()
+#define GB_TR_ADD(arr, idx, t0)                                        \
+    do {                                                               \
+        const long long _t1 = clock64();                               \
+        if (arr) arr[(idx) - kTrEpDBox] += static_cast<unsigned long long>(_t1 - (t0)); \
+        t0 = _t1;                                                      \
+    } while (0)
+#else
+#define GB_TR_T0(name)
+#define GB_TR_ADD(arr, idx, t0)
+#endif
+
+struct TraceAcc {  // blocked cycles and blocked waits of one thread
+    unsigned long long cyc = 0, n = 0;
 };
 
 struct SharedCtl {
@@ -157,11 +213,23 @@ __device__ __forceinline__ void record_timeout(uint32_t role, uint32_t where, vo
 // Bounded wait for the phase of `bar` with the given parity.  Returns false if
 // the CTA is aborting or the time limit ran out (then it records the timeout).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort,
-                                         uint64_t timeout_ns, uint32_t role, uint32_t where) {
+                                         uint64_t timeout_ns, uint32_t role, uint32_t where,
+                                         TraceAcc* acc = nullptr) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+#ifdef GB_TRACE
+    const long long c0 = clock64();
+#endif
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) {
+#ifdef GB_TRACE
+            if (acc) {
+                acc->cyc += static_cast<unsigned long long>(clock64() - c0);
+                acc->n += 1;
+            }
+#endif
+            return true;
+        }
         if (*abort) return false;
         if (global_timer_ns() - t0 > timeout_ns) {
             record_timeout(role, where, abort);
@@ -190,6 +258,26 @@ __device__ __forceinline__ void tile_coords(int32_t tile, const GemmParams& p, i
     mb = first_m + local % rows;
     nb = local / rows;
     if (group & 1) nb = p.num_n_blocks - 1 - nb;
+}
+
+// TMA operand loads and output stores, with an L2 policy when one is set.
+template <bool PAIR>
+__device__ __forceinline__ void tma_load_op(uint32_t dst, const void* tm, uint32_t bar, int32_t c0, int32_t c1,
+                                            uint64_t pol) {
+    if constexpr (PAIR) {
+        if (pol) tma_load_2d_pair_hint(dst, tm, bar, c0, c1, pol);
+        else tma_load_2d_pair(dst, tm, bar, c0, c1);
+    } else {
+        if (pol) tma_load_2d_hint(dst, tm, bar, c0, c1, pol);
+        else tma_load_2d(dst, tm, bar, c0, c1);
+    }
+}
+
+// `hint` is an l2_policy code; the policy is made at the store, so the epilogue keeps
+// no 64-bit policy register live across its loops.
+__device__ __forceinline__ void tma_store_op(const void* tm, uint32_t src, int32_t c0, int32_t c1, uint32_t hint) {
+    if (hint) tma_store_2d_hint(tm, src, c0, c1, l2_policy(hint));
+    else tma_store_2d(tm, src, c0, c1);
 }
 
 // ---------------------------------------------------------------- epilogue math
@@ -221,8 +309,54 @@ __device__ __forceinline__ float silu(float x) {
     return x * rcp_approx(1.0f + ex2_approx(x * kNegLog2e));
 }
 
+// Derivatives of act_apply's activations, for the activation-gradient epilogue:
+// GELU (tanh form) x s(x) with s = 1 / (1 + e^{-2u}):  s (1 + x (1 - s) 2 sqrt(2/pi) (1 + 3 0.044715 x^2));
+// SiLU x s(x) with s = 1 / (1 + e^{-x}):              s (1 + x (1 - s));  ReLU: 1 for x > 0, else 0.
+__device__ __forceinline__ float dact_apply(int act, float x) {
+    constexpr double kLog2e = 1.4426950408889634;
+    constexpr double kSqrt2OverPi = 0.7978845608028654;
+    constexpr float c0 = static_cast<float>(-2.0 * kLog2e * kSqrt2OverPi);
+    constexpr float c1 = static_cast<float>(-2.0 * kLog2e * kSqrt2OverPi * 0.044715);
+    constexpr float k0 = static_cast<float>(2.0 * kSqrt2OverPi);
+    constexpr float k1 = static_cast<float>(2.0 * kSqrt2OverPi * 3.0 * 0.044715);
+    switch (act) {
+        case 1: {
+            const float x2 = x * x;
+            const float sg = rcp_approx(1.0f + ex2_approx(x * fmaf(c1, x2, c0)));
+            return sg * fmaf(x * (1.0f - sg), fmaf(k1, x2, k0), 1.0f);
+        }
+        case 2: {
+            const float sg = rcp_approx(1.0f + ex2_approx(x * static_cast<float>(-kLog2e)));
+            return sg * fmaf(x, 1.0f - sg, 1.0f);
+        }
+        case 3:
+            return x > 0.0f ? 1.0f : 0.0f;
+        default:
+            return 1.0f;
+    }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// How an epilogue input value r combines with the accumulator value v: OP 0 adds
+// (v + r), OP 1..3 multiplies by the derivative of activation OP at r (v * act'(r),
+// the activation gradient), OP 4 leaves v (the identity's derivative is 1).
+template <int OP>
+__device__ __forceinline__ void combine2(float& a, float& b, uint32_t w) {
+    if constexpr (OP == 0) {
+        a += bf16_lo(w);
+        b += bf16_hi(w);
+    } else if constexpr (OP <= 3) {
+        a *= dact_apply(OP, bf16_lo(w));
+        b *= dact_apply(OP, bf16_hi(w));
+    }
+}
+
+// The combine OP of this launch's epilogue input.
+__device__ __forceinline__ int input_op(uint32_t flags, int act) {
+    return (flags & 512u /* kFlagDact */) ? (act >= 1 && act <= 3 ? act : 4) : 0;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -270,6 +404,49 @@ __device__ __forceinline__ void add_bf16_box_row(float (&v)[32], uint32_t box, i
         v[8 * u + 5] += bf16_hi(w2);
         v[8 * u + 6] += bf16_lo(w3);
         v[8 * u + 7] += bf16_hi(w3);
+    }
+}
+
+// Combine this lane's row of a 32x32 bf16 box staged by TMA (64-byte swizzle) into v.
+template <int OP>
+__device__ __forceinline__ void combine_box_row(float (&v)[32], uint32_t box, int lane) {
+    const uint32_t row = box + lane * 64;
+    const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(row + ((u ^ sw) << 4)));
+        combine2<OP>(v[8 * u + 0], v[8 * u + 1], w0);
+        combine2<OP>(v[8 * u + 2], v[8 * u + 3], w1);
+        combine2<OP>(v[8 * u + 4], v[8 * u + 5], w2);
+        combine2<OP>(v[8 * u + 6], v[8 * u + 7], w3);
+    }
+}
+
+// The epilogue input of one chunk from its TMA box: added (linear), or the
+// activation gradient's multiplier act'(r) (kFlagDact).
+__device__ __forceinline__ void apply_input_box(const GemmParams& p, float (&v)[32], uint32_t box, int lane) {
+    switch (input_op(p.flags, p.act)) {
+        case 0: combine_box_row<0>(v, box, lane); break;
+        case 1: combine_box_row<1>(v, box, lane); break;
+        case 2: combine_box_row<2>(v, box, lane); break;
+        case 3: combine_box_row<3>(v, box, lane); break;
+        default: break;
+    }
+}
+
+// The same from global memory: a 16-byte aligned row segment of 32 values (rows past M skipped).
+template <int OP>
+__device__ __forceinline__ void combine_row_vec(float (&v)[32], const uint16_t* src) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 w = ld_global_nc_v4(src + 8 * i);
+        combine2<OP>(v[8 * i + 0], v[8 * i + 1], w.x);
+        combine2<OP>(v[8 * i + 2], v[8 * i + 3], w.y);
+        combine2<OP>(v[8 * i + 4], v[8 * i + 5], w.z);
+        combine2<OP>(v[8 * i + 6], v[8 * i + 7], w.w);
     }
 }
 
@@ -327,11 +504,25 @@ __device__ __forceinline__ void add_rows_transposed(const GemmParams& p, float (
     for (int r = 0; r < 32; ++r) col[r * (kTRow / 2)] = h[r];
     __syncwarp();
     const uint32_t* mine = reinterpret_cast<const uint32_t*>(tbuf + lane * kTRow);
+    switch (input_op(p.flags, p.act)) {
+        case 0:
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint32_t w = mine[j];
-        v[2 * j] += bf16_lo(w);
-        v[2 * j + 1] += bf16_hi(w);
+            for (int j = 0; j < 16; ++j) combine2<0>(v[2 * j], v[2 * j + 1], mine[j]);
+            break;
+        case 1:
+#pragma unroll
+            for (int j = 0; j < 16; ++j) combine2<1>(v[2 * j], v[2 * j + 1], mine[j]);
+            break;
+        case 2:
+#pragma unroll
+            for (int j = 0; j < 16; ++j) combine2<2>(v[2 * j], v[2 * j + 1], mine[j]);
+            break;
+        case 3:
+#pragma unroll
+            for (int j = 0; j < 16; ++j) combine2<3>(v[2 * j], v[2 * j + 1], mine[j]);
+            break;
+        default:
+            break;
     }
     __syncwarp();
 }
@@ -358,7 +549,7 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorM
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tm, smem_addr(buf), n0, row0);
+            tma_store_op(tm, smem_addr(buf), n0, row0, p.hint_d);
             bulk_commit_group();
         }
         if (++dslot == p.d_boxes) dslot = 0;
@@ -376,7 +567,9 @@ template <int NUM_B>
 // queue and its position.  Warp-collective.
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32], int32_t m, int32_t row0,
                                              int32_t n0, int lane, uint8_t* dbox, int32_t& dslot,
-                                             uint32_t rbox, uint8_t* tbuf_r) {
+                                             uint32_t rbox, uint8_t* tbuf_r,
+                                             unsigned long long* tr_ep = nullptr) {
+    GB_TR_T0(tx);
     const int valid = min(32, p.n - n0);
     if (NUM_B == 1) {
         if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, valid, p.flags & kFlagBiasVec);
@@ -386,29 +579,56 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
             for (int j = 0; j < 16; ++j) zp[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
             store_chunk(p, &p.tm_z, p.z, p.ldz, p.flags & kFlagZTma, zp, row0, n0, valid, lane, dbox, dslot);
         }
-        switch (p.act) {
-            case 1:
+        const bool dact = p.flags & kFlagDact;
+        if (!dact) {
+            switch (p.act) {
+                case 1:
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
-                break;
-            case 2:
+                    for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                    break;
+                case 2:
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
-                break;
-            case 3:
+                    for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                    break;
+                case 3:
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
-                break;
-            default:
-                break;
+                    for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                    break;
+                default:
+                    break;
+            }
         }
         if (rbox) {
-            add_bf16_box_row(v, rbox, lane);
+            apply_input_box(p, v, rbox, lane);
         } else if (p.flags & kFlagResidual) {
             if (p.flags & kFlagRVec) {
-                if (m < p.m) add_bf16_row(v, p.r + static_cast<int64_t>(m) * p.ldr + n0, valid, true);
+                // R (Z) rows are 16-byte aligned and ldr is a multiple of 8, so a row's
+                // segment is readable to 32 columns whenever the row exists (a partial
+                // segment's tail columns are not stored).  The scalar path covers the
+                // segment past the row's end.
+                if (m < p.m) {
+                    const uint16_t* src = p.r + static_cast<int64_t>(m) * p.ldr + n0;
+                    if (valid == 32) {
+                        switch (input_op(p.flags, p.act)) {
+                            case 0: combine_row_vec<0>(v, src); break;
+                            case 1: combine_row_vec<1>(v, src); break;
+                            case 2: combine_row_vec<2>(v, src); break;
+                            case 3: combine_row_vec<3>(v, src); break;
+                            default: break;
+                        }
+                    } else if (!dact) {
+                        add_bf16_row(v, src, valid, false);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < valid)
+                                v[j] *= dact_apply(p.act, __uint_as_float(static_cast<uint32_t>(__ldg(src + j)) << 16));
+                    }
+                }
             } else {
+                GB_TR_ADD(tr_ep, kTrEpMath, tx);
                 add_rows_transposed(p, v, row0, n0, valid, lane, tbuf_r);
+                GB_TR_ADD(tr_ep, kTrEpRWait, tx);
             }
         }
     }
@@ -416,7 +636,9 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
     uint32_t packed[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    GB_TR_ADD(tr_ep, kTrEpMath, tx);
     store_chunk(p, &p.tm_d, p.d, p.ldd, p.flags & kFlagDTma, packed, row0, n0, valid, lane, dbox, dslot);
+    GB_TR_ADD(tr_ep, kTrEpStore, tx);
 }
 
 // 32 floats added into global memory with vector fp32 reductions (performed in L2).
@@ -510,6 +732,10 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t tmo = p.timeout_ns;
+#ifdef GB_TRACE
+    unsigned long long* trace = p.trace ? p.trace + static_cast<size_t>(blockIdx.x) * kTraceWords : nullptr;
+    if (trace && threadIdx.x == 0) trace[kTrStartNs] = global_timer_ns();
+#endif
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // position in the CTA pair
     const bool leader = rank == 0;
     const int32_t unit = PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
@@ -554,6 +780,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int32_t* abort_flag = &ctl->abort;
+#ifdef GB_TRACE
+    if (trace && threadIdx.x == 0) trace[kTrSetupNs] = global_timer_ns();
+#endif
 
     // Role split.  Each warpgroup sets its register budget inside its own branch, so
     // the compiler holds the control roles to the small budget and gives the
@@ -567,6 +796,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 uint32_t s = 0, ph = 0;  // ring slot and phase of k-block `it`
                 bool ok = true;
                 int32_t local = 0;
+                const uint64_t pol_a = l2_policy(p.hint_a);
+                const uint64_t pol_b = l2_policy(p.hint_b);
+                TraceAcc tr_empty;
                 for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
                     const int32_t tile = w / p.splits;
                     const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
@@ -584,7 +816,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                 ph ^= 1u;
                             }
                         }
-                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, tmo, kRoleProducer, s)) {
+                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, tmo, kRoleProducer, s, &tr_empty)) {
                             ok = false;
                             break;
                         }
@@ -593,21 +825,39 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const uint32_t own_full = smem_addr(&full[s]);
                         if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
                         uint8_t* sb = st + S::kABytes;
-                        if constexpr (PAIR) {
+                        if (NUM_B == 1 && (p.flags & kFlagBMn)) {
+                            // MN-major B (a row-major [K, N] matrix): boxes of 64 output columns
+                            // x 64 contraction rows, one after the other along N
+                            const uint32_t fb = PAIR ? mapa_shared(own_full, 0) : own_full;
+                            tma_load_op<PAIR>(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row, pol_a);
+#pragma unroll
+                            for (int h = 0; h < S::kBRows / 64; ++h)
+                                tma_load_op<PAIR>(smem_addr(sb + h * kMnBoxBytes), &p.tm_b0, fb, b_row + h * 64,
+                                                  kb * kBK, pol_b);
+                        } else if constexpr (PAIR) {
                             const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
-                            tma_load_2d_pair(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row);
+                            tma_load_op<true>(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row, pol_a);
                             if (NUM_B == 1)
-                                tma_load_2d_pair(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row);
+                                tma_load_op<true>(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row, pol_b);
                             else  // this CTA's half of the N = 2 BN operand is one whole product
-                                tma_load_2d_pair(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK, nb * BN);
+                                tma_load_op<true>(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK, nb * BN,
+                                                  pol_b);
                         } else {
-                            tma_load_2d(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row);
-                            tma_load_2d(smem_addr(sb), &p.tm_b0, own_full, kb * kBK, NUM_B == 1 ? b_row : nb * BN);
+                            tma_load_op<false>(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row, pol_a);
+                            tma_load_op<false>(smem_addr(sb), &p.tm_b0, own_full, kb * kBK,
+                                               NUM_B == 1 ? b_row : nb * BN, pol_b);
                             if (NUM_B == 2)
-                                tma_load_2d(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK, nb * BN);
+                                tma_load_op<false>(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK, nb * BN,
+                                                   pol_b);
                         }
                     }
                 }
+#ifdef GB_TRACE
+                if (trace) {
+                    trace[kTrProdEmptyCyc] = tr_empty.cyc;
+                    trace[kTrProdEmptyN] = tr_empty.n;
+                }
+#endif
                 if (!ok && leader) {
                     // Drain: the leader's full barriers count the bytes of both CTAs; wait
                     // (bounded) for the loads of the last `stages` k-blocks to land.
@@ -627,13 +877,22 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 bool ok = true;
                 bool issued = false;
                 int32_t local = 0;
+                TraceAcc tr_full, tr_acc;
+                const bool b_mn = NUM_B == 1 && (p.flags & kFlagBMn);
+                const uint32_t idesc = S::kIdesc | (b_mn ? kIdescBMnMajor : 0u);
+                const uint32_t bstep = b_mn ? (16u * 128u) >> 4 : 2u;
+#ifdef GB_TRACE
+                const long long mma_c0 = clock64();
+                if (trace) trace[kTrMmaFirstNs] = 0;
+#endif
                 for (int32_t w = unit; ok && w < num_work; w += units, ++local) {
                     const int32_t tile = w / p.splits;
                     const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
                     const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
                     const uint32_t b = local & 1;
                     const uint32_t aph = (local >> 1) & 1u;
-                    if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, tmo, kRoleMma, 0x100u | b)) {
+                    if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, tmo, kRoleMma, 0x100u | b,
+                                  &tr_acc)) {
                         ok = false;
                         break;
                     }
@@ -644,19 +903,24 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             s = 0;
                             ph ^= 1u;
                         }
-                        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s)) {
+                        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s, &tr_full)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
+#ifdef GB_TRACE
+                        if (trace && !issued) trace[kTrMmaFirstNs] = global_timer_ns();
+#endif
                         const uint32_t a_addr = smem_addr(ring + s * S::kStageBytes);
                         const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
-                        const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + S::kABytes);
+                        const uint64_t bdesc = b_mn ? sdesc_mnmajor_sw128(a_addr + S::kABytes, kMnBoxBytes)
+                                                    : sdesc_kmajor_sw128(a_addr + S::kABytes);
     #pragma unroll
                         for (int j = 0; j < kBK / 16; ++j) {
-                            // +32 bytes along K per 16-element slice: +2 in the >>4-encoded address
+                            // per 16-element K slice: +32 bytes in a K-major tile, +16 rows of 128 bytes
+                            // in an MN-major one (+2 / +128 in the >>4-encoded address)
                             const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
-                            mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, S::kIdesc, acc);
+                            mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + bstep * j, idesc, acc);
                         }
                         issued = true;
                         if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
@@ -666,6 +930,17 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), 0x3);
                     else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
                 }
+#ifdef GB_TRACE
+                if (trace) {
+                    trace[kTrMmaLastNs] = global_timer_ns();
+                    trace[kTrMmaCyc] = static_cast<unsigned long long>(clock64() - mma_c0);
+                    trace[kTrMmaFullCyc] = tr_full.cyc;
+                    trace[kTrMmaFullN] = tr_full.n;
+                    trace[kTrMmaAccCyc] = tr_acc.cyc;
+                    trace[kTrMmaAccN] = tr_acc.n;
+                    trace[kTrMmaItems] = static_cast<unsigned long long>(local);
+                }
+#endif
                 if (!ok && issued) {
                     // Drain: every MMA issued so far must finish before TMEM is freed.
                     mma_commit<CG>(smem_addr(&ctl->drain));
@@ -692,6 +967,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         uint8_t* dbox = dstage + e * p.d_boxes * kDStageBytes;  // this warp's D staging queue
         int32_t dslot = 0;
         int32_t local = 0;
+        TraceAcc tr_accfull;
+#ifdef GB_TRACE
+        unsigned long long tr_body = 0;
+        unsigned long long tr_ep[7] = {0, 0, 0, 0, 0, 0, 0};
+#endif
 
         // R by TMA (linear, no split): a cursor over this warp's future (tile, chunk)
         // pairs keeps up to r_boxes 32x32 R boxes in flight ahead of their use, so
@@ -736,8 +1016,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_islot]);
                 mbar_arrive_expect_tx(bar, kDStageBytes);
-                tma_load_2d(smem_addr(rbox0 + r_islot * kDStageBytes), &p.tm_r, bar, rc_nb * BN + rc_c * kDChunk,
-                            rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32);
+                tma_load_op<false>(smem_addr(rbox0 + r_islot * kDStageBytes), &p.tm_r, bar, rc_nb * BN + rc_c * kDChunk,
+                                   rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32, l2_policy(p.hint_r));
             }
             ++r_pending;
             if (++r_islot == p.r_boxes) r_islot = 0;
@@ -758,10 +1038,18 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             const uint32_t aph = (local >> 1) & 1u;
             bool ok = true;
             if (lane == 0)
-                ok = wait_bar(smem_addr(&ctl->acc_full[b]), aph, abort_flag, tmo, kRoleEpilogue, b);
+                ok = wait_bar(smem_addr(&ctl->acc_full[b]), aph, abort_flag, tmo, kRoleEpilogue, b, &tr_accfull);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
+#ifdef GB_TRACE
+            const long long body_c0 = clock64();
+            struct BodyTimer {  // adds the cycles of this iteration, however it ends
+                unsigned long long& sum;
+                long long c0;
+                __device__ ~BodyTimer() { sum += static_cast<unsigned long long>(clock64() - c0); }
+            } body_timer{tr_body, body_c0};
+#endif
 
             const int32_t tile = w / p.splits;
             int32_t mb, nb;
@@ -779,6 +1067,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const int32_t n0 = nb * BN + c * kDChunk;
                     const bool chunk_on = warp_rows && n0 < p.n;
                     float v[32];
+                    GB_TR_T0(tx);
                     if (chunk_on) {
                         uint32_t r0[32];
                         tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
@@ -802,6 +1091,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                         }
                     }
+                    GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
                     if (!chunk_on) continue;
                     if (NUM_B == 1) {
                         if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
@@ -825,9 +1115,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     uint32_t packed[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                    GB_TR_ADD(tr_ep, kTrEpMath, tx);
                     uint8_t* buf = dbox + dslot * kDStageBytes;
                     if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
                     __syncwarp();
+                    GB_TR_ADD(tr_ep, kTrEpDBox, tx);
                     const uint32_t row_addr = smem_addr(buf) + lane * 64;
                     const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
@@ -837,10 +1129,14 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tm_d, smem_addr(buf), n0, row0);
+                        tma_store_op(&p.tm_d, smem_addr(buf), n0, row0, p.hint_d);
                         bulk_commit_group();
                     }
                     if (++dslot == p.d_boxes) dslot = 0;
+                    GB_TR_ADD(tr_ep, kTrEpStore, tx);
+#ifdef GB_TRACE
+                    tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+#endif
                 }
                 continue;
             }
@@ -857,11 +1153,16 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const bool last = c + 2 * cstep >= kChunks;
                         const int nchunks = !(warp_rows && nb * BN + c * kDChunk < p.n) ? 0
                                             : (nb * BN + (c + cstep) * kDChunk < p.n ? 2 : 1);
+                        GB_TR_T0(tx);
                         if (nchunks > 0) {
                             // two D boxes free: the stores that last used them have read them
                             if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 2);
                             __syncwarp();
                         }
+                        GB_TR_ADD(tr_ep, kTrEpDBox, tx);
+#ifdef GB_TRACE
+                        tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+#endif
                         uint32_t box_a = 0;
 #pragma unroll 1
                         for (int i = 0; i < 2; ++i) {
@@ -875,6 +1176,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
                             }
+                            GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
                             if (last && i == 1) {  // this warp's last TMEM reads of the buffer are done
                                 tc_fence_before_sync();
                                 __syncwarp();
@@ -885,7 +1187,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             }
                             if (i >= nchunks) continue;
                             if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
-                            switch (p.act) {
+                            switch ((p.flags & kFlagDact) ? 0 : p.act) {
                                 case 1:
 #pragma unroll
                                     for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
@@ -901,6 +1203,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                 default:
                                     break;
                             }
+                            GB_TR_ADD(tr_ep, kTrEpMath, tx);
                             // this chunk's R box: the one at the use position of the queue
                             const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
                             const uint32_t par = (r_phase >> r_uslot) & 1u;
@@ -909,13 +1212,15 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             if (!rok) break;
                             while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
                             }
+                            GB_TR_ADD(tr_ep, kTrEpRWait, tx);
                             r_phase ^= 1u << r_uslot;
-                            add_bf16_box_row(v, smem_addr(rbox0 + r_uslot * kDStageBytes), lane);
+                            apply_input_box(p, v, smem_addr(rbox0 + r_uslot * kDStageBytes), lane);
                             --r_pending;
                             if (++r_uslot == p.r_boxes) r_uslot = 0;
                             const uint32_t box = smem_addr(dbox + dslot * kDStageBytes);
                             if (++dslot == p.d_boxes) dslot = 0;
                             stage_box_row(box, v, lane);
+                            GB_TR_ADD(tr_ep, kTrEpMath, tx);
                             if (i == 0) {
                                 box_a = box;
                                 continue;
@@ -925,23 +1230,26 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                tma_store_2d(&p.tm_d, box_a, n0 - cstep * kDChunk, row0);
+                                tma_store_op(&p.tm_d, box_a, n0 - cstep * kDChunk, row0, p.hint_d);
                                 bulk_commit_group();
-                                tma_store_2d(&p.tm_d, box, n0, row0);
+                                tma_store_op(&p.tm_d, box, n0, row0, p.hint_d);
                                 bulk_commit_group();
                             }
+                            GB_TR_ADD(tr_ep, kTrEpStore, tx);
                         }
                         if (!rok) break;
                         if (nchunks == 1) {  // chunk a alone (b is past N)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                tma_store_2d(&p.tm_d, box_a, nb * BN + c * kDChunk, row0);
+                                tma_store_op(&p.tm_d, box_a, nb * BN + c * kDChunk, row0, p.hint_d);
                                 bulk_commit_group();
                             }
                         }
+                        GB_TR_T0(ti);
 #pragma unroll 1
                         for (int i = 0; i < nchunks; ++i) r_issue();
+                        GB_TR_ADD(tr_ep, kTrEpRIssue, ti);
                     }
                     if (!rok) break;
                     continue;
@@ -957,6 +1265,10 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 const int32_t n0 = nb * BN + c * kDChunk;
                 const bool chunk_on = warp_rows && n0 < p.n;
                 float v[32];
+                GB_TR_T0(tg);
+#ifdef GB_TRACE
+                tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+#endif
                 if (chunk_on && p.num_k_blocks > 0) {
                     uint32_t r0[32];
                     tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
@@ -995,6 +1307,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                     }
                 }
+                GB_TR_ADD(tr_ep, kTrEpTmemLd, tg);
                 if (!chunk_on || split_mode) continue;
                 uint32_t rbox = 0;
                 if (r_tma) {
@@ -1009,7 +1322,12 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     r_phase ^= 1u << r_uslot;
                     rbox = smem_addr(rbox0 + r_uslot * kDStageBytes);
                 }
+                GB_TR_ADD(tr_ep, kTrEpRWait, tg);
+#ifdef GB_TRACE
+                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r, tr_ep);
+#else
                 finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r);
+#endif
                 if (r_tma) {
                     __syncwarp();  // every lane has read the box: refill it
                     fence_proxy_async_smem();
@@ -1049,6 +1367,15 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, 0u, tbuf_r);
             }
         }
+#ifdef GB_TRACE
+        if (trace && e == 0 && lane == 0) {
+            trace[kTrEpiFullCyc] = tr_accfull.cyc;
+            trace[kTrEpiFullN] = tr_accfull.n;
+            trace[kTrEpiBodyCyc] = tr_body;
+            trace[kTrEndNs] = global_timer_ns();
+            for (int i = 0; i < 7; ++i) trace[kTrEpDBox + i] = tr_ep[i];
+        }
+#endif
         if (lane == 0) {
             // R boxes still in flight after an early stop (at most r_boxes, from the use
             // position on): wait (bounded) for them to land.

@@ -94,6 +94,47 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// ---------------------------------------------------------------- L2 cache policies
+
+// An L2 eviction policy for the whole access (fraction 1.0): code 1 = evict first
+// (streamed data that should not displace reused data), 2 = evict last (data that
+// is read again by other CTAs soon).  Returns 0 for code 0 (no hint).
+__device__ __forceinline__ uint64_t l2_policy(uint32_t code) {
+    uint64_t pol = 0;
+    if (code == 1)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else if (code == 2)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d / tma_load_2d_pair with an L2 cache policy from l2_policy().
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                                 int32_t c1, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                                      int32_t c1, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+// 2-D tiled store shared -> global with an L2 cache policy.
+__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src, int32_t c0, int32_t c1,
+                                                  uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(src), "l"(pol)
+                 : "memory");
+}
+
 // 2-D tiled store shared -> global (out-of-range parts of the box are not written).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -179,6 +220,22 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile (B of a product
+// whose contraction runs over the rows of a row-major matrix) written by TMA in
+// boxes of 64 contiguous elements (128 bytes, 128B swizzle) x 64 contraction rows:
+// one row per contraction index, 8-row swizzle atoms 1024 B apart along the
+// contraction (stride-dimension offset), and 64-element blocks along MN
+// `mn_block_bytes` apart (leading-dimension offset: one box).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both K-major:
 // D format (bits 4-5) = 1 (f32), A format (7-9) = 1 (bf16), B format (10-12)
 // = 1 (bf16), no negation / transposition, N >> 3 in bits 17-22, M >> 4 in
@@ -187,6 +244,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+// Bit 16 of the instruction descriptor: the B operand is MN-major (transposed).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 
 // One thread: D[tmem] (+)= A[smem] . B[smem]^T for one K=16 slice.  With
 // CG == 2 (issued by the even CTA of a pair) A is M=256 rows split 128/128

@@ -18,6 +18,10 @@ synthetic stand-ins the library is measured and checked on):
                  variance like R; scaling both would make the product ~1/sqrt(K),
                  smaller than the tolerance.)
 * ``int64``      A[65536,65536] (2^32 elements), B[4096,65536] ~ U(-1,1)/256; D = A.B^T.
+* ``mlp_dact``   the MLP layer's backward activation-gradient product: dY[8192,14336] ~ N(0,1)
+                 (the gradient of the layer's output), W[14336,4096] ~ N(0, 0.02) (the MLP
+                 weight, in the layout the forward pass reads), Z[8192,4096] ~ N(0,1) (the
+                 stored pre-activation of the layer's input); D = (dY.W) * GELU_tanh'(Z).
 
 N(mu, s) means standard deviation s.  Every tensor is drawn in fp32 from its own
 ``torch.Generator`` seeded with ``seed + offset`` (A/X: 0, B/W/W1: 1, bias/W3: 2,
@@ -118,6 +122,13 @@ def int64_case(device="cpu", seed: int = 0, M: int = 65536, N: int = 4096, K: in
             "act": "none"}
 
 
+def mlp_dact(device="cpu", seed: int = 0, M: int = 8192, N: int = 14336, K: int = 4096) -> dict:
+    return {"dY": randn_bf16((M, N), seed=seed + OFFSETS["A"], device=device),
+            "W": randn_bf16((N, K), seed=seed + OFFSETS["B"], std=0.02, device=device),
+            "Z": randn_bf16((M, K), seed=seed + OFFSETS["R"], device=device),
+            "act": "gelu_tanh"}
+
+
 def ragged_combos():
     return [(m, n, k) for m in RAGGED_M for n in RAGGED_N for k in RAGGED_K]
 
@@ -147,6 +158,18 @@ def sample_indices(M: int, N: int, *, seed: int = 1234, rows: int = 256, cols: i
         return np.sort(np.concatenate([special, extra]))
 
     return pick(M, rows, tile_m), pick(N, cols, tile_n)
+
+
+def sample_pairs(M: int, N: int, *, n: int = 65536, seed: int = 4242) -> tuple[np.ndarray, np.ndarray]:
+    """n independent output entries (i, j): the four corners, then i and j drawn
+    independently and uniformly with replacement from ``numpy.random.default_rng(seed)``."""
+    rng = np.random.default_rng(seed)
+    i = rng.integers(0, M, size=n, dtype=np.int64)
+    j = rng.integers(0, N, size=n, dtype=np.int64)
+    corners = np.array([[0, 0], [0, N - 1], [M - 1, 0], [M - 1, N - 1]], dtype=np.int64)
+    k = min(4, n)
+    i[:k], j[:k] = corners[:k, 0], corners[:k, 1]
+    return i, j
 
 
 def to_bits(t: torch.Tensor) -> np.ndarray:

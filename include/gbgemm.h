@@ -169,6 +169,33 @@ GB_API gb_status_t gb_gemm_ffn_gated_splitk(const void* X, int64_t ldx, const vo
                                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Activation gradient of a linear layer's input (the backward-pass consumer of
+ * the pre-activation that gb_gemm_linear_preact stores):
+ *
+ *   D[m,k] = bf16( sum_n dY[m,n] W[n,k] * act'(Z[m,k]) )
+ *
+ * dY [M,N] is the gradient of the layer's output, W [N,K] the layer's weight in
+ * the same row-major layout gb_gemm_linear takes as B (so the contraction runs
+ * over the rows of W: an MN-major tensor-core operand, read by TMA as it is, with
+ * no transposed copy), and Z [M,K] the pre-activation whose activation `act`
+ * produced the layer's input.  act' is the derivative of the tanh-form GELU, of
+ * SiLU, of ReLU (1 for z > 0, else 0) or of the identity (1).  "Implement
+ * persistent matmul scheduling" (NVIDIA/Fuser PR #3812, description: MLP
+ * benchmark tests with epilogue fusions) and "Automate performant Hopper matmul"
+ * (NVIDIA/Fuser issue #3819, section "Epilogue": epilogue inputs) name the
+ * fusion pattern; the formula is its plain reading (chain rule).
+ * dY and W: base 16-byte aligned, lddy and ldw multiples of 8 (TMA), lddy >= N,
+ * ldw >= K.  Z and D: 2-byte aligned, ldz >= K, ldd >= K; TMA when 16-byte
+ * aligned rows, else plain loads and stores.  Z is required (GB_ERR_INVALID_ARG
+ * if NULL).  N == 0 gives D = 0 * act'(Z) (signed zeros).  D must not overlap dY
+ * or W; D == Z (same pointer and leading dimension) is allowed.  Other arguments,
+ * errors and limits as gb_gemm_linear.
+ */
+GB_API gb_status_t gb_gemm_linear_dact(const void* dY, int64_t lddy, const void* W, int64_t ldw,
+                                       const void* Z, int64_t ldz, int act, void* D, int64_t ldd,
+                                       int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * Workspace bytes the split-K call needs for this problem on the current
  * device under the current configuration (ffn: 0 = linear, 1 = FFN fusion;
  * splits as above).  Writes 0 when the plan does not split.  Needs a CUDA
@@ -239,7 +266,10 @@ GB_API const char* gb_last_error(void);
  * pingpong (1 = the two epilogue warpgroups alternate whole tiles, each owning
  * one TMEM accumulator buffer, instead of sharing every tile's chunks; implies
  * epi=2, GB_ERR_INVALID_ARG with epi=1 at the call, no effect with split-K;
- * 0 = never; -1 = auto: on for work items of at most 4 k-blocks).
+ * 0 = never; -1 = auto: on for work items of at most 4 k-blocks), hint_a,
+ * hint_b, hint_r, hint_d (L2 eviction policy of the TMA loads of A, of B / W1 /
+ * W3, of R, and of the TMA stores of D and Z: 0 = none, 1 = evict first, 2 =
+ * evict last, -1 = the built-in choice).
  * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
  */
 GB_API gb_status_t gb_set_config(const char* spec);
@@ -265,6 +295,33 @@ GB_API gb_status_t gb_set_fault_injection(int mode);
  * (tile shape, stages, grid, swizzle, store path) into buf (NUL-terminated,
  * truncated to len). Returns GB_OK, or GB_ERR_INVALID_ARG for a null buf. */
 GB_API gb_status_t gb_last_plan(char* buf, size_t len);
+
+/*
+ * Timing trace, for a library built with -DGB_TRACE (the normal build returns
+ * GB_ERR_UNSUPPORTED).  `buf` is device memory of the caller (NULL turns the
+ * trace off).  Every later launch whose grid fits (16 unsigned 64-bit words per
+ * CTA) writes one record per CTA: %globaltimer at entry, after set-up, at the
+ * first MMA, at the last accumulator commit and at the end of the epilogue, and
+ * the SM clock cycles the producer, the MMA issuer and the first epilogue warp
+ * spent blocked on their barriers (with the number of blocked waits).  The layout
+ * is kTrace* in gemm_kernel.cuh.
+ */
+GB_API gb_status_t gb_set_trace_buffer(void* buf, size_t bytes);
+
+/*
+ * Tensor-core rate probe (a measurement, not part of the GEMM path): `units`
+ * CTAs (cta_group 1) or CTA pairs (cta_group 2), one per SM (pair of SMs), each
+ * issue `num_mma` back-to-back tcgen05.mma.kind::f16 instructions of
+ * M = 128 * cta_group, N = n (128 or 256), K = 16 from zeroed shared memory into
+ * TMEM (alternate != 0: two accumulators in turn), with no loads and no
+ * epilogue, and time them in SM clock cycles.  Writes the median over units of
+ * the cycles per MMA and the dense bf16 rate per SM and clock it implies
+ * (2 M N 16 / cycles / cta_group).  The nominal peak of the GPU is then
+ * SMs x clock x that rate.  Runs on the legacy default stream and synchronises
+ * the device.  num_mma in [8, 65536]; units in [1, SMs / cta_group].
+ */
+GB_API gb_status_t gb_measure_mma_rate(int cta_group, int n, int alternate, int num_mma, int units,
+                                       double* flops_per_clk_per_sm, double* cycles_per_mma);
 
 /* Library version as "major.minor.patch". */
 GB_API const char* gb_version(void);

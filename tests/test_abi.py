@@ -152,3 +152,33 @@ def test_preact_entry_point_validates_first(L):
     assert call(ldz=16) == GB_ERR_INVALID_ARG and b"ldz" in L.gb_last_error()
     assert call(Z=P1) == GB_ERR_UNSUPPORTED
     assert L.gb_gemm_linear_preact(None, 0, None, 0, None, None, 0, 0, None, 0, None, 0, 0, 4, 4, None) == GB_OK
+
+
+def dact(L, dY=P16, lddy=64, W=P16, ldw=32, Z=P16, ldz=32, act=1, D=P16, ldd=32, M=16, N=64, K=32):
+    return L.gb_gemm_linear_dact(dY, lddy, W, ldw, Z, ldz, act, D, ldd, M, N, K, None)
+
+
+@pytest.mark.parametrize("kwargs,status,needle", [
+    (dict(Z=None), GB_ERR_INVALID_ARG, "Z is null"),
+    (dict(dY=None), GB_ERR_INVALID_ARG, "dY is null"),
+    (dict(W=None), GB_ERR_INVALID_ARG, "W is null"),
+    (dict(lddy=32), GB_ERR_INVALID_ARG, "lddy"),
+    (dict(ldw=16), GB_ERR_INVALID_ARG, "ldw"),
+    (dict(ldz=16), GB_ERR_INVALID_ARG, "ldz"),
+    (dict(ldd=16), GB_ERR_INVALID_ARG, "ldd"),
+    (dict(act=9), GB_ERR_INVALID_ARG, "activation"),
+    (dict(W=P2), GB_ERR_UNSUPPORTED, "16-byte"),
+    (dict(ldw=36), GB_ERR_UNSUPPORTED, "multiples of 8"),
+    (dict(Z=P1), GB_ERR_UNSUPPORTED, "2-byte"),
+])
+def test_dact_rejects(L, kwargs, status, needle):
+    assert dact(L, **kwargs) == status
+    assert needle in L.gb_last_error().decode()
+
+
+def test_probe_rejects_bad_arguments(L):
+    import ctypes
+    r, c = ctypes.c_double(0), ctypes.c_double(0)
+    assert L.gb_measure_mma_rate(3, 256, 0, 1024, 1, ctypes.byref(r), ctypes.byref(c)) == GB_ERR_INVALID_ARG
+    assert L.gb_measure_mma_rate(2, 64, 0, 1024, 1, ctypes.byref(r), ctypes.byref(c)) == GB_ERR_INVALID_ARG
+    assert L.gb_measure_mma_rate(2, 256, 0, 4, 1, ctypes.byref(r), ctypes.byref(c)) == GB_ERR_INVALID_ARG

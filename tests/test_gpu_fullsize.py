@@ -1,7 +1,9 @@
 """Full-size workloads on the GPU, in the launch configuration the benchmark times,
-checked against the CPU oracle on a seeded sample of 65536 output entries (a
-256 x 256 grid of rows and columns that always includes the first/last row and
-column and tile boundaries), or on every entry when the oracle can afford it.
+checked against the CPU oracle on two seeded samples of 65536 output entries each
+-- a 256 x 256 grid of rows and columns that always includes the first/last row
+and column and tile boundaries, and 65536 independent (i, j) pairs -- or on every
+entry when the oracle can afford it.  On the sampled pairs at least 99 % of the
+entries must also lie within one bf16 ulp of the float64 result.
 
 Workloads (shapes and distributions as in ``dense_bf16_gemm_persistent_gb300.inputs``):
 MLP linear + bias + GELU_tanh 8192x14336x4096; Llama-FFN 8192x14336x4096; the
@@ -14,7 +16,7 @@ import torch
 import oracle
 import dense_bf16_gemm_persistent_gb300 as gb
 from dense_bf16_gemm_persistent_gb300 import inputs
-from tests.gpu_util import assert_bitexact, assert_close, bits, ulp_hist
+from tests.gpu_util import assert_bitexact, assert_close, bits, check_pairs, ulp_hist
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +57,8 @@ def test_mlp_gelu_8192x14336x4096():
     ref64 = oracle.linear_f64(rows_of(w["A"], r), rows_of(w["B"], c), bits(w["bias"])[c], None, "gelu_tanh")
     h = ulp_hist(got, ref64)
     assert sum(v for k, v in h.items() if k <= 1) >= 0.99 * got.size, h
+    i, j = inputs.sample_pairs(8192, 14336, seed=11)
+    check_pairs("linear", D, w, i, j, act="gelu_tanh", what="mlp_gelu pairs")
 
 
 def test_llama_ffn_8192x14336x4096():
@@ -64,6 +68,8 @@ def test_llama_ffn_8192x14336x4096():
     r, c = sample(8192, 14336, seed=4321)
     ref = oracle.ffn_gated(rows_of(w["X"], r), rows_of(w["W1"], c), rows_of(w["W3"], c))
     assert_close(grid_of(D, r, c), ref, "llama_ffn")
+    i, j = inputs.sample_pairs(8192, 14336, seed=12)
+    check_pairs("ffn", D, w, i, j, what="llama_ffn pairs")
 
 
 @pytest.mark.parametrize("split_k", [None, "auto"], ids=["nosplit", "autosplit"])
@@ -77,10 +83,17 @@ def test_ragged_residual(M, N, K, split_k):
     if M * N * K <= FULL_COMPARE_MACS:
         ref = oracle.linear(bits(w["A"]), bits(w["B"]), None, bits(w["R"]))
         assert_close(bits(D), ref, f"ragged {M}x{N}x{K}")
+        if K == 65536:
+            ref64 = oracle.linear_f64(bits(w["A"]), bits(w["B"]), None, bits(w["R"]))
+            h = ulp_hist(bits(D), ref64)
+            assert sum(v for k, v in h.items() if k <= 1) >= 0.99 * D.numel(), h
     else:
         r, c = sample(M, N, seed=M + N + K)
         ref = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c), None, grid_of(w["R"], r, c))
         assert_close(grid_of(D, r, c), ref, f"ragged {M}x{N}x{K}")
+        i, j = inputs.sample_pairs(M, N, seed=M * 3 + N + K)
+        check_pairs("linear", D, {"A": w["A"], "B": w["B"], "R": w["R"]}, i, j,
+                    ulp_gate=0.99 if K == 65536 else None, what=f"ragged {M}x{N}x{K} pairs")
     if K == 4096 and split_k is None:
         # the product alone (R = 0), and the residual alone (A = 0: D must equal R exactly)
         Z = torch.zeros_like(w["R"])
@@ -104,6 +117,9 @@ def test_int64_indexing_65536x4096x65536():
     assert (r >= 32768).sum() >= 100
     ref = oracle.linear(rows_of(w["A"], r), rows_of(w["B"], c))
     assert_close(grid_of(D, r, c), ref, "int64")
+    i, j = inputs.sample_pairs(M, N, seed=13)
+    assert (i >= 32768).sum() >= 30000
+    check_pairs("linear", D, w, i, j, what="int64 pairs")
     # an index-revealing pattern: A[i, 0] = (i mod 7) - 3, B[n, 0] = 1, all else 0  ->  D[i, n] = (i mod 7) - 3
     A = w["A"]
     A.zero_()
