@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.gb_set_trace_buffer.argtypes = [p, ctypes.c_size_t]
         L.gb_measure_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        L.gb_probe_mma_issue.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_double)]
         L.gb_version.argtypes = []
         L.gb_version.restype = ctypes.c_char_p
         for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_preact", "gb_gemm_linear_dact",
@@ -82,7 +85,7 @@ def lib() -> ctypes.CDLL:
                      "gb_splitk_workspace_bytes", "gb_gemm_linear_splitk_noalloc", "gb_static_scratch_bytes",
                      "gb_get_device_status", "gb_set_config",
                      "gb_set_wait_timeout_ns", "gb_set_fault_injection", "gb_last_plan", "gb_set_trace_buffer",
-                     "gb_measure_mma_rate"):
+                     "gb_measure_mma_rate", "gb_probe_mma_issue"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -248,6 +251,16 @@ def measure_mma_rate(cta_group: int = 2, n: int = 256, alternate: bool = False, 
     _check(lib().gb_measure_mma_rate(int(cta_group), int(n), 1 if alternate else 0, int(num_mma), int(units),
                                      ctypes.byref(rate), ctypes.byref(cyc)))
     return rate.value, cyc.value
+
+
+def probe_mma_issue(cta_group: int = 2, n: int = 256, mode: int = 0, alu: int = 0, num_mma: int = 8192,
+                    units: int = 1) -> tuple[float, float]:
+    """(cycles per MMA, TMEM loads per MMA) with the steps of `mode` around or beside the MMAs
+    (see the header)."""
+    cyc, lds = ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().gb_probe_mma_issue(int(cta_group), int(n), int(mode), int(alu), int(num_mma), int(units),
+                                    ctypes.byref(cyc), ctypes.byref(lds)))
+    return cyc.value, lds.value
 
 
 def set_trace_buffer(buf: torch.Tensor | None) -> None:

@@ -60,6 +60,10 @@ struct Config {
     // L2 eviction hints for the TMA traffic of A, B, R and D (and Z): -1 = default,
     // 0 = none, 1 = evict first, 2 = evict last
     int hint_a = -1, hint_b = -1, hint_r = -1, hint_d = -1;
+    int mc = -1;         // A multicast between two CTA pairs (4-CTA clusters): -1 auto, 0 off, 1 on
+    int issue = -1;      // MMA issue loop: -1 auto, 0 rebuild, 1 lean, 2 lean with look-ahead wait
+    int tmem_ld = 0;     // TMEM columns per load on the express path: 0 auto, 32 or 64
+    int prod = 0;        // producer threads: 0 auto, 1 or 2 (A and B loads issued by different warps)
 };
 
 std::mutex g_cfg_mu;
@@ -195,10 +199,11 @@ struct Variant {
     static constexpr bool kPair = PAIR;
     static constexpr int kTileM = S::kTileM;
 
-    static gb_status_t prepare(int dev, const DeviceInfo& info, int* max_units) {
+    static gb_status_t prepare(int dev, const DeviceInfo& info, int* max_units, int* max_units_mc) {
         static std::mutex mu;
         static bool ready[64] = {};
         static int units[64] = {};
+        static int units_mc[64] = {};
         auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR, EPI>;
         const uint32_t smem_max = S::smem_bytes(STAGES, 2, 0);
         const uint32_t smem_min = S::smem_bytes(2, 2, NUM_B == 1 ? 2 : 0);
@@ -227,12 +232,21 @@ struct Variant {
                 if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
                 if (n < 1) return fail(GB_ERR_UNSUPPORTED, "no CTA pair fits on this device");
                 units[dev] = n;
+                // clusters of two CTA pairs (A multicast); 0 if none fits
+                attr[0].val.clusterDim.x = 4;
+                cfg.gridDim = dim3(4 * (info.sms / 4), 1, 1);
+                int n4 = 0;
+                e = cudaOccupancyMaxActiveClusters(&n4, kern, &cfg);
+                units_mc[dev] = e == cudaSuccess ? n4 : 0;
+                (void)cudaGetLastError();
             } else {
                 units[dev] = info.sms;
+                units_mc[dev] = 0;
             }
             ready[dev] = true;
         }
         *max_units = units[dev];
+        if (max_units_mc) *max_units_mc = units_mc[dev];
         return GB_OK;
     }
 
@@ -261,13 +275,13 @@ struct Variant {
         auto kern = gb::gemm_persistent_kernel<BN, NUM_B, STAGES, PAIR, EPI>;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
-        cfg.gridDim = dim3(units * S::kCG, 1, 1);
+        cfg.gridDim = dim3(units * S::kCG * (p.mc ? 2 : 1), 1, 1);
         cfg.blockDim = dim3(S::kThreads, 1, 1);
         cfg.dynamicSmemBytes = S::smem_bytes(p.stages, p.d_boxes, p.r_boxes);
         cfg.stream = stream;
         if (PAIR) {
             attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.x = p.mc ? 4 : 2;
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
@@ -371,8 +385,8 @@ template <class V>
 gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int dev, const DeviceInfo& info,
                             uint64_t timeout_ns, int inject, cudaStream_t stream, const SplitReq& sr) {
     gb_status_t st;
-    int max_units = 0;
-    if ((st = V::prepare(dev, info, &max_units)) != GB_OK) return st;
+    int max_units = 0, max_units_mc = 0;
+    if ((st = V::prepare(dev, info, &max_units, &max_units_mc)) != GB_OK) return st;
 
     GemmParams prm;
     memset(&prm, 0, sizeof prm);
@@ -382,7 +396,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.num_m_blocks = static_cast<int32_t>(cdiv(pr.m, V::kTileM));
     prm.num_n_blocks = static_cast<int32_t>(cdiv(pr.n, bn));
     prm.num_k_blocks = static_cast<int32_t>(cdiv(pr.k, gb::kBK));
-    const int64_t tiles = static_cast<int64_t>(prm.num_m_blocks) * prm.num_n_blocks;
+    // A multicast between two CTA pairs: on request, for CTA-pair variants without a
+    // split, when 4-CTA clusters fit; a work item is then one tile-row x two tile-columns.
+    const bool mc = V::kPair && cfg.mc == 1 && max_units_mc > 0 && !(sr.allowed) && pr.k > 0;
+    prm.mc = mc ? 1 : 0;
+    prm.sched_n_blocks = mc ? static_cast<int32_t>(cdiv(prm.num_n_blocks, 2)) : prm.num_n_blocks;
+    const int64_t tiles = static_cast<int64_t>(prm.num_m_blocks) * prm.sched_n_blocks;
     if (tiles > kMaxDim) return fail(GB_ERR_UNSUPPORTED, "too many tiles");
     prm.num_tiles = static_cast<int32_t>(tiles);
 
@@ -451,6 +470,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.hint_b = hint(cfg.hint_b, 0);
     prm.hint_r = hint(cfg.hint_r, 0);
     prm.hint_d = hint(cfg.hint_d, 0);
+    prm.issue = cfg.issue >= 0 ? cfg.issue : 0;
+    prm.tmem_ld = cfg.tmem_ld > 0 ? cfg.tmem_ld : 32;
+    // two producer threads by default: measured 7-12 % faster than one on the MLP, FFN,
+    // activation-gradient, 64-bit and unaligned shapes (one thread issuing both loads of
+    // every stage falls behind the MMAs)
+    prm.prod = cfg.prod > 0 ? cfg.prod : 2;
     uint32_t flags = 0;
     if (!pr.ffn && pr.bias) flags |= gb::kFlagBias | (aligned16(pr.bias) ? gb::kFlagBiasVec : 0u);
     if (!pr.ffn && pr.r) flags |= gb::kFlagResidual | ((aligned16(pr.r) && pr.ldr % 8 == 0) ? gb::kFlagRVec : 0u);
@@ -477,6 +502,9 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         if ((st = make_tmap(&prm.tm_a, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             GB_OK)
             return st;
+        if ((mc || prm.prod == 3) && (st = make_tmap(&prm.tm_a_half, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM / 2,
+                                                    CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
+            return st;
         if (pr.dact) {
             // B = W [k rows (contraction), n columns]: boxes of 64 columns x 64 rows
             if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.n, pr.k, pr.ldb0 * 2, 64, gb::kBK,
@@ -502,9 +530,10 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
 
     // Scheduling units: CTAs, or CTA pairs.  Persistent: at most one per SM (pair
     // of SMs); one work item per unit otherwise.
-    int64_t units = cfg.persistent ? max_units : work;
+    int64_t units = cfg.persistent ? (mc ? max_units_mc : max_units) : work;
     if (cfg.grid > 0) {
-        const int64_t cap = V::kPair ? (cfg.grid + 1) / 2 : cfg.grid;
+        const int64_t per_unit = V::kPair ? (mc ? 4 : 2) : 1;
+        const int64_t cap = (cfg.grid + per_unit - 1) / per_unit;
         if (cap < units) units = cap;
     }
     if (units > work) units = work;
@@ -520,21 +549,22 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
 
     char plan[360];
     snprintf(plan, sizeof plan,
-             "kernel=%s pair=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
+             "kernel=%s pair=%d mc=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
              "k_blocks=%d splits=%d group=%d zigzag=%d "
              "d_store=%s r_load=%s z_store=%s",
-             pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : "linear", V::kPair ? 1 : 0, V::kEpi, prm.pingpong,
+             pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : "linear", V::kPair ? 1 : 0, prm.mc, V::kEpi,
+             prm.pingpong,
              V::kTileM, bn, gb::kBK,
              prm.stages,
              prm.d_boxes, prm.r_boxes,
-             static_cast<long long>(units * (V::kPair ? 2 : 1)), prm.num_tiles, prm.num_k_blocks, splits,
+             static_cast<long long>(units * (V::kPair ? (mc ? 4 : 2) : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, d_tma ? "tma" : "st.transposed",
              pr.r ? (r_tma ? "tma" : (flags & gb::kFlagRVec) ? "ld.v4" : "ld.transposed") : "none",
              pr.z ? (z_tma ? "tma" : "st.transposed") : "none");
     t_plan = plan;
     {
         std::lock_guard<std::mutex> lk(g_cfg_mu);
-        const size_t need = static_cast<size_t>(units) * (V::kPair ? 2 : 1) * gb::kTraceWords * 8;
+        const size_t need = static_cast<size_t>(units) * (V::kPair ? (mc ? 4 : 2) : 1) * gb::kTraceWords * 8;
         prm.trace = (g_trace && g_trace_bytes >= need) ? g_trace : nullptr;
     }
     if (ws_needed) {  // counters and accumulators start at zero
@@ -658,16 +688,32 @@ gb_status_t splitk_bytes_for(const Problem& pr, int splits, size_t* bytes) {
 
 // ---------------------------------------------------------------- tensor-core rate probe
 
-template <int CG, int N>
-gb_status_t probe_run(int units, int num_mma, int alternate, cudaStream_t stream) {
-    auto kern = gb::mma_rate_kernel<CG, N>;
+// The probe's TMA-writer modes read g_probe_src as bf16 [8192 rows][64 columns] in
+// 128-row boxes (128-byte swizzle); other modes get an unused, zeroed map.
+gb_status_t probe_source_map(CUtensorMap* out) {
+    void* src = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&src, gb::g_probe_src);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(probe source)");
+    return make_tmap(out, src, 64, gb::kProbeSrcBytes / 128, 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int CG, int N, int MODE>
+gb_status_t probe_launch(int units, int num_mma, int alternate, int alu, cudaStream_t stream) {
+    CUtensorMap tmap;
+    memset(&tmap, 0, sizeof tmap);
+    if (MODE == gb::kProbeStagesTma || MODE == gb::kProbeStagesTma2 || MODE == gb::kProbeTmaStore ||
+        MODE == gb::kProbePipeline) {
+        gb_status_t st = probe_source_map(&tmap);
+        if (st != GB_OK) return st;
+    }
+    auto kern = gb::mma_rate_kernel<CG, N, MODE>;
     const int smem = 200 * 1024;  // one CTA per SM: its 512 TMEM columns are free
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(probe)");
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(units * CG, 1, 1);
-    cfg.blockDim = dim3(128, 1, 1);
+    cfg.blockDim = dim3(MODE == gb::kProbeSmspMath || MODE == gb::kProbeSmspPoll ? 256 : 128, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     if (CG == 2) {
@@ -678,8 +724,87 @@ gb_status_t probe_run(int units, int num_mma, int alternate, cudaStream_t stream
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, kern, num_mma, alternate, static_cast<uint64_t>(1000000000ull));
+    e = cudaLaunchKernelEx(&cfg, kern, num_mma, alternate, static_cast<uint64_t>(1000000000ull), alu, tmap);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(probe)");
+    return GB_OK;
+}
+
+template <int CG, int N>
+gb_status_t probe_run(int mode, int units, int num_mma, int alternate, int alu, cudaStream_t stream) {
+    if constexpr (CG != 2 || N != 256) {  // the issue-path variants exist for the GEMMs' pair shape only
+        if (mode != gb::kProbePlain) return fail(GB_ERR_INVALID_ARG, "probe modes other than 0 need cta_group 2, n 256");
+        return probe_launch<CG, N, gb::kProbePlain>(units, num_mma, alternate, alu, stream);
+    } else {
+    switch (mode) {
+        case gb::kProbePlain: return probe_launch<CG, N, gb::kProbePlain>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeCommit: return probe_launch<CG, N, gb::kProbeCommit>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeWait: return probe_launch<CG, N, gb::kProbeWait>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeFence: return probe_launch<CG, N, gb::kProbeFence>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeWaitFence:
+            return probe_launch<CG, N, gb::kProbeWaitFence>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeGemmStep: return probe_launch<CG, N, gb::kProbeGemmStep>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeAlu: return probe_launch<CG, N, gb::kProbeAlu>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeTmemLd16: return probe_launch<CG, N, gb::kProbeTmemLd16>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeTmemLd32: return probe_launch<CG, N, gb::kProbeTmemLd32>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeTmemLd64: return probe_launch<CG, N, gb::kProbeTmemLd64>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeStages: return probe_launch<CG, N, gb::kProbeStages>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeStagesWrites:
+            return probe_launch<CG, N, gb::kProbeStagesWrites>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeStagesStores:
+            return probe_launch<CG, N, gb::kProbeStagesStores>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeStagesTma: return probe_launch<CG, N, gb::kProbeStagesTma>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeStagesTma2: return probe_launch<CG, N, gb::kProbeStagesTma2>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeFenceProxy: return probe_launch<CG, N, gb::kProbeFenceProxy>(units, num_mma, alternate, alu, stream);
+        case gb::kProbePoll: return probe_launch<CG, N, gb::kProbePoll>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeTmaStore: return probe_launch<CG, N, gb::kProbeTmaStore>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeSmspMath: return probe_launch<CG, N, gb::kProbeSmspMath>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeSmspPoll: return probe_launch<CG, N, gb::kProbeSmspPoll>(units, num_mma, alternate, alu, stream);
+        default: return probe_launch<CG, N, gb::kProbePipeline>(units, num_mma, alternate, alu, stream);
+    }
+    }
+}
+
+// Shared by the two probe entry points: launch, synchronise, median cycles per MMA.
+gb_status_t probe_measure(int cta_group, int n, int mode, int alternate, int alu, int num_mma, int units,
+                          double* cycles_per_mma, double* loads_per_mma = nullptr) {
+    if (cta_group != 1 && cta_group != 2) return fail(GB_ERR_INVALID_ARG, "cta_group must be 1 or 2");
+    if (n != 128 && n != 256) return fail(GB_ERR_INVALID_ARG, "n must be 128 or 256");
+    if (num_mma < 8 || num_mma > 65536 || num_mma % 4) return fail(GB_ERR_INVALID_ARG, "num_mma must be a multiple of 4 in [8, 65536]");
+    if (mode < 0 || mode >= gb::kProbeModes) return fail(GB_ERR_INVALID_ARG, "unknown probe mode %d", mode);
+    if (alu < 0 || alu > 1024) return fail(GB_ERR_INVALID_ARG, "alu must be in [0, 1024]");
+    int dev = 0;
+    DeviceInfo info;
+    gb_status_t st = device_info(&dev, &info);
+    if (st != GB_OK) return st;
+    const int max_units = std::min(gb::kProbeMaxUnits, info.sms / cta_group);
+    if (units < 1 || units > max_units)
+        return fail(GB_ERR_INVALID_ARG, "units must be in [1, %d] (one CTA per SM)", max_units);
+    static const unsigned long long zeros[gb::kProbeMaxUnits] = {};
+    cudaError_t e = cudaMemcpyToSymbol(gb::g_probe_cycles, zeros, sizeof zeros);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(gb::g_probe_loads, zeros, sizeof zeros);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the probe results");
+    cudaStream_t stream = nullptr;
+    if (cta_group == 1)
+        st = n == 128 ? probe_run<1, 128>(mode, units, num_mma, alternate, alu, stream)
+                      : probe_run<1, 256>(mode, units, num_mma, alternate, alu, stream);
+    else
+        st = n == 128 ? probe_run<2, 128>(mode, units, num_mma, alternate, alu, stream)
+                      : probe_run<2, 256>(mode, units, num_mma, alternate, alu, stream);
+    if (st != GB_OK) return st;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize(probe)");
+    unsigned long long cyc[gb::kProbeMaxUnits];
+    if ((e = cudaMemcpyFromSymbol(cyc, gb::g_probe_cycles, sizeof cyc)) != cudaSuccess)
+        return cuda_fail(e, "reading the probe results");
+    std::sort(cyc, cyc + units);
+    if (cyc[0] == 0) return fail(GB_ERR_TIMEOUT, "a probe unit's wait for its MMAs ran out");
+    *cycles_per_mma = static_cast<double>(cyc[units / 2]) / num_mma;
+    if (loads_per_mma) {
+        unsigned long long ld[gb::kProbeMaxUnits];
+        if ((e = cudaMemcpyFromSymbol(ld, gb::g_probe_loads, sizeof ld)) != cudaSuccess)
+            return cuda_fail(e, "reading the probe load counts");
+        std::sort(ld, ld + units);
+        *loads_per_mma = static_cast<double>(ld[units / 2]) / num_mma;
+    }
     return GB_OK;
 }
 
@@ -691,40 +816,23 @@ gb_status_t gb_measure_mma_rate(int cta_group, int n, int alternate, int num_mma
                                 double* flops_per_clk_per_sm, double* cycles_per_mma) {
     t_error.clear();
     if (!flops_per_clk_per_sm || !cycles_per_mma) return fail(GB_ERR_INVALID_ARG, "output pointer is null");
-    if (cta_group != 1 && cta_group != 2) return fail(GB_ERR_INVALID_ARG, "cta_group must be 1 or 2");
-    if (n != 128 && n != 256) return fail(GB_ERR_INVALID_ARG, "n must be 128 or 256");
-    if (num_mma < 8 || num_mma > 65536) return fail(GB_ERR_INVALID_ARG, "num_mma must be in [8, 65536]");
-    int dev = 0;
-    DeviceInfo info;
-    gb_status_t st = device_info(&dev, &info);
+    double per_mma = 0;
+    gb_status_t st = probe_measure(cta_group, n, gb::kProbePlain, alternate ? 1 : 0, 0, num_mma, units, &per_mma);
     if (st != GB_OK) return st;
-    const int max_units = std::min(gb::kProbeMaxUnits, info.sms / cta_group);
-    if (units < 1 || units > max_units)
-        return fail(GB_ERR_INVALID_ARG, "units must be in [1, %d] (one CTA per SM)", max_units);
-    static const unsigned long long zeros[gb::kProbeMaxUnits] = {};
-    cudaError_t e = cudaMemcpyToSymbol(gb::g_probe_cycles, zeros, sizeof zeros);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the probe results");
-    cudaStream_t stream = nullptr;
-    if (cta_group == 1)
-        st = n == 128 ? probe_run<1, 128>(units, num_mma, alternate, stream)
-                      : probe_run<1, 256>(units, num_mma, alternate, stream);
-    else
-        st = n == 128 ? probe_run<2, 128>(units, num_mma, alternate, stream)
-                      : probe_run<2, 256>(units, num_mma, alternate, stream);
-    if (st != GB_OK) return st;
-    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize(probe)");
-    unsigned long long cyc[gb::kProbeMaxUnits];
-    if ((e = cudaMemcpyFromSymbol(cyc, gb::g_probe_cycles, sizeof cyc)) != cudaSuccess)
-        return cuda_fail(e, "reading the probe results");
-    std::sort(cyc, cyc + units);
-    if (cyc[0] == 0) return fail(GB_ERR_TIMEOUT, "a probe unit's wait for its MMAs ran out");
-    const double per_mma = static_cast<double>(cyc[units / 2]) / num_mma;
-    const double flops = 2.0 * 128.0 * cta_group * n * 16.0;
     *cycles_per_mma = per_mma;
-    *flops_per_clk_per_sm = flops / per_mma / cta_group;
+    *flops_per_clk_per_sm = 2.0 * 128.0 * cta_group * n * 16.0 / per_mma / cta_group;
     return GB_OK;
 }
 
+gb_status_t gb_probe_mma_issue(int cta_group, int n, int mode, int alu, int num_mma, int units,
+                               double* cycles_per_mma, double* tmem_loads_per_mma) {
+    t_error.clear();
+    if (!cycles_per_mma) return fail(GB_ERR_INVALID_ARG, "output pointer is null");
+    // mode bit 8: operands of random bf16 values instead of zeros
+    const int noisy = (mode >> 8) & 1;
+    return probe_measure(cta_group, n, mode & 0xff, noisy ? 2 : 0, alu, num_mma, units, cycles_per_mma,
+                         tmem_loads_per_mma);
+}
 
 gb_status_t gb_gemm_linear(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, const void* R,
                            int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
@@ -893,6 +1001,10 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "hint_b" && v >= -1 && v <= 2) c.hint_b = static_cast<int>(v);
             else if (key == "hint_r" && v >= -1 && v <= 2) c.hint_r = static_cast<int>(v);
             else if (key == "hint_d" && v >= -1 && v <= 2) c.hint_d = static_cast<int>(v);
+            else if (key == "mc" && v >= -1 && v <= 1) c.mc = static_cast<int>(v);
+            else if (key == "issue" && v >= -1 && v <= 3) c.issue = static_cast<int>(v);
+            else if (key == "tmem_ld" && (v == 0 || v == 32 || v == 64)) c.tmem_ld = static_cast<int>(v);
+            else if (key == "prod" && v >= 0 && v <= 3) c.prod = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

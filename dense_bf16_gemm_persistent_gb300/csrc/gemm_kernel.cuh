@@ -142,6 +142,22 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     // L2 eviction hints (l2_policy codes: 0 none, 1 evict first, 2 evict last) for the
     // TMA loads of A, of B (W1/W3), of R, and the TMA stores of D and Z.
     uint32_t hint_a, hint_b, hint_r, hint_d;
+    // A multicast between two CTA pairs (4-CTA clusters, CTA-pair variants only): a work
+    // item is one tile-row x 2 tile-columns; pair q of the cluster computes tile-column
+    // 2 * item + q, and each CTA loads half of its A tile and multicasts it to the CTA
+    // of the other pair that needs the same rows (tm_a_half: box {64, 64}).
+    int32_t mc;
+    int32_t sched_n_blocks;  // tile-columns of the work-item grid (num_n_blocks, or half of it with mc)
+    // MMA issue loop: 0 descriptors rebuilt per k-block; 1 lean (descriptors advanced
+    // per stage); 2 lean, and the next stage's wait and fence done while the k-block's
+    // third MMA runs, before its fourth is issued
+    int32_t issue;
+    // TMEM columns per tcgen05.ld on the express path (32, or 64: two chunks per load)
+    int32_t tmem_ld;
+    // producer threads: 1 (warp 0 issues the A and B loads of every stage) or 2 (warp 0
+    // the A loads and the expected byte count, warp 2 the B loads)
+    int32_t prod;
+    CUtensorMap tm_a_half;
     // Timing trace (libraries built with GB_TRACE only): kTraceWords words per CTA.
     unsigned long long* trace;
 };
@@ -174,6 +190,16 @@ enum : int {
     kTrEpStore = 20,       // proxy fence, warp sync, TMA store issue
     kTrEpRIssue = 21,      // issuing the next R box loads
     kTrEpSteps = 22,       // chunk steps
+    // MMA issuer: k-block-to-k-block intervals (cycles between the first MMAs of
+    // consecutive k-blocks of a tile) whose wait did not block, by length:
+    // < 560, 560-700, 700-1000, >= 1000; and their total cycles
+    kTrKbFast = 23,
+    kTrKbMid = 24,
+    kTrKbSlow = 25,
+    kTrKbVerySlow = 26,
+    kTrKbCycUnblocked = 27,
+    kTrKbCycBlocked = 28,  // the same intervals' total where the wait did block
+    kTrMmaWaitCyc = 29,    // MMA issuer: cycles inside every operand wait (try_wait can suspend inside)
 };
 
 // Per-phase cycle counters of the first epilogue warp (GB_TRACE builds).
@@ -182,7 +208,7 @@ enum : int {
 #define GB_TR_ADD(arr, idx, t0)                                        \
     do {                                                               \
         const long long _t1 = clock64();                               \
-        if (arr) arr[(idx) - kTrEpDBox] += static_cast<unsigned long long>(_t1 - (t0)); \
+        if (arr) arr[(idx) - kTrEpDBox] += static_cast<uint32_t>(_t1 - (t0)); \
         t0 = _t1;                                                      \
     } while (0)
 #else
@@ -200,6 +226,7 @@ struct SharedCtl {
     uint64_t drain;
     uint32_t tmem_base;
     volatile int32_t abort;
+    uint32_t trace_ep[8];  // GB_TRACE builds: the first epilogue warp's per-phase cycle counters
 };
 
 // The device status word of this translation unit (see gb_get_device_status).
@@ -250,14 +277,22 @@ __device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, uint64_
 // Persistent tile order: groups of `group_m` tile-rows; inside a group the
 // tile-row index runs fastest; odd groups walk the tile-columns backwards.
 __device__ __forceinline__ void tile_coords(int32_t tile, const GemmParams& p, int32_t& mb, int32_t& nb) {
-    const int32_t per_group = p.group_m * p.num_n_blocks;
+    const int32_t per_group = p.group_m * p.sched_n_blocks;
     const int32_t group = tile / per_group;
     const int32_t first_m = group * p.group_m;
     const int32_t rows = min(p.num_m_blocks - first_m, p.group_m);
     const int32_t local = tile - group * per_group;
     mb = first_m + local % rows;
     nb = local / rows;
-    if (group & 1) nb = p.num_n_blocks - 1 - nb;
+    if (group & 1) nb = p.sched_n_blocks - 1 - nb;
+}
+
+// The tile this CTA computes for work-item tile index `tile`: with A multicast, pair
+// `pairi` of the cluster takes tile-column 2 * item-column + pairi.
+__device__ __forceinline__ void work_tile(int32_t tile, const GemmParams& p, uint32_t pairi, int32_t& mb,
+                                          int32_t& nb) {
+    tile_coords(tile, p, mb, nb);
+    if (p.mc) nb = 2 * nb + static_cast<int32_t>(pairi);
 }
 
 // TMA operand loads and output stores, with an L2 policy when one is set.
@@ -568,7 +603,7 @@ template <int NUM_B>
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32], int32_t m, int32_t row0,
                                              int32_t n0, int lane, uint8_t* dbox, int32_t& dslot,
                                              uint32_t rbox, uint8_t* tbuf_r,
-                                             unsigned long long* tr_ep = nullptr) {
+                                             uint32_t* tr_ep = nullptr) {
     GB_TR_T0(tx);
     const int valid = min(32, p.n - n0);
     if (NUM_B == 1) {
@@ -663,6 +698,77 @@ __device__ __forceinline__ void add_f32x32_cg(float (&v)[32], const float* src) 
     }
 }
 
+// ---------------------------------------------------------------- lean MMA issue
+
+// The stage descriptors of ring slot `slot`: the slot's A tile and, kABytes further,
+// its B tile (K-major, or MN-major boxes of 64 columns).
+__device__ __forceinline__ void stage_descs(uint32_t ring0, uint32_t slot, uint32_t stage_bytes, uint32_t a_bytes,
+                                            bool b_mn, uint64_t& ad, uint64_t& bd) {
+    const uint32_t a_addr = ring0 + slot * stage_bytes;
+    ad = sdesc_kmajor_sw128(a_addr);
+    bd = b_mn ? sdesc_mnmajor_sw128(a_addr + a_bytes, kMnBoxBytes) : sdesc_kmajor_sw128(a_addr + a_bytes);
+}
+
+// One work item's k-blocks on the lean issue path.  The ring position (s, ph) and the
+// k-block counter `it` describe the k-block consumed last (it == 0: none yet), as in
+// the rebuild path, so both paths can follow each other.  Returns false if a wait gave up.
+template <int CG, uint32_t kStageBytes, uint32_t kABytes>
+__device__ __forceinline__ bool issue_tile_lean(const GemmParams& p, uint32_t d_tmem, int32_t nkb, uint64_t* full,
+                                                uint64_t* empty, uint8_t* ring, uint32_t stages, uint32_t& s,
+                                                uint32_t& ph, uint32_t& it, bool b_mn, uint32_t idesc, uint32_t bstep,
+                                                uint16_t empty_mask, volatile int32_t* abort_flag, uint64_t tmo,
+                                                TraceAcc& tr_full, bool& issued) {
+    if (nkb <= 0) return true;
+    const uint32_t ring0 = smem_addr(ring);
+    const uint32_t full0 = smem_addr(full), empty0 = smem_addr(empty);
+    // position of the first k-block of this item
+    uint32_t cs = s, cph = ph;
+    if (it > 0 && ++cs == stages) {
+        cs = 0;
+        cph ^= 1u;
+    }
+    uint64_t ad, bd;
+    stage_descs(ring0, cs, kStageBytes, kABytes, b_mn, ad, bd);
+    if (!wait_bar(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
+    tc_fence_after_sync();
+    const bool lookahead = p.issue == 2;
+    for (int32_t kk = 0; kk < nkb; ++kk) {
+        mma_bf16<CG>(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        mma_bf16<CG>(d_tmem, ad + 2, bd + bstep, idesc, 1u);
+        mma_bf16<CG>(d_tmem, ad + 4, bd + 2 * bstep, idesc, 1u);
+        issued = true;
+        const uint32_t done = cs;
+        const uint64_t ad3 = ad + 6, bd3 = bd + 3 * bstep;
+        const bool more = kk + 1 < nkb;
+        if (more) {  // the next k-block's stage
+            if (++cs == stages) {
+                cs = 0;
+                cph ^= 1u;
+                ad -= static_cast<uint64_t>((stages - 1) * (kStageBytes >> 4));
+                bd -= static_cast<uint64_t>((stages - 1) * (kStageBytes >> 4));
+            } else {
+                ad += kStageBytes >> 4;
+                bd += kStageBytes >> 4;
+            }
+            if (lookahead) {
+                if (!wait_bar(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
+                tc_fence_after_sync();
+            }
+        }
+        mma_bf16<CG>(d_tmem, ad3, bd3, idesc, 1u);
+        if constexpr (CG == 2) mma_commit_multicast2(empty0 + 8 * done, empty_mask);
+        else mma_commit<1>(empty0 + 8 * done);
+        if (more && !lookahead) {
+            if (!wait_bar(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
+            tc_fence_after_sync();
+        }
+    }
+    s = cs;
+    ph = cph;
+    it += static_cast<uint32_t>(nkb);
+    return true;
+}
+
 // ---------------------------------------------------------------- the kernel
 
 // Compile-time shape of one kernel variant.
@@ -736,10 +842,16 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     unsigned long long* trace = p.trace ? p.trace + static_cast<size_t>(blockIdx.x) * kTraceWords : nullptr;
     if (trace && threadIdx.x == 0) trace[kTrStartNs] = global_timer_ns();
 #endif
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // position in the CTA pair
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;  // position in the cluster (pair, or two pairs)
+    const uint32_t rank = crank & 1u;                      // position in the CTA pair
+    const uint32_t pairi = crank >> 1;                     // which pair of the cluster (A multicast)
+    const uint32_t lead = crank & ~1u;                     // cluster rank of this pair's leader
     const bool leader = rank == 0;
-    const int32_t unit = PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
-    const int32_t units = PAIR ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
+    const bool mc = PAIR && p.mc != 0;
+    const int32_t cta_per_unit = PAIR ? (mc ? 4 : 2) : 1;
+    const int32_t unit = static_cast<int32_t>(blockIdx.x) / cta_per_unit;
+    const int32_t units = static_cast<int32_t>(gridDim.x) / cta_per_unit;
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);  // both CTAs of this pair
     const int32_t num_work = p.num_tiles * p.splits;
     // ping-pong takes effect with two epilogue warpgroups and no split only
     const bool pingpong = kEpiGroups == 2 && p.pingpong != 0 && p.splits == 1;
@@ -747,7 +859,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), 1);
+            // with A multicast a stage is free once both pairs' MMAs have read it
+            mbar_init(smem_addr(&empty[s]), mc ? 2 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&ctl->acc_full[b]), 1);
@@ -763,7 +876,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     }
     if (warp == 0 && lane == 0) {
         if (p.num_k_blocks > 0) {
-            tma_prefetch_desc(&p.tm_a);
+            tma_prefetch_desc(mc ? &p.tm_a_half : &p.tm_a);
             tma_prefetch_desc(&p.tm_b0);
             if (NUM_B == 2) tma_prefetch_desc(&p.tm_b1);
         }
@@ -789,8 +902,15 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     // epilogue the large one; only the short teardown after the branches is shared.
     if (warp < kEpiWarp0) {
         if constexpr (W::kRealloc) setmaxnreg_dec<W::kRegsControl>();
-        if (warp == 0) {
+        if (warp == 0 || (warp == 2 && p.prod >= 2) || (warp == 3 && p.prod == 3)) {
             // ------------------------------------------------------------ producer (every CTA)
+            // One thread issues every stage's loads, or two split them: warp 0 the A tile (and
+            // the leader's expected byte count), warp 2 the B tile.  Both wait for the stage
+            // to be free; the full barrier completes when all of the stage's bytes have landed.
+            // prod == 3: warps 0 and 2 load the upper and lower halves of the A tile, warp 3 B
+            const bool split_a = p.prod == 3 && !mc;
+            const bool do_a = warp == 0 || (split_a && warp == 2);
+            const bool do_b = p.prod == 1 || (p.prod == 2 && warp == 2) || (p.prod == 3 && warp == 3);
             if (lane == 0) {
                 uint32_t it = 0;
                 uint32_t s = 0, ph = 0;  // ring slot and phase of k-block `it`
@@ -804,7 +924,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
                     const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
                     int32_t mb, nb;
-                    tile_coords(tile, p, mb, nb);
+                    work_tile(tile, p, pairi, mb, nb);
                     const bool reverse = p.zigzag && (local & 1);
                     const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
                     const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
@@ -820,47 +940,80 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             ok = false;
                             break;
                         }
-                        if (p.inject == kInjectSkipFirstStage && it == 0 && leader) continue;  // test hook
+                        if (p.inject == kInjectSkipFirstStage && it == 0 && leader && warp == 0) continue;  // test hook
                         uint8_t* st = ring + s * S::kStageBytes;
                         const uint32_t own_full = smem_addr(&full[s]);
-                        if (leader) mbar_arrive_expect_tx(own_full, S::kTxBytes);
+                        if (leader && warp == 0) mbar_arrive_expect_tx(own_full, S::kTxBytes);
                         uint8_t* sb = st + S::kABytes;
+                        if (mc && do_a) {
+                            // A multicast: this CTA loads rows [pairi * 64, +64) of its 128-row A
+                            // tile into that offset of its own and the other pair's same-rank CTA
+                            const uint32_t fb = mapa_shared(own_full, lead);
+                            tma_load_2d_pair_multicast(smem_addr(st + pairi * (S::kABytes / 2)), &p.tm_a_half, fb,
+                                                       kb * kBK, a_row + static_cast<int32_t>(pairi) * (kBM / 2),
+                                                       static_cast<uint16_t>((1u << rank) | (1u << (2 + rank))));
+                        }
                         if (NUM_B == 1 && (p.flags & kFlagBMn)) {
                             // MN-major B (a row-major [K, N] matrix): boxes of 64 output columns
                             // x 64 contraction rows, one after the other along N
-                            const uint32_t fb = PAIR ? mapa_shared(own_full, 0) : own_full;
-                            tma_load_op<PAIR>(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row, pol_a);
+                            const uint32_t fb = PAIR ? mapa_shared(own_full, lead) : own_full;
+                            if (split_a && do_a) {
+                                const int32_t half = warp == 0 ? 0 : 1;
+                                tma_load_op<PAIR>(smem_addr(st + half * (S::kABytes / 2)), &p.tm_a_half, fb, kb * kBK,
+                                                  a_row + half * (kBM / 2), pol_a);
+                            } else if (!mc && do_a) {
+                                tma_load_op<PAIR>(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row, pol_a);
+                            }
+                            if (do_b) {
 #pragma unroll
-                            for (int h = 0; h < S::kBRows / 64; ++h)
-                                tma_load_op<PAIR>(smem_addr(sb + h * kMnBoxBytes), &p.tm_b0, fb, b_row + h * 64,
-                                                  kb * kBK, pol_b);
+                                for (int h = 0; h < S::kBRows / 64; ++h)
+                                    tma_load_op<PAIR>(smem_addr(sb + h * kMnBoxBytes), &p.tm_b0, fb, b_row + h * 64,
+                                                      kb * kBK, pol_b);
+                            }
                         } else if constexpr (PAIR) {
-                            const uint32_t fb = mapa_shared(own_full, 0);  // the leader's full barrier
-                            tma_load_op<true>(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row, pol_a);
-                            if (NUM_B == 1)
-                                tma_load_op<true>(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row, pol_b);
-                            else  // this CTA's half of the N = 2 BN operand is one whole product
-                                tma_load_op<true>(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK, nb * BN,
-                                                  pol_b);
+                            const uint32_t fb = mapa_shared(own_full, lead);  // the pair leader's full barrier
+                            if (split_a && do_a) {  // this warp's 64-row half of the A tile
+                                const int32_t half = warp == 0 ? 0 : 1;
+                                tma_load_op<true>(smem_addr(st + half * (S::kABytes / 2)), &p.tm_a_half, fb, kb * kBK,
+                                                  a_row + half * (kBM / 2), pol_a);
+                            } else if (!mc && do_a) {
+                                tma_load_op<true>(smem_addr(st), &p.tm_a, fb, kb * kBK, a_row, pol_a);
+                            }
+                            if (do_b) {
+                                if (NUM_B == 1)
+                                    tma_load_op<true>(smem_addr(sb), &p.tm_b0, fb, kb * kBK, b_row, pol_b);
+                                else  // this CTA's half of the N = 2 BN operand is one whole product
+                                    tma_load_op<true>(smem_addr(sb), leader ? &p.tm_b0 : &p.tm_b1, fb, kb * kBK,
+                                                      nb * BN, pol_b);
+                            }
                         } else {
-                            tma_load_op<false>(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row, pol_a);
-                            tma_load_op<false>(smem_addr(sb), &p.tm_b0, own_full, kb * kBK,
-                                               NUM_B == 1 ? b_row : nb * BN, pol_b);
-                            if (NUM_B == 2)
-                                tma_load_op<false>(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK, nb * BN,
-                                                   pol_b);
+                            if (split_a && do_a) {
+                                const int32_t half = warp == 0 ? 0 : 1;
+                                tma_load_op<false>(smem_addr(st + half * (S::kABytes / 2)), &p.tm_a_half, own_full,
+                                                   kb * kBK, a_row + half * (kBM / 2), pol_a);
+                            } else if (do_a) {
+                                tma_load_op<false>(smem_addr(st), &p.tm_a, own_full, kb * kBK, a_row, pol_a);
+                            }
+                            if (do_b) {
+                                tma_load_op<false>(smem_addr(sb), &p.tm_b0, own_full, kb * kBK,
+                                                   NUM_B == 1 ? b_row : nb * BN, pol_b);
+                                if (NUM_B == 2)
+                                    tma_load_op<false>(smem_addr(sb + BN * kBK * 2), &p.tm_b1, own_full, kb * kBK,
+                                                       nb * BN, pol_b);
+                            }
                         }
                     }
                 }
 #ifdef GB_TRACE
-                if (trace) {
+                if (trace && warp == 0) {
                     trace[kTrProdEmptyCyc] = tr_empty.cyc;
                     trace[kTrProdEmptyN] = tr_empty.n;
                 }
 #endif
                 if (!ok && leader) {
-                    // Drain: the leader's full barriers count the bytes of both CTAs; wait
-                    // (bounded) for the loads of the last `stages` k-blocks to land.
+                    // Drain: the leader's full barriers count the bytes of both CTAs (and of
+                    // both producer threads); wait (bounded) for the k-blocks this thread
+                    // issued among the last `stages` to land.
                     const uint32_t first = it > stages ? it - stages : 0u;
                     for (uint32_t i = first; i < it; ++i) {
                         if (p.inject == kInjectSkipFirstStage && i == 0) continue;
@@ -878,6 +1031,10 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 bool issued = false;
                 int32_t local = 0;
                 TraceAcc tr_full, tr_acc;
+#ifdef GB_TRACE
+                unsigned long long kb_hist[7] = {0, 0, 0, 0, 0, 0, 0};  // [6]: cycles inside every full wait
+                long long kb_prev = 0;
+#endif
                 const bool b_mn = NUM_B == 1 && (p.flags & kFlagBMn);
                 const uint32_t idesc = S::kIdesc | (b_mn ? kIdescBMnMajor : 0u);
                 const uint32_t bstep = b_mn ? (16u * 128u) >> 4 : 2u;
@@ -898,36 +1055,77 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + b * kAccStride;
+                    if (p.issue == 1 || p.issue == 2) {
+                        // Lean issue: the stage's descriptors advance with the ring position
+                        // (no per-k-block rebuild), and with issue == 2 the next stage's wait and
+                        // fence run while this k-block's third MMA executes.
+                        if (!issue_tile_lean<CG, S::kStageBytes, S::kABytes>(
+                                p, d_tmem, nkb, full, empty, ring, stages, s, ph, it, b_mn, idesc, bstep,
+                                mc ? static_cast<uint16_t>(0xF) : pair_mask, abort_flag, tmo, tr_full, issued)) {
+                            ok = false;
+                            break;
+                        }
+                        if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), pair_mask);
+                        else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
+                        continue;
+                    }
                     for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
                         if (it > 0 && ++s == stages) {
                             s = 0;
                             ph ^= 1u;
                         }
+#ifdef GB_TRACE
+                        const unsigned long long blocked_before = tr_full.n;
+                        const long long wait_c0 = clock64();
+#endif
                         if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s, &tr_full)) {
                             ok = false;
                             break;
                         }
+#ifdef GB_TRACE
+                        kb_hist[6] += static_cast<unsigned long long>(clock64() - wait_c0);
+#endif
                         tc_fence_after_sync();
 #ifdef GB_TRACE
                         if (trace && !issued) trace[kTrMmaFirstNs] = global_timer_ns();
+                        {
+                            const long long now = clock64();
+                            if (kk > 0) {
+                                const long long d = now - kb_prev;
+                                if (tr_full.n != blocked_before) {
+                                    kb_hist[5] += static_cast<unsigned long long>(d);
+                                } else {
+                                    kb_hist[d < 560 ? 0 : d < 700 ? 1 : d < 1000 ? 2 : 3] += 1;
+                                    kb_hist[4] += static_cast<unsigned long long>(d);
+                                }
+                            }
+                            kb_prev = now;
+                        }
 #endif
                         const uint32_t a_addr = smem_addr(ring + s * S::kStageBytes);
                         const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
                         const uint64_t bdesc = b_mn ? sdesc_mnmajor_sw128(a_addr + S::kABytes, kMnBoxBytes)
                                                     : sdesc_kmajor_sw128(a_addr + S::kABytes);
-    #pragma unroll
-                        for (int j = 0; j < kBK / 16; ++j) {
-                            // per 16-element K slice: +32 bytes in a K-major tile, +16 rows of 128 bytes
-                            // in an MN-major one (+2 / +128 in the >>4-encoded address)
-                            const uint32_t acc = (kk > 0 || j > 0) ? 1u : 0u;
-                            mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + bstep * j, idesc, acc);
+                        // per 16-element K slice: +32 bytes in a K-major tile, +16 rows of 128 bytes
+                        // in an MN-major one (+2 / +128 in the >>4-encoded address); the four MMAs
+                        // leave one asm block back to back
+                        if (p.issue == 3) {  // the MMAs as four separate statements (comparison)
+#pragma unroll
+                            for (int j = 0; j < kBK / 16; ++j)
+                                mma_bf16<CG>(d_tmem, adesc + 2 * j, bdesc + bstep * j, idesc, (kk > 0 || j > 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t bdesc1 = bdesc + bstep, bdesc2 = bdesc1 + bstep, bdesc3 = bdesc2 + bstep;
+                            mma_bf16_x4<CG>(d_tmem, adesc, adesc + 2, adesc + 4, adesc + 6, bdesc, bdesc1, bdesc2,
+                                            bdesc3, idesc, kk > 0 ? 1u : 0u);
                         }
                         issued = true;
-                        if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
+                        // the stage is free in this pair (and, with A multicast, in the other pair's
+                        // view too: its producers write A halves into this pair's stage)
+                        if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), mc ? 0xF : pair_mask);
                         else mma_commit<1>(smem_addr(&empty[s]));
                     }
                     if (!ok) break;
-                    if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), 0x3);
+                    if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), pair_mask);
                     else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
                 }
 #ifdef GB_TRACE
@@ -939,6 +1137,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     trace[kTrMmaAccCyc] = tr_acc.cyc;
                     trace[kTrMmaAccN] = tr_acc.n;
                     trace[kTrMmaItems] = static_cast<unsigned long long>(local);
+                    for (int i = 0; i < 7; ++i) trace[kTrKbFast + i] = kb_hist[i];
                 }
 #endif
                 if (!ok && issued) {
@@ -970,7 +1169,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         TraceAcc tr_accfull;
 #ifdef GB_TRACE
         unsigned long long tr_body = 0;
-        unsigned long long tr_ep[7] = {0, 0, 0, 0, 0, 0, 0};
+        // per-phase counters in shared memory (no registers held across the loops); only the
+        // first epilogue warp's lane 0 counts
+        uint32_t* tr_ep = (e == 0 && lane == 0) ? ctl->trace_ep : nullptr;
+        if (tr_ep)
+            for (int i = 0; i < 8; ++i) tr_ep[i] = 0;
 #endif
 
         // R by TMA (linear, no split): a cursor over this warp's future (tile, chunk)
@@ -998,7 +1201,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     ++rc_local;
                     continue;
                 }
-                if (rc_mb < 0) tile_coords(rc_w, p, rc_mb, rc_nb);
+                if (rc_mb < 0) work_tile(rc_w, p, pairi, rc_mb, rc_nb);
                 const int32_t r0 = rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;
                 if (rc_c < kChunks && r0 < p.m && rc_nb * BN + rc_c * kDChunk < p.n) return true;
                 rc_c += cstep;
@@ -1053,7 +1256,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 
             const int32_t tile = w / p.splits;
             int32_t mb, nb;
-            tile_coords(tile, p, mb, nb);
+            work_tile(tile, p, pairi, mb, nb);
             const int32_t row0 = mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;  // this warp's slab
             const int32_t m = row0 + lane;
             const bool warp_rows = row0 < p.m;
@@ -1087,7 +1290,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) {
-                            if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), 0));
+                            if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
                             else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                         }
                     }
@@ -1135,7 +1338,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     if (++dslot == p.d_boxes) dslot = 0;
                     GB_TR_ADD(tr_ep, kTrEpStore, tx);
 #ifdef GB_TRACE
-                    tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+                    if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
                 }
                 continue;
@@ -1161,7 +1364,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         }
                         GB_TR_ADD(tr_ep, kTrEpDBox, tx);
 #ifdef GB_TRACE
-                        tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+                        if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
                         uint32_t box_a = 0;
 #pragma unroll 1
@@ -1181,7 +1384,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                 tc_fence_before_sync();
                                 __syncwarp();
                                 if (lane == 0) {
-                                    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), 0));
+                                    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
                                     else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                                 }
                             }
@@ -1267,7 +1470,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 float v[32];
                 GB_TR_T0(tg);
 #ifdef GB_TRACE
-                tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+                if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
                 if (chunk_on && p.num_k_blocks > 0) {
                     uint32_t r0[32];
@@ -1303,7 +1506,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
-                        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), 0));
+                        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
                         else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                     }
                 }

@@ -318,10 +318,40 @@ GB_API gb_status_t gb_set_trace_buffer(void* buf, size_t bytes);
  * the cycles per MMA and the dense bf16 rate per SM and clock it implies
  * (2 M N 16 / cycles / cta_group).  The nominal peak of the GPU is then
  * SMs x clock x that rate.  Runs on the legacy default stream and synchronises
- * the device.  num_mma in [8, 65536]; units in [1, SMs / cta_group].
+ * the device.  num_mma a multiple of 4 in [8, 65536]; units in [1, SMs / cta_group].
  */
 GB_API gb_status_t gb_measure_mma_rate(int cta_group, int n, int alternate, int num_mma, int units,
                                        double* flops_per_clk_per_sm, double* cycles_per_mma);
+
+/*
+ * The same probe with the issuing thread's steps around the MMAs (what those steps
+ * cost the tensor pipe): mode 0 the MMAs alone; per four MMAs (one 64-wide
+ * k-block) 1 a tcgen05.commit, 2 an already-satisfied mbarrier wait, 3 a
+ * tcgen05.fence::after_thread_sync, 4 wait and fence, 5 wait, fence, descriptors
+ * rebuilt from a stage index and a commit (the GEMM issuer's step); 6 `alu`
+ * dependent integer operations after every MMA; 7, 8, 9 the MMAs alone while
+ * warps 1-3 of every CTA read the other TMEM accumulator in a loop with
+ * tcgen05.ld.32x32b of 16, 32 or 64 columns (an epilogue's TMEM reads); 10 the
+ * MMAs reading six distinct 32 KiB operand stages in turn (an operand ring); 11
+ * four stages while warp 1 keeps four 16 KiB bulk copies from global into other
+ * shared memory in flight (a ring's fills); 12 four stages while warps 1-3 store
+ * 16-byte vectors to other shared memory as fast as they can; 13 four stages
+ * while warp 1 keeps four 16 KiB 2-D TMA tile loads (128-byte swizzle) into other
+ * shared memory in flight, 14 the same from warps 1 and 2; 15-17 an epilogue's
+ * steps in warps 1-3 beside the MMAs: 15 shared-memory stores then
+ * fence.proxy.async and a warp sync, 16 polling an mbarrier that never completes,
+ * 17 (warp 1) 2-D TMA stores of shared memory; 18, 19 with 256 threads, warps 4-7
+ * (one on each SM sub-partition, warp 4 beside the issuing thread) running FMA
+ * math (18) or polling an mbarrier that never completes (19); 20 a GEMM mainloop
+ * without epilogue (TMA into a 6-stage ring, full/empty barriers, two producer
+ * threads, the MMAs of each stage, a commit per stage).  Writes the median
+ * cycles per MMA and, when tmem_loads_per_mma is not NULL, the TMEM loads (modes
+ * 7-9), 16 KiB copies (modes 11, 13, 14) or warp-wide 16-byte stores (mode 12) the leader
+ * CTA completed per MMA (0 otherwise).  mode | 256: the operand tiles hold random
+ * bf16 values instead of zeros.
+ */
+GB_API gb_status_t gb_probe_mma_issue(int cta_group, int n, int mode, int alu, int num_mma, int units,
+                                      double* cycles_per_mma, double* tmem_loads_per_mma);
 
 /* Library version as "major.minor.patch". */
 GB_API const char* gb_version(void);

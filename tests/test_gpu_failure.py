@@ -14,16 +14,21 @@ from tests.gpu_util import assert_close, bits
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("extra", ["", "prod=2", "prod=3", "mc=1", "mc=1,prod=2"])
 @pytest.mark.parametrize("epi", [1, 2])
 @pytest.mark.parametrize("kind", ["linear", "ffn"])
 @pytest.mark.parametrize("pair", [0, 1])
-def test_wait_timeout_is_reported_and_context_survives(kind, pair, epi):
+def test_wait_timeout_is_reported_and_context_survives(kind, pair, epi, extra):
+    """Also with two producer threads (A and B loads from different warps) and with the
+    A tile multicast between two CTA pairs: every role still drains and returns."""
+    if "mc=1" in extra and not pair:
+        pytest.skip("A multicast is a CTA-pair schedule")
     M, N, K = 512, 768, 1024
     A = inputs.randn_bf16((M, K), seed=1).cuda()
     B = inputs.randn_bf16((N, K), seed=2, std=1.0 / np.sqrt(K)).cuda()
     B3 = inputs.randn_bf16((N, K), seed=3, std=1.0 / np.sqrt(K)).cuda()
     gb.device_status()
-    gb.set_config(f"pair={pair},epi={epi}")
+    gb.set_config(f"pair={pair},epi={epi}" + (f",{extra}" if extra else ""))
     gb.set_wait_timeout_ns(100_000_000)  # 0.1 s
     gb.set_fault_injection(1)
     try:

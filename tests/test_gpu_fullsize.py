@@ -140,3 +140,17 @@ def test_bench_configuration_is_the_default():
     gb.linear(w["A"], w["B"], w["bias"], None, act="gelu_tanh")
     plan = gb.last_plan()
     assert "kernel=linear pair=1" in plan and "tile=256x256x64" in plan and "d_store=tma" in plan, plan
+
+
+@pytest.mark.parametrize("spec", ["mc=1,issue=2", "issue=2", "prod=2", "prod=2,mc=1"])
+def test_mlp_schedules_identical_bits_full_size(spec):
+    """The whole 8192x14336 MLP output under the multicast and issue-loop schedules equals
+    the default schedule's bit for bit (the per-element sum order is the same)."""
+    w = inputs.mlp_gelu(device=DEV)
+    D0 = gb.linear(w["A"], w["B"], w["bias"], None, act="gelu_tanh")
+    gb.device_status()
+    gb.set_config(spec)
+    D1 = gb.linear(w["A"], w["B"], w["bias"], None, act="gelu_tanh")
+    gb.device_status()
+    gb.set_config(None)
+    assert torch.equal(D0.view(torch.int16), D1.view(torch.int16)), spec

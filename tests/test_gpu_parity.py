@@ -234,7 +234,12 @@ def test_ffn_integer_bit_exact_when_gate_is_relu_like():
                                   "stages=4,pair=0", "stages=16", "epi=1", "epi=2", "epi=1,pair=0,grid=3",
                                   "epi=2,pair=1,grid=2,stages=3", "boxes=2", "boxes=8,grid=3",
                                   "boxes=5,stages=6", "boxes=3,epi=1,pair=0", "pingpong=1", "pingpong=1,grid=3",
-                                  "pingpong=1,pair=0,grid=2"])
+                                  "pingpong=1,pair=0,grid=2", "issue=1", "issue=2", "issue=2,pair=0",
+                                  "issue=2,stages=2", "issue=1,zigzag=1", "mc=1", "mc=1,issue=2",
+                                  "mc=1,grid=4", "mc=1,epi=2,issue=1", "hint_a=2,hint_b=1,hint_d=1,hint_r=1",
+                                  "prod=2", "prod=2,pair=0", "prod=2,epi=2,stages=2", "prod=2,mc=1",
+                                  "prod=2,issue=2,grid=3", "prod=3", "prod=3,pair=0", "prod=3,epi=2",
+                                  "issue=3"])
 def test_config_overrides_give_identical_bits(spec):
     """Tile size, grid, swizzle and persistence change which CTA computes a tile but not
     the per-element accumulation order within the tile: identical bits."""
@@ -510,3 +515,27 @@ def test_preact_integer_exact_and_k_zero():
                               torch.empty((N, 0), dtype=torch.bfloat16, device=DEV), bias.to(DEV), act="gelu_tanh")
     gb.device_status()
     assert torch.equal(Z0.view(torch.int16), bias.to(DEV).view(torch.int16)[None, :].expand(M, N))
+
+
+@pytest.mark.parametrize("spec", ["mc=1", "mc=1,issue=2", "issue=2", "prod=2", "prod=2,mc=1", "prod=3"])
+def test_schedules_identical_bits_on_ragged_shapes(spec):
+    """A multicast between CTA pairs and the issue loops on shapes with an odd number of
+    tile-columns (a multicast partner tile past N), ragged M, an epilogue input and the FFN."""
+    for M, N, K in [(700, 900, 520), (513, 1300, 200), (300, 257, 64)]:
+        A = inputs.randn_bf16((M, K), seed=M + 1)
+        B = inputs.randn_bf16((N, K), seed=N + 2, std=0.1)
+        bias = inputs.randn_bf16((N,), seed=3, std=0.1)
+        R = inputs.randn_bf16((M, N), seed=4)
+        base = run_linear(A, B, bias, R, "silu")
+        gb.set_config(spec)
+        got = run_linear(A, B, bias, R, "silu")
+        assert ("mc=1" in gb.last_plan()) == ("mc=1" in spec), gb.last_plan()
+        gb.set_config(None)
+        assert_bitexact(got, base, f"{spec} {M}x{N}x{K}")
+        X, W1, W3 = A, B, inputs.randn_bf16((N, K), seed=N + 5, std=0.1)
+        d0 = bits(gb.ffn_gated(X.to(DEV), W1.to(DEV), W3.to(DEV)))
+        gb.set_config(spec)
+        d1 = bits(gb.ffn_gated(X.to(DEV), W1.to(DEV), W3.to(DEV)))
+        gb.device_status()
+        gb.set_config(None)
+        assert_bitexact(d1, d0, f"ffn {spec} {M}x{N}x{K}")
