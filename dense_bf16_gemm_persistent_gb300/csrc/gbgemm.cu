@@ -64,6 +64,9 @@ struct Config {
     int issue = -1;      // MMA issue loop: -1 auto, 0 rebuild, 1 lean, 2 lean with look-ahead wait
     int tmem_ld = 0;     // TMEM columns per load on the express path: 0 auto, 32 or 64
     int prod = 0;        // producer threads: 0 auto, 1 or 2 (A and B loads issued by different warps)
+    int r_async = -1;    // unaligned R rows (no split): -1 auto, 0 synchronous loads at use, 1 cp.async queue
+    int r_boxes = 0;     // R queue depth per epilogue warp: 0 = heuristic, 2..8
+    int wide = -1;       // 32x64 R/D boxes on the paired epilogue path: -1 auto, 0 off, 1 on
 };
 
 std::mutex g_cfg_mu;
@@ -195,6 +198,7 @@ template <int BN, int NUM_B, int STAGES, bool PAIR, int EPI>
 struct Variant {
     using S = gb::KernelShape<BN, NUM_B, STAGES, PAIR, EPI>;
     static constexpr int kEpi = EPI;
+    static constexpr int kBN = BN;
     static constexpr int kStages = STAGES;
     static constexpr bool kPair = PAIR;
     static constexpr int kTileM = S::kTileM;
@@ -256,18 +260,41 @@ struct Variant {
     // bound by the epilogue's global traffic, so they take a 3-stage ring and spend
     // the rest on deeper D/R queues (more bytes in flight per SM).  `r_mode`: 0 no
     // R boxes, 1 two boxes as the transpose buffer of unaligned R rows, 2 a queue
-    // of R boxes loaded by TMA.  Boxes shrink first, then the ring, down to 2 each.
+    // of R boxes loaded by TMA, 3 a queue of cp.async slots for unaligned R rows
+    // (3 deep by default: a long-K tile's next chunks all land during its MMAs).
+    // Boxes shrink first, then the ring, down to 2 each.
     struct Layout {
         int stages, d_boxes, r_boxes;
     };
-    static Layout choose_layout(int kb_per_item, int r_mode, const Config& cfg, size_t smem_optin) {
+    // Bytes of one R / D queue entry for a launch's flags.
+    static uint32_t r_slot_bytes(uint32_t flags) {
+        return (flags & gb::kFlagRAsync) ? gb::kRSlotAsyncBytes : (flags & gb::kFlagWide) ? gb::kWideBoxBytes
+                                                                                          : gb::kDStageBytes;
+    }
+    static uint32_t d_slot_bytes(uint32_t flags) {
+        return (flags & gb::kFlagWide) ? gb::kWideBoxBytes : gb::kDStageBytes;
+    }
+    static Layout choose_layout(int kb_per_item, int r_mode, uint32_t flags, const Config& cfg, size_t smem_optin) {
         const bool short_k = kb_per_item <= 4;
         int st = cfg.stages > 0 ? std::min(cfg.stages, STAGES) : (short_k ? std::min(3, STAGES) : STAGES);
         st = std::max(2, st);
         int boxes = cfg.boxes > 0 ? cfg.boxes : (short_k ? gb::kMaxBoxes : 2);
-        auto r_of = [&](int b) { return r_mode == 2 ? b : (r_mode == 1 ? 2 : 0); };
-        while (boxes > 2 && S::smem_bytes(st, boxes, r_of(boxes)) > smem_optin) --boxes;
-        while (st > 2 && S::smem_bytes(st, boxes, r_of(boxes)) > smem_optin) --st;
+        int rq = cfg.r_boxes > 0 ? cfg.r_boxes : (short_k ? gb::kMaxBoxes : 3);
+        auto r_of = [&](int b) { return r_mode == 2 ? (cfg.r_boxes > 0 ? rq : b) : r_mode == 3 ? rq : (r_mode == 1 ? 2 : 0); };
+        const uint32_t rs = r_slot_bytes(flags), ds = d_slot_bytes(flags);
+        if (short_k && (flags & gb::kFlagWide) && cfg.stages <= 0 && cfg.boxes <= 0 && cfg.r_boxes <= 0) {
+            // Wide boxes on items of 1-4 k-blocks: a 2-stage ring is enough (the MMAs are a
+            // few percent of the time) and the room goes to R boxes in flight, whose loads
+            // gate every step (measured on GB300, K = 64 residual: 2 stages + 2 D + 3 R
+            // boxes 3 % faster than 3 stages + 2 + 2).
+            int r = gb::kMaxBoxes;
+            while (r > 2 && S::smem_bytes(2, 2, r, rs, ds) > smem_optin) --r;
+            return Layout{2, 2, r};
+        }
+        while (r_mode == 3 && rq > 2 && S::smem_bytes(2, 2, rq, rs, ds) > smem_optin) --rq;
+        while (boxes > 2 && S::smem_bytes(st, boxes, r_of(boxes), rs, ds) > smem_optin) --boxes;
+        while (st > 2 && S::smem_bytes(st, boxes, r_of(boxes), rs, ds) > smem_optin) --st;
+        while (rq > 2 && S::smem_bytes(st, boxes, r_of(boxes), rs, ds) > smem_optin) --rq;
         return Layout{st, boxes, r_of(boxes)};
     }
 
@@ -277,7 +304,7 @@ struct Variant {
         cudaLaunchAttribute attr[1];
         cfg.gridDim = dim3(units * S::kCG * (p.mc ? 2 : 1), 1, 1);
         cfg.blockDim = dim3(S::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = S::smem_bytes(p.stages, p.d_boxes, p.r_boxes);
+        cfg.dynamicSmemBytes = S::smem_bytes(p.stages, p.d_boxes, p.r_boxes, r_slot_bytes(p.flags));
         cfg.stream = stream;
         if (PAIR) {
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -297,6 +324,7 @@ struct Variant {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -489,17 +517,36 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     if (d_tma) flags |= gb::kFlagDTma;
     const bool r_tma = !pr.ffn && pr.r && aligned16(pr.r) && pr.ldr % 8 == 0 && splits == 1;
     if (r_tma) flags |= gb::kFlagRTma;
+    // Unaligned R rows: cp.async word copies need a 4-byte aligned base (a segment's
+    // first word may then start one element early, still inside the tensor).  Off by
+    // default: measured on GB300 (N = 4099 residual shapes) the prefetch queue hides the
+    // R loads, but the shared memory it takes costs one operand stage, and the launches
+    // came out 0.5-2.5 % slower than synchronous loads at use.
+    const bool r_async = !pr.ffn && pr.r && !(flags & gb::kFlagRVec) && splits == 1 && aligned4(pr.r) &&
+                         cfg.r_async == 1;
+    if (r_async) flags |= gb::kFlagRAsync;
+    // Wide 32x64 boxes on the paired path (R and D by TMA, no Z, no split): one TMA load,
+    // one TMA store, one R wait and one fence per 64 columns instead of per 32.  Measured
+    // on GB300: +11 % on the K = 64 residual shape, +3 % on the activation-gradient shape;
+    // on by default.  A wide step spans two chunks, so every warpgroup's share of a tile
+    // must be whole steps.
+    const bool paired = r_tma && pr.k > 0 && d_tma && !pr.z;
+    const int groups = V::kEpi;
+    const bool wide_fits = (V::kBN / gb::kDChunk) % (2 * groups) == 0;
+    if (paired && wide_fits && cfg.wide != 0) flags |= gb::kFlagWide;
     const bool z_tma = pr.z && aligned16(pr.z) && pr.ldz % 8 == 0;
     if (!pr.ffn && pr.z) flags |= gb::kFlagZ | (z_tma ? gb::kFlagZTma : 0u);
     prm.z = static_cast<uint16_t*>(pr.z);
     prm.ldz = pr.ldz;
     prm.flags = flags;
     {
-        const int r_mode = r_tma ? 2 : (!pr.ffn && pr.r && !(flags & gb::kFlagRVec)) ? 1 : 0;
-        const auto lay = V::choose_layout(prm.kb_per_split, r_mode, cfg, info.smem_optin);
+        const int r_mode = r_tma ? 2 : r_async ? 3 : (!pr.ffn && pr.r && !(flags & gb::kFlagRVec)) ? 1 : 0;
+        const auto lay = V::choose_layout(prm.kb_per_split, r_mode, flags, cfg, info.smem_optin);
         prm.stages = lay.stages;
         prm.d_boxes = lay.d_boxes;
         prm.r_boxes = lay.r_boxes;
+        if (flags & gb::kFlagWide) prm.d_boxes *= 2;  // counted in 32x32 boxes
+        prm.r_warp_bytes = static_cast<uint32_t>(lay.r_boxes) * V::r_slot_bytes(flags);
     }
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
@@ -523,11 +570,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
                                       CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
             return st;
     }
-    if (d_tma &&
-        (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
+    const bool wide = flags & gb::kFlagWide;
+    const uint32_t box_n = wide ? 2 * gb::kDChunk : gb::kDChunk;
+    const CUtensorMapSwizzle box_sw = wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (d_tma && (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, box_n, 32, box_sw)) != GB_OK)
         return st;
-    if (r_tma &&
-        (st = make_tmap(&prm.tm_r, pr.r, pr.n, pr.m, pr.ldr * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
+    if (r_tma && (st = make_tmap(&prm.tm_r, pr.r, pr.n, pr.m, pr.ldr * 2, box_n, 32, box_sw)) != GB_OK)
         return st;
     if (z_tma &&
         (st = make_tmap(&prm.tm_z, pr.z, pr.n, pr.m, pr.ldz * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
@@ -561,11 +609,13 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
              prm.pingpong,
              V::kTileM, bn, gb::kBK,
              prm.stages,
-             prm.d_boxes, prm.r_boxes,
+             (flags & gb::kFlagWide) ? prm.d_boxes / 2 : prm.d_boxes, prm.r_boxes,
              static_cast<long long>(units * (V::kPair ? (mc ? 4 : 2) : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, prm.prod, prm.hint_a, prm.hint_b, prm.hint_r, prm.hint_d,
-             d_tma ? "tma" : "st.transposed",
-             pr.r ? (r_tma ? "tma" : (flags & gb::kFlagRVec) ? "ld.v4" : "ld.transposed") : "none",
+             d_tma ? (wide ? "tma.64x32" : "tma") : "st.transposed",
+             pr.r ? (r_tma ? (wide ? "tma.64x32" : "tma") : r_async ? "cp.async" : (flags & gb::kFlagRVec) ? "ld.v4"
+                                                                                                  : "ld.transposed")
+                  : "none",
              pr.z ? (z_tma ? "tma" : "st.transposed") : "none");
     t_plan = plan;
     {
@@ -1011,6 +1061,9 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "issue" && v >= -1 && v <= 3) c.issue = static_cast<int>(v);
             else if (key == "tmem_ld" && (v == 0 || v == 32 || v == 64)) c.tmem_ld = static_cast<int>(v);
             else if (key == "prod" && v >= 0 && v <= 3) c.prod = static_cast<int>(v);
+            else if (key == "r_async" && v >= -1 && v <= 1) c.r_async = static_cast<int>(v);
+            else if (key == "r_boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.r_boxes = static_cast<int>(v);
+            else if (key == "wide" && v >= -1 && v <= 1) c.wide = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

@@ -91,7 +91,17 @@ enum : uint32_t {
     kFlagZTma = 128u,    // Z stored by TMA (16-byte aligned rows)
     kFlagBMn = 256u,     // B is MN-major: a row-major [K, N] matrix (contraction over its rows)
     kFlagDact = 512u,    // the epilogue input multiplies: v *= act'(R) (activation gradient), no act
+    kFlagRAsync = 1024u, // R rows not 16-byte aligned (4-byte aligned base): cp.async word copies into
+                         // shared-memory slots, prefetched ahead of use like the TMA boxes
+    kFlagWide = 2048u,   // paired path with 32x64 R and D boxes (128-byte swizzle): one TMA load, one
+                         // TMA store, one barrier wait and one fence per 64 columns
 };
+constexpr uint32_t kWideBoxBytes = 32 * 2 * kDChunk * 2;  // one warp's 32x64 bf16 box
+// One R slot of the cp.async queue: 32 rows x 17 words (a 32-column row segment that
+// starts on a 2-byte boundary spans up to 17 aligned 4-byte words).  The 68-byte row
+// stride also makes a lane's reads of its own row conflict-free (17 is odd).
+constexpr uint32_t kRSlotWords = 17;
+constexpr uint32_t kRSlotAsyncBytes = 32 * kRSlotWords * 4;
 constexpr uint32_t kMnBoxBytes = 64 * kBK * 2;  // one MN-major B box: 64 columns x 64 contraction rows
 
 // Codes written to the device status word (low byte = gb_status_t).
@@ -133,8 +143,11 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     float* ws;
     uint32_t* ws_cnt;
     int32_t stages;   // depth of the operand ring (<= the variant's maximum)
-    int32_t d_boxes;  // D staging boxes per epilogue warp, 2..kMaxBoxes
-    int32_t r_boxes;  // R boxes per epilogue warp: 2..kMaxBoxes with an epilogue input (linear), else 0
+    // D staging boxes per epilogue warp, 2..kMaxBoxes, counted in 32x32 boxes (a wide
+    // 32x64 box takes two)
+    int32_t d_boxes;
+    int32_t r_boxes;  // R queue entries per epilogue warp: 2..kMaxBoxes with an epilogue input (linear), else 0
+    uint32_t r_warp_bytes;  // bytes of one epilogue warp's R queue: r_boxes x r_slot_bytes
     // Ping-pong (two epilogue warpgroups, no split): warpgroup g takes every work item
     // of local parity g -- always TMEM buffer g -- and all of its chunks, instead of
     // both warpgroups sharing every tile's chunks.
@@ -161,6 +174,15 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     // Timing trace (libraries built with GB_TRACE only): kTraceWords words per CTA.
     unsigned long long* trace;
 };
+
+// Bytes of one D / R queue entry of a launch: a 32x32 box, a 32x64 box (wide), or a
+// cp.async slot (unaligned R rows).
+__host__ __device__ __forceinline__ uint32_t d_slot_bytes(const GemmParams& p) {
+    return (p.flags & kFlagWide) ? kWideBoxBytes : kDStageBytes;
+}
+__host__ __device__ __forceinline__ uint32_t r_slot_bytes(const GemmParams& p) {
+    return (p.flags & kFlagRAsync) ? kRSlotAsyncBytes : (p.flags & kFlagWide) ? kWideBoxBytes : kDStageBytes;
+}
 
 // Trace record of one CTA (GB_TRACE builds): where each role waited, in SM clock
 // cycles, and when the CTA started and finished, in %globaltimer nanoseconds.
@@ -472,6 +494,77 @@ __device__ __forceinline__ void apply_input_box(const GemmParams& p, float (&v)[
     }
 }
 
+// Write chunk `half` (0: columns 0-31, 1: 32-63) of this lane's row of a 32x64 bf16
+// box, 128-byte swizzled for the TMA store (16-byte unit u of row r at u ^ (r % 8)).
+__device__ __forceinline__ void stage_wide_half(uint32_t box, const float (&v)[32], int half, int lane) {
+    const uint32_t row_addr = box + lane * 128;
+    const uint32_t sw = lane & 7u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        st_shared_v4(row_addr + (((4 * half + u) ^ sw) << 4), pack_bf16x2(v[8 * u], v[8 * u + 1]),
+                     pack_bf16x2(v[8 * u + 2], v[8 * u + 3]), pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
+                     pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+}
+
+// Combine chunk `half` of this lane's row of a 32x64 bf16 box staged by TMA (128-byte
+// swizzle) into v.
+template <int OP>
+__device__ __forceinline__ void combine_wide_half(float (&v)[32], uint32_t box, int half, int lane) {
+    const uint32_t row = box + lane * 128;
+    const uint32_t sw = lane & 7u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(row + (((4 * half + u) ^ sw) << 4)));
+        combine2<OP>(v[8 * u + 0], v[8 * u + 1], w0);
+        combine2<OP>(v[8 * u + 2], v[8 * u + 3], w1);
+        combine2<OP>(v[8 * u + 4], v[8 * u + 5], w2);
+        combine2<OP>(v[8 * u + 6], v[8 * u + 7], w3);
+    }
+}
+
+__device__ __forceinline__ void apply_input_wide(const GemmParams& p, float (&v)[32], uint32_t box, int half,
+                                                 int lane) {
+    switch (input_op(p.flags, p.act)) {
+        case 0: combine_wide_half<0>(v, box, half, lane); break;
+        case 1: combine_wide_half<1>(v, box, half, lane); break;
+        case 2: combine_wide_half<2>(v, box, half, lane); break;
+        case 3: combine_wide_half<3>(v, box, half, lane); break;
+        default: break;
+    }
+}
+
+// Combine this lane's row of a cp.async R slot (17 words per row, 68-byte stride) into v.
+// The row segment starts `sh` bits (0 or 16) into the row's first word.
+template <int OP>
+__device__ __forceinline__ void combine_slot_row(float (&v)[32], uint32_t slot, uint32_t sh, int lane) {
+    const uint32_t row = slot + static_cast<uint32_t>(lane) * (kRSlotWords * 4);
+    uint32_t w[kRSlotWords];
+#pragma unroll
+    for (uint32_t k = 0; k < kRSlotWords; ++k)
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[k]) : "r"(row + 4 * k));
+#pragma unroll
+    for (int k = 0; k < 16; ++k) combine2<OP>(v[2 * k], v[2 * k + 1], __funnelshift_r(w[k], w[k + 1], sh));
+}
+
+// The epilogue input of one chunk from its cp.async slot; `m` is this lane's row.  The
+// base is 4-byte aligned, so the segment starts mid-word exactly when its element
+// index m * ldr + n0 is odd.
+__device__ __forceinline__ void apply_input_slot(const GemmParams& p, float (&v)[32], uint32_t slot, int32_t m,
+                                                 int32_t n0, int lane) {
+    const uint32_t sh = ((static_cast<uint32_t>(m) & static_cast<uint32_t>(p.ldr)) ^ static_cast<uint32_t>(n0)) & 1u
+                            ? 16u : 0u;
+    switch (input_op(p.flags, p.act)) {
+        case 0: combine_slot_row<0>(v, slot, sh, lane); break;
+        case 1: combine_slot_row<1>(v, slot, sh, lane); break;
+        case 2: combine_slot_row<2>(v, slot, sh, lane); break;
+        case 3: combine_slot_row<3>(v, slot, sh, lane); break;
+        default: break;
+    }
+}
+
 // The same from global memory: a 16-byte aligned row segment of 32 values (rows past M skipped).
 template <int OP>
 __device__ __forceinline__ void combine_row_vec(float (&v)[32], const uint16_t* src) {
@@ -569,13 +662,13 @@ __device__ __forceinline__ void add_rows_transposed(const GemmParams& p, float (
 // `dbox` is this warp's first box, `dslot` the queue position (wraps).
 __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorMap* tm, uint16_t* out, int64_t ld,
                                             bool by_tma, const uint32_t (&packed)[16], int32_t row0, int32_t n0,
-                                            int valid, int lane, uint8_t* dbox, int32_t& dslot) {
+                                            int valid, int lane, uint32_t dbox, int32_t& dslot) {
     if (by_tma) {
-        uint8_t* buf = dbox + dslot * kDStageBytes;
+        const uint32_t buf = dbox + dslot * kDStageBytes;
         if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
         __syncwarp();
         // 64-byte rows, 16-byte units XOR-swizzled with (row / 2) % 4 (TMA 64B swizzle).
-        const uint32_t row_addr = smem_addr(buf) + lane * 64;
+        const uint32_t row_addr = buf + lane * 64;
         const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -584,12 +677,12 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorM
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_op(tm, smem_addr(buf), n0, row0, p.hint_d);
+            tma_store_op(tm, buf, n0, row0, p.hint_d);
             bulk_commit_group();
         }
         if (++dslot == p.d_boxes) dslot = 0;
     } else {
-        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, dbox);
+        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, shared_ptr(dbox));
     }
 }
 
@@ -601,8 +694,8 @@ template <int NUM_B>
 // R whose rows are not 16-byte aligned; `dbox`/`dslot` are this warp's D staging
 // queue and its position.  Warp-collective.
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32], int32_t m, int32_t row0,
-                                             int32_t n0, int lane, uint8_t* dbox, int32_t& dslot,
-                                             uint32_t rbox, uint8_t* tbuf_r,
+                                             int32_t n0, int lane, uint32_t dbox, int32_t& dslot,
+                                             uint32_t rbox, uint32_t tbuf_r,
                                              uint32_t* tr_ep = nullptr) {
     GB_TR_T0(tx);
     const int valid = min(32, p.n - n0);
@@ -634,7 +727,8 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
             }
         }
         if (rbox) {
-            apply_input_box(p, v, rbox, lane);
+            if (p.flags & kFlagRAsync) apply_input_slot(p, v, rbox, m, n0, lane);
+            else apply_input_box(p, v, rbox, lane);
         } else if (p.flags & kFlagResidual) {
             if (p.flags & kFlagRVec) {
                 // R (Z) rows are 16-byte aligned and ldr is a multiple of 8, so a row's
@@ -662,7 +756,7 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
                 }
             } else {
                 GB_TR_ADD(tr_ep, kTrEpMath, tx);
-                add_rows_transposed(p, v, row0, n0, valid, lane, tbuf_r);
+                add_rows_transposed(p, v, row0, n0, valid, lane, shared_ptr(tbuf_r));
                 GB_TR_ADD(tr_ep, kTrEpRWait, tx);
             }
         }
@@ -797,11 +891,17 @@ struct KernelShape {
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTxBytes = kCG * kStageBytes;  // bytes the leader's full barrier waits for
     static constexpr uint32_t kBarBytes = 2 * STAGES * 8 + kMaxBoxes * kEpiWarps * 8;  // ring + R barriers
-    // Layout: [ring: stages x stage][D boxes: warps x d_boxes][R boxes: warps x r_boxes][barriers][control].
-    static constexpr uint32_t smem_bytes(int stages, int d_boxes, int r_boxes) {
-        return 1024 /* alignment slack */ + stages * kStageBytes +
-               static_cast<uint32_t>(kEpiWarps * (d_boxes + r_boxes)) * kDStageBytes + kBarBytes + sizeof(SharedCtl);
+    // Layout: [barriers][control] in the first 1 KiB (fixed offsets, whatever the queue
+    // sizes), then [ring: stages x stage][D boxes: warps x d_boxes][R boxes: warps x r_boxes].
+    // `r_slot`, `d_slot`: bytes of one R / D queue entry (a 32x32 or 32x64 TMA box, or a
+    // cp.async slot).
+    static constexpr uint32_t kCtlBytes = 1024;
+    static constexpr uint32_t smem_bytes(int stages, int d_boxes, int r_boxes, uint32_t r_slot = kDStageBytes,
+                                         uint32_t d_slot = kDStageBytes) {
+        return 1024 /* alignment slack */ + kCtlBytes + stages * kStageBytes +
+               static_cast<uint32_t>(kEpiWarps * d_boxes) * d_slot + static_cast<uint32_t>(kEpiWarps * r_boxes) * r_slot;
     }
+    static_assert(kBarBytes + sizeof(SharedCtl) <= kCtlBytes, "barriers and control block fit in their 1 KiB");
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kMmaN);
     static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * kCG;  // epilogue warps of every CTA in the pair
     // split-K counters per tile: one per epilogue warp of every CTA of the tile, laid out
@@ -827,17 +927,18 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t stages = static_cast<uint32_t>(p.stages);
-    uint8_t* ring = smem;
-    uint8_t* dstage = smem + stages * S::kStageBytes;
-    uint8_t* rstage = dstage + kEpiWarps * p.d_boxes * kDStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(rstage + kEpiWarps * p.r_boxes * kDStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + STAGES;
     uint64_t* rbar = empty + STAGES;  // kMaxBoxes per epilogue warp
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(rbar + kMaxBoxes * kEpiWarps);
+    uint8_t* ring = smem + S::kCtlBytes;
+    uint8_t* dstage = ring + stages * S::kStageBytes;
+    const bool r_async = (NUM_B == 1) && (p.flags & kFlagRAsync);
+    uint8_t* rstage = dstage + kEpiWarps * p.d_boxes * kDStageBytes;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint64_t tmo = p.timeout_ns;
+    // (the wait limit p.timeout_ns is read from the parameter space where used: no register held)
 #ifdef GB_TRACE
     unsigned long long* trace = p.trace ? p.trace + static_cast<size_t>(blockIdx.x) * kTraceWords : nullptr;
     if (trace && threadIdx.x == 0) trace[kTrStartNs] = global_timer_ns();
@@ -870,7 +971,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                                               : S::kAccEmptyArrivals);
         }
         mbar_init(smem_addr(&ctl->drain), 1);
-        for (int i = 0; i < kMaxBoxes * kEpiWarps; ++i) mbar_init(smem_addr(&rbar[i]), 1);
+        // an R box lands on one arrival with its byte count (TMA); a cp.async slot on the
+        // 32 lanes' arrivals as their copies land
+        for (int i = 0; i < kMaxBoxes * kEpiWarps; ++i) mbar_init(smem_addr(&rbar[i]), r_async ? 32 : 1);
         ctl->abort = 0;
         fence_mbar_init();
     }
@@ -936,7 +1039,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                 ph ^= 1u;
                             }
                         }
-                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, tmo, kRoleProducer, s, &tr_empty)) {
+                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
                             ok = false;
                             break;
                         }
@@ -1017,7 +1120,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const uint32_t first = it > stages ? it - stages : 0u;
                     for (uint32_t i = first; i < it; ++i) {
                         if (p.inject == kInjectSkipFirstStage && i == 0) continue;
-                        drain_bar(smem_addr(&full[i % stages]), (i / stages) & 1u, tmo);
+                        drain_bar(smem_addr(&full[i % stages]), (i / stages) & 1u, p.timeout_ns);
                     }
                 }
             }
@@ -1048,7 +1151,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
                     const uint32_t b = local & 1;
                     const uint32_t aph = (local >> 1) & 1u;
-                    if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, tmo, kRoleMma, 0x100u | b,
+                    if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, p.timeout_ns, kRoleMma, 0x100u | b,
                                   &tr_acc)) {
                         ok = false;
                         break;
@@ -1061,7 +1164,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         // fence run while this k-block's third MMA executes.
                         if (!issue_tile_lean<CG, S::kStageBytes, S::kABytes>(
                                 p, d_tmem, nkb, full, empty, ring, stages, s, ph, it, b_mn, idesc, bstep,
-                                mc ? static_cast<uint16_t>(0xF) : pair_mask, abort_flag, tmo, tr_full, issued)) {
+                                mc ? static_cast<uint16_t>(0xF) : pair_mask, abort_flag, p.timeout_ns, tr_full, issued)) {
                             ok = false;
                             break;
                         }
@@ -1078,7 +1181,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const unsigned long long blocked_before = tr_full.n;
                         const long long wait_c0 = clock64();
 #endif
-                        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s, &tr_full)) {
+                        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, p.timeout_ns, kRoleMma, s, &tr_full)) {
                             ok = false;
                             break;
                         }
@@ -1143,7 +1246,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 if (!ok && issued) {
                     // Drain: every MMA issued so far must finish before TMEM is freed.
                     mma_commit<CG>(smem_addr(&ctl->drain));
-                    drain_bar(smem_addr(&ctl->drain), 0, tmo);
+                    drain_bar(smem_addr(&ctl->drain), 0, p.timeout_ns);
                 }
             }
             __syncwarp();
@@ -1163,7 +1266,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const int32_t slab_row = static_cast<int32_t>(rank) * kBM + q * 32 + lane;  // row within the tile
         constexpr int64_t kPartFloats = static_cast<int64_t>(S::kTileM) * BN;       // one partial accumulator
-        uint8_t* dbox = dstage + e * p.d_boxes * kDStageBytes;  // this warp's D staging queue
+        const uint32_t dbox = smem_addr(dstage) + e * p.d_boxes * kDStageBytes;  // this warp's D staging queue
         int32_t dslot = 0;
         int32_t local = 0;
         TraceAcc tr_accfull;
@@ -1180,6 +1283,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         // pairs keeps up to r_boxes 32x32 R boxes in flight ahead of their use, so
         // the loads for the next tile overlap the current tile's MMAs.
         const bool r_tma = (NUM_B == 1) && (p.flags & kFlagRTma);
+        // R rows not 16-byte aligned: the same queue, filled by per-lane cp.async word copies
+        // (general path; the host sets this only without split-K)
+        const bool r_queue = r_tma || r_async;
         const bool express = p.splits == 1 && p.num_k_blocks > 0 && (p.flags & kFlagDTma) &&
                              !(p.flags & (kFlagResidual | kFlagZ));
         // Paired path (R by TMA, D by TMA, no second output, no split): two chunks per
@@ -1189,9 +1295,15 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             !(p.flags & kFlagZ);
         // this warp's R boxes; also the transpose buffer for unaligned R rows (the
         // boxes are unused then)
-        uint8_t* rbox0 = rstage + e * p.r_boxes * kDStageBytes;
-        uint8_t* tbuf_r = NUM_B == 1 ? rbox0 : nullptr;
-        int32_t rc_w = unit, rc_local = 0, rc_c = c0, rc_mb = -1, rc_nb = -1;
+        const uint32_t r_slot = r_slot_bytes(p);  // bytes per R queue entry
+        const uint32_t rbox0 = smem_addr(rstage) + e * p.r_warp_bytes;
+        const uint32_t tbuf_r = rbox0;
+        // Wide boxes (paired path only): a step covers chunks (c, c + 1); warpgroup g takes
+        // the steps starting at chunk 2g, 2g + 2 * groups, ... (all of them with ping-pong),
+        // i.e. first chunk 2 * c0 and stride 2 * cstep.  The R cursor walks this warp's R
+        // boxes: chunks, or the first chunks of wide steps.
+        const bool wide = (NUM_B == 1) && (p.flags & kFlagWide);
+        int32_t rc_w = unit, rc_local = 0, rc_c = wide ? 2 * c0 : c0, rc_mb = -1, rc_nb = -1;
         uint32_t r_pending = 0, r_phase = 0;  // R boxes issued and not yet used; one parity bit per box
         int32_t r_islot = 0, r_uslot = 0;                 // queue positions of the next load and the next use
         auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
@@ -1204,9 +1316,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 if (rc_mb < 0) work_tile(rc_w, p, pairi, rc_mb, rc_nb);
                 const int32_t r0 = rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;
                 if (rc_c < kChunks && r0 < p.m && rc_nb * BN + rc_c * kDChunk < p.n) return true;
-                rc_c += cstep;
+                rc_c += wide ? 2 * cstep : cstep;
                 if (rc_c >= kChunks) {
-                    rc_c = c0;
+                    rc_c = wide ? 2 * c0 : c0;
                     rc_w += units;
                     ++rc_local;
                     rc_mb = -1;
@@ -1215,24 +1327,57 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             return false;
         };
         auto r_issue = [&]() {
-            if (!r_tma || !r_find()) return;
-            if (lane == 0) {
+            if (!r_queue || !r_find()) return;
+            if (r_async) {
+                // 32 rows x 17 words, row-major over the warp: copy t = 32 i + lane is word
+                // t % 17 of row t / 17, so each instruction reads consecutive words of two or three rows
+                // and writes 128 contiguous bytes of the slot.  A word reads only the bytes
+                // of its row segment [n0, n0 + valid) (src-size), except that a segment
+                // starting on a 2-byte boundary also reads the element just before it (in
+                // the tensor: the base is 4-byte aligned, so that element index is >= 0).
+                const int32_t rbase = rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;
+                const int32_t n0 = rc_nb * BN + rc_c * kDChunk;
+                const int32_t valid = min(kDChunk, p.n - n0);
+                const uint32_t dst0 = rbox0 + r_islot * kRSlotAsyncBytes;
                 const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_islot]);
-                mbar_arrive_expect_tx(bar, kDStageBytes);
-                tma_load_op<false>(smem_addr(rbox0 + r_islot * kDStageBytes), &p.tm_r, bar, rc_nb * BN + rc_c * kDChunk,
+                const uintptr_t base = reinterpret_cast<uintptr_t>(p.r);
+#pragma unroll 1
+                for (uint32_t i = 0; i < kRSlotWords; ++i) {
+                    const uint32_t t = i * 32u + static_cast<uint32_t>(lane);
+                    const uint32_t rr = t / kRSlotWords;
+                    const uint32_t j = t - rr * kRSlotWords;
+                    const int32_t row = rbase + static_cast<int32_t>(rr);
+                    const void* src = p.r;
+                    uint32_t bytes = 0;
+                    if (row < p.m) {
+                        const uintptr_t a = base + 2u * static_cast<uintptr_t>(static_cast<int64_t>(row) * p.ldr + n0);
+                        const uintptr_t w = (a & ~static_cast<uintptr_t>(3)) + 4u * j;
+                        const uintptr_t end = a + 2u * static_cast<uintptr_t>(valid);
+                        if (w < end) {
+                            bytes = static_cast<uint32_t>(min(static_cast<uintptr_t>(4), end - w));
+                            src = reinterpret_cast<const void*>(w);
+                        }
+                    }
+                    cp_async_4(dst0 + 4u * t, src, bytes);
+                }
+                cp_async_mbar_arrive_noinc(bar);
+            } else if (lane == 0) {
+                const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_islot]);
+                mbar_arrive_expect_tx(bar, r_slot);
+                tma_load_op<false>(rbox0 + r_islot * r_slot, &p.tm_r, bar, rc_nb * BN + rc_c * kDChunk,
                                    rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32, l2_policy(p.hint_r));
             }
             ++r_pending;
             if (++r_islot == p.r_boxes) r_islot = 0;
-            rc_c += cstep;
+            rc_c += wide ? 2 * cstep : cstep;
             if (rc_c >= kChunks) {
-                rc_c = c0;
+                rc_c = wide ? 2 * c0 : c0;
                 rc_w += units;
                 ++rc_local;
                 rc_mb = -1;
             }
         };
-        if (r_tma)
+        if (r_queue)
             for (int i = 0; i < p.r_boxes; ++i) r_issue();
 
         for (int32_t w = unit; w < num_work; w += units, ++local) {
@@ -1241,7 +1386,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             const uint32_t aph = (local >> 1) & 1u;
             bool ok = true;
             if (lane == 0)
-                ok = wait_bar(smem_addr(&ctl->acc_full[b]), aph, abort_flag, tmo, kRoleEpilogue, b, &tr_accfull);
+                ok = wait_bar(smem_addr(&ctl->acc_full[b]), aph, abort_flag, p.timeout_ns, kRoleEpilogue, b, &tr_accfull);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
@@ -1319,11 +1464,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 #pragma unroll
                     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                     GB_TR_ADD(tr_ep, kTrEpMath, tx);
-                    uint8_t* buf = dbox + dslot * kDStageBytes;
+                    const uint32_t buf = dbox + dslot * kDStageBytes;
                     if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
                     __syncwarp();
                     GB_TR_ADD(tr_ep, kTrEpDBox, tx);
-                    const uint32_t row_addr = smem_addr(buf) + lane * 64;
+                    const uint32_t row_addr = buf + lane * 64;
                     const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
@@ -1332,7 +1477,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_op(&p.tm_d, smem_addr(buf), n0, row0, p.hint_d);
+                        tma_store_op(&p.tm_d, buf, n0, row0, p.hint_d);
                         bulk_commit_group();
                     }
                     if (++dslot == p.d_boxes) dslot = 0;
@@ -1345,31 +1490,36 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             }
             if constexpr (NUM_B == 1) {
                 if (paired) {
-                    // This warp's chunks of the tile come in pairs (c, c + cstep): kChunks /
+                    // This warp's chunks of the tile come in pairs (c, c + cs): kChunks /
                     // cstep is even for every variant.  The two chunks are computed one after
-                    // the other (one chunk's registers), but share one wait for two free D
-                    // boxes, one proxy fence and one warp sync before their two stores.
-                    // Chunk b is on only if chunk a is.
+                    // the other (one chunk's registers), but share one wait for free D boxes,
+                    // one proxy fence and one warp sync before their stores.  Chunk b is on
+                    // only if chunk a is.  With wide boxes the pair is two adjacent chunks
+                    // (cs = 1; pairs start at 2 * c0, 2 * c0 + 2 * cstep, ...) that share one
+                    // 32x64 R box and one 32x64 D box (one TMA load, one store, one R wait);
+                    // a box half past N is loaded as zeros and clipped by the store.
+                    const int cs = wide ? 1 : cstep;
                     bool rok = true;
 #pragma unroll 1
-                    for (int c = c0; c < kChunks; c += 2 * cstep) {
+                    for (int c = wide ? 2 * c0 : c0; c < kChunks; c += 2 * cstep) {
                         const bool last = c + 2 * cstep >= kChunks;
                         const int nchunks = !(warp_rows && nb * BN + c * kDChunk < p.n) ? 0
-                                            : (nb * BN + (c + cstep) * kDChunk < p.n ? 2 : 1);
+                                            : (nb * BN + (c + cs) * kDChunk < p.n ? 2 : 1);
                         GB_TR_T0(tx);
                         if (nchunks > 0) {
-                            // two D boxes free: the stores that last used them have read them
-                            if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 2);
+                            // D boxes free (two, or one wide): the stores that last used them
+                            // have read them
+                            if (lane == 0) bulk_wait_group_read_at_most(wide ? (p.d_boxes >> 1) - 1 : p.d_boxes - 2);
                             __syncwarp();
                         }
                         GB_TR_ADD(tr_ep, kTrEpDBox, tx);
 #ifdef GB_TRACE
                         if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
-                        uint32_t box_a = 0;
+                        uint32_t box_a = 0, rcur = 0;
 #pragma unroll 1
                         for (int i = 0; i < 2; ++i) {
-                            const int ci = c + i * cstep;
+                            const int ci = c + i * cs;
                             const int32_t n0 = nb * BN + ci * kDChunk;
                             float v[32];
                             if (i < nchunks) {
@@ -1407,22 +1557,33 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                     break;
                             }
                             GB_TR_ADD(tr_ep, kTrEpMath, tx);
-                            // this chunk's R box: the one at the use position of the queue
-                            const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
-                            const uint32_t par = (r_phase >> r_uslot) & 1u;
-                            if (lane == 0) rok = wait_bar(bar, par, abort_flag, tmo, kRoleEpilogue, 0x200u | r_uslot);
-                            rok = __shfl_sync(0xffffffffu, rok, 0);
-                            if (!rok) break;
-                            while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
+                            if (!wide || i == 0) {
+                                // this chunk's (step's) R box: the one at the use position of the queue
+                                const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
+                                const uint32_t par = (r_phase >> r_uslot) & 1u;
+                                if (lane == 0) rok = wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot);
+                                rok = __shfl_sync(0xffffffffu, rok, 0);
+                                if (!rok) break;
+                                while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
+                                }
+                                r_phase ^= 1u << r_uslot;
+                                rcur = rbox0 + r_uslot * r_slot;
+                                --r_pending;
+                                if (++r_uslot == p.r_boxes) r_uslot = 0;
                             }
                             GB_TR_ADD(tr_ep, kTrEpRWait, tx);
-                            r_phase ^= 1u << r_uslot;
-                            apply_input_box(p, v, smem_addr(rbox0 + r_uslot * kDStageBytes), lane);
-                            --r_pending;
-                            if (++r_uslot == p.r_boxes) r_uslot = 0;
-                            const uint32_t box = smem_addr(dbox + dslot * kDStageBytes);
-                            if (++dslot == p.d_boxes) dslot = 0;
-                            stage_box_row(box, v, lane);
+                            uint32_t box = box_a;
+                            if (!wide || i == 0) {
+                                box = dbox + dslot * d_slot_bytes(p);
+                                if (++dslot == (wide ? p.d_boxes >> 1 : p.d_boxes)) dslot = 0;
+                            }
+                            if (wide) {
+                                apply_input_wide(p, v, rcur, i, lane);
+                                stage_wide_half(box, v, i, lane);
+                            } else {
+                                apply_input_box(p, v, rcur, lane);
+                                stage_box_row(box, v, lane);
+                            }
                             GB_TR_ADD(tr_ep, kTrEpMath, tx);
                             if (i == 0) {
                                 box_a = box;
@@ -1433,10 +1594,12 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                tma_store_op(&p.tm_d, box_a, n0 - cstep * kDChunk, row0, p.hint_d);
+                                tma_store_op(&p.tm_d, box_a, n0 - cs * kDChunk, row0, p.hint_d);
                                 bulk_commit_group();
-                                tma_store_op(&p.tm_d, box, n0, row0, p.hint_d);
-                                bulk_commit_group();
+                                if (!wide) {
+                                    tma_store_op(&p.tm_d, box, n0, row0, p.hint_d);
+                                    bulk_commit_group();
+                                }
                             }
                             GB_TR_ADD(tr_ep, kTrEpStore, tx);
                         }
@@ -1450,8 +1613,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             }
                         }
                         GB_TR_T0(ti);
+                        const int n_issue = wide ? (nchunks > 0 ? 1 : 0) : nchunks;
 #pragma unroll 1
-                        for (int i = 0; i < nchunks; ++i) r_issue();
+                        for (int i = 0; i < n_issue; ++i) r_issue();
                         GB_TR_ADD(tr_ep, kTrEpRIssue, ti);
                     }
                     if (!rok) break;
@@ -1513,17 +1677,17 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 GB_TR_ADD(tr_ep, kTrEpTmemLd, tg);
                 if (!chunk_on || split_mode) continue;
                 uint32_t rbox = 0;
-                if (r_tma) {
+                if (r_queue) {
                     const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
                     const uint32_t par = (r_phase >> r_uslot) & 1u;
                     bool rok = true;
-                    if (lane == 0) rok = wait_bar(bar, par, abort_flag, tmo, kRoleEpilogue, 0x200u | r_uslot);
+                    if (lane == 0) rok = wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot);
                     rok = __shfl_sync(0xffffffffu, rok, 0);
                     if (!rok) break;
-                    while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
+                    while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the slot's data
                     }
                     r_phase ^= 1u << r_uslot;
-                    rbox = smem_addr(rbox0 + r_uslot * kDStageBytes);
+                    rbox = rbox0 + r_uslot * r_slot;
                 }
                 GB_TR_ADD(tr_ep, kTrEpRWait, tg);
 #ifdef GB_TRACE
@@ -1531,9 +1695,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 #else
                 finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r);
 #endif
-                if (r_tma) {
+                if (r_queue) {
                     __syncwarp();  // every lane has read the box: refill it
-                    fence_proxy_async_smem();
+                    if (r_tma) fence_proxy_async_smem();
                     --r_pending;
                     if (++r_uslot == p.r_boxes) r_uslot = 0;
                     r_issue();
@@ -1584,7 +1748,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             // position on): wait (bounded) for them to land.
             int32_t slot = r_uslot;
             for (uint32_t i = 0; i < r_pending; ++i) {
-                drain_bar(smem_addr(&rbar[e * kMaxBoxes + slot]), (r_phase >> slot) & 1u, tmo);
+                drain_bar(smem_addr(&rbar[e * kMaxBoxes + slot]), (r_phase >> slot) & 1u, p.timeout_ns);
                 if (++slot == p.r_boxes) slot = 0;
             }
             bulk_wait_group<0>();

@@ -11,6 +11,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// A generic pointer to the shared-memory byte at 32-bit shared address `addr`.
+__device__ __forceinline__ uint8_t* shared_ptr(uint32_t addr) {
+    return static_cast<uint8_t*>(__cvta_shared_to_generic(addr));
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -114,6 +119,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
     asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+// Per-thread asynchronous copy of one 4-byte word global -> shared (4-byte aligned
+// addresses).  Only the first `src_bytes` (0..4) bytes are read; the rest of the word
+// is zero-filled, so a word that is partly or wholly outside a row segment reads
+// nothing outside it.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued before has landed; the
+// barrier's expected count includes this arrival (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---------------------------------------------------------------- L2 cache policies

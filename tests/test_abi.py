@@ -97,10 +97,11 @@ def test_ffn_rejects(L, args, needle):
 
 def test_config_parser(L):
     assert L.gb_set_config(b"bn=128,grid=4,persistent=0,group=8,zigzag=1,pair=1,stages=3,boxes=4,pingpong=1") == GB_OK
+    assert L.gb_set_config(b"r_async=0,r_boxes=5") == GB_OK
     assert L.gb_set_config(None) == GB_OK
     assert L.gb_set_config(b"") == GB_OK
     for bad in (b"bn=96", b"nope=1", b"grid", b"group=0", b"zigzag=2", b"bn=12x", b"pair=2", b"stages=-1", b"boxes=1",
-                b"boxes=9", b"pingpong=2", b"pingpong=-2"):
+                b"boxes=9", b"pingpong=2", b"pingpong=-2", b"r_async=2", b"r_boxes=1", b"r_boxes=9"):
         assert L.gb_set_config(bad) == GB_ERR_INVALID_ARG, bad
     assert L.gb_set_config(None) == GB_OK
 

@@ -87,7 +87,8 @@ def test_dact_index_pattern():
 
 
 @pytest.mark.parametrize("cfg", ["pair=0", "pair=1", "epi=1", "epi=2", "stages=3", "boxes=4", "bn=128",
-                                 "pingpong=1", "grid=8", "persistent=0"])
+                                 "pingpong=1", "grid=8", "persistent=0", "wide=1", "wide=1,pingpong=1",
+                                 "wide=1,epi=1,bn=128"])
 def test_dact_configs_identical_bits(cfg):
     """Every schedule gives the same bits (the per-element sum order inside a tile is fixed)."""
     M, N, K = 400, 320, 600
@@ -110,6 +111,10 @@ def test_dact_unaligned_z_and_d(act):
     plan = gb.last_plan()
     assert "d_store=st.transposed" in plan and "r_load=ld.transposed" in plan, plan
     assert_close(got, ref(dY, W, Z, act), f"K=4099 {act}")
+    gb.set_config("r_async=1")
+    pre = run(dY, W, Z, act)
+    assert "r_load=cp.async" in gb.last_plan(), gb.last_plan()
+    assert_bitexact(pre, got, f"K=4099 {act} cp.async queue vs loads at use")
 
 
 def test_dact_strided_views_and_vector_loads():

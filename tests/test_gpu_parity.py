@@ -92,16 +92,76 @@ def test_epilogue_variants(act, with_bias, with_r):
     assert_close(run_linear(A, B, bias, R, act), ref_linear(A, B, bias, R, act), f"{act} {with_bias} {with_r}")
 
 
-def test_unaligned_d_and_r_use_plain_loads_and_stores():
+@pytest.mark.parametrize("r_async", [0, 1])
+def test_unaligned_d_and_r_use_plain_loads_and_stores(r_async):
     """N = 4099: rows of D and R are 8198 bytes apart (not a multiple of 16), so the
-    kernel moves them through its shared-memory transpose with plain loads/stores."""
+    kernel stores D through its shared-memory transpose with plain stores, and reads R
+    either the same way at use (r_async=0) or by cp.async words into a prefetch queue."""
+    gb.set_config(f"r_async={r_async}")
     M, N, K = 200, 4099, 128
     A = inputs.randn_bf16((M, K), seed=30)
     B = inputs.randn_bf16((N, K), seed=31, std=1.0 / np.sqrt(K))
     R = inputs.randn_bf16((M, N), seed=32)
     got = run_linear(A, B, None, R)
-    assert "d_store=st.transposed" in gb.last_plan() and "r_load=ld.transposed" in gb.last_plan()
+    plan = gb.last_plan()
+    assert "d_store=st.transposed" in plan, plan
+    assert ("r_load=cp.async" if r_async else "r_load=ld.transposed") in plan, plan
     assert_close(got, ref_linear(A, B, None, R), "N=4099")
+
+
+def _unaligned_r(M, N, ldr, off, seed):
+    """R[M, N] as a view with leading dimension `ldr` starting `off` elements into its
+    buffer: the host copy (contiguous) and the device view."""
+    big = inputs.randn_bf16((M * ldr + off + 8,), seed=seed)
+    host = big[off:off + M * ldr].view(M, ldr)[:, :N]
+    dev = big.to(DEV)[off:off + M * ldr].view(M, ldr)[:, :N]
+    return host.contiguous(), dev
+
+
+@pytest.mark.parametrize("spec", ["", "epi=1", "epi=2", "pair=0,grid=3", "pingpong=1", "r_boxes=2", "r_boxes=8",
+                                  "r_boxes=8,stages=2", "grid=1", "bn=128,grid=5", "boxes=8,r_boxes=3"])
+@pytest.mark.parametrize("M,N,K,ldr,off", [
+    (300, 4099, 520, 4099, 0),   # odd row stride: segments alternate between word and half-word starts
+    (130, 520, 192, 522, 2),     # 4-byte (not 16-byte) aligned base, even stride: every segment word-aligned
+    (77, 516, 64, 519, 2),       # 4-byte aligned base, odd stride, ragged M
+    (45, 13, 72, 13, 0),         # N < 32: every segment shorter than a chunk
+    (129, 33, 0, 35, 4),         # K = 0: D = R; a 1-column tail chunk
+    (257, 1001, 4096, 1001, 0),  # long K, ragged in every dimension
+])
+def test_unaligned_r_cp_async_queue(spec, M, N, K, ldr, off):
+    """R rows not 16-byte aligned but the base 4-byte aligned: the cp.async prefetch queue.
+    Bit-identical to the synchronous loads at use (the same bf16 values are combined in
+    the same order) and within tolerance of the oracle; the elements outside the view
+    (the stride's padding, the element before an odd segment) do not leak in."""
+    A = inputs.randn_bf16((M, K), seed=M + K)
+    B = inputs.randn_bf16((N, K), seed=N + 1, std=1.0 / np.sqrt(max(K, 1)))
+    bias = inputs.randn_bf16((N,), seed=5, std=0.1)
+    R_host, R_dev = _unaligned_r(M, N, ldr, off, seed=ldr + off)
+    assert R_dev.data_ptr() % 4 == 0 and (R_dev.data_ptr() % 16 != 0 or ldr % 8 != 0)
+    outs = {}
+    for ra in (0, 1):
+        gb.set_config(",".join(x for x in (spec, f"r_async={ra}") if x))
+        d = gb.linear(A.to(DEV), B.to(DEV), bias.to(DEV), R_dev, act="gelu_tanh")
+        gb.device_status()
+        plan = gb.last_plan()
+        assert ("r_load=cp.async" if ra else "r_load=ld.transposed") in plan, plan
+        outs[ra] = bits(d)
+    assert_bitexact(outs[1], outs[0], f"{spec} {M}x{N}x{K} ldr={ldr} off={off}")
+    assert_close(outs[1], ref_linear(A, B, bias, R_host, "gelu_tanh"), f"{spec} {M}x{N}x{K}")
+
+
+def test_unaligned_r_2_byte_base_stays_synchronous():
+    """A base only 2-byte aligned cannot be copied in aligned words without reading the
+    element before the tensor: the synchronous loads serve it."""
+    M, N, K = 64, 300, 64
+    A = inputs.randn_bf16((M, K), seed=7)
+    B = inputs.randn_bf16((N, K), seed=8, std=0.1)
+    R_host, R_dev = _unaligned_r(M, N, 301, 1, seed=9)
+    assert R_dev.data_ptr() % 4 == 2
+    d = gb.linear(A.to(DEV), B.to(DEV), None, R_dev)
+    gb.device_status()
+    assert "r_load=ld.transposed" in gb.last_plan(), gb.last_plan()
+    assert_close(bits(d), ref_linear(A, B, None, R_host), "2-byte base")
 
 
 def test_strided_views_and_offset_d():
@@ -419,15 +479,23 @@ def test_ragged_last_tile_column(pair, rem):
 
 
 def test_short_k_plan_takes_deep_queues():
-    """Work items of at most 4 k-blocks get a 3-stage ring, the deepest queues that fit
-    and, with at least 4 work items per unit, the ping-pong schedule; long-K items keep
-    the deepest ring, two boxes per warp and the shared schedule."""
+    """Work items of at most 4 k-blocks get a short ring and deep queues -- with wide
+    32x64 boxes a 2-stage ring, two D boxes and the deepest R queue that fits; with 32x32
+    boxes a 3-stage ring and the deepest D and R queues -- and, with at least 4 work items
+    per unit, the ping-pong schedule; long-K items keep the deepest ring, two boxes per
+    warp and the shared schedule."""
     A = inputs.randn_bf16((512, 4096), seed=150)
     B = inputs.randn_bf16((512, 4096), seed=151, std=1.0 / 64)
     R = inputs.randn_bf16((512, 512), seed=152)
     run_linear(A[:, :64].contiguous(), B[:, :64].contiguous(), None, R)
     short = gb.last_plan()
-    assert "stages=3" in short and "boxes=2/" not in short and "pingpong=0" in short, short  # 4 tiles only
+    assert "stages=2" in short and "boxes=2/" in short and "boxes=2/2" not in short, short
+    assert "pingpong=0" in short and "tma.64x32" in short, short  # 4 tiles only
+    gb.set_config("wide=0")
+    run_linear(A[:, :64].contiguous(), B[:, :64].contiguous(), None, R)
+    short = gb.last_plan()
+    gb.set_config(None)
+    assert "stages=3" in short and "boxes=2/" not in short and "pingpong=0" in short, short
     run_linear(A, B, None, R)
     long = gb.last_plan()
     assert "boxes=2/2" in long and "stages=3 " not in long and "pingpong=0" in long, long
@@ -438,7 +506,7 @@ def test_short_k_plan_takes_deep_queues():
     D = gb.linear(Ab, Bb, None, Rb)
     gb.device_status()
     big = gb.last_plan()
-    assert "pingpong=1" in big and "stages=3" in big, big
+    assert "pingpong=1" in big and "stages=2" in big and "tma.64x32" in big, big
     assert torch.equal(D.view(torch.int16), Rb.view(torch.int16))
 
 
@@ -539,3 +607,30 @@ def test_schedules_identical_bits_on_ragged_shapes(spec):
         gb.device_status()
         gb.set_config(None)
         assert_bitexact(d1, d0, f"ffn {spec} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("spec", ["", "wide=1", "wide=1,pingpong=1", "wide=1,pingpong=0", "wide=1,epi=1",
+                                  "wide=1,bn=128", "wide=1,bn=128,epi=2,pingpong=0", "wide=1,boxes=8",
+                                  "wide=1,pair=0,grid=3", "wide=1,stages=2,grid=2", "wide=1,r_boxes=2,boxes=2"])
+def test_wide_boxes_identical_bits(spec):
+    """32x64 R and D boxes (128-byte swizzle) on the paired epilogue path: the same values
+    combined in the same order as with 32x32 boxes, so identical bits -- on shapes whose
+    last 64-column step is partial (N = 904, 264, 96: one chunk, 8 or 32 columns, the box's
+    other half zero-filled on load and clipped by the store; N = 1320: a full chunk and an
+    8-column one), ragged M, short and long K, with bias, activation and the residual."""
+    for M, N, K in [(700, 904, 64), (513, 1320, 200), (300, 264, 64), (129, 96, 128), (64, 2048, 64)]:
+        A = inputs.randn_bf16((M, K), seed=M + 11)
+        B = inputs.randn_bf16((N, K), seed=N + 12, std=0.1)
+        bias = inputs.randn_bf16((N,), seed=13, std=0.1)
+        R = inputs.randn_bf16((M, N), seed=14)
+        gb.set_config("wide=0")
+        base = run_linear(A, B, bias, R, "gelu_tanh")
+        assert "r_load=tma " in gb.last_plan() + " ", gb.last_plan()
+        gb.set_config(spec or None)
+        got = run_linear(A, B, bias, R, "gelu_tanh")
+        plan = gb.last_plan()
+        gb.set_config(None)
+        assert "d_store=tma.64x32" in plan and "r_load=tma.64x32" in plan, plan
+        assert_bitexact(got, base, f"{spec} {M}x{N}x{K}")
+        if (M, N, K) == (700, 904, 64):
+            assert_close(got, ref_linear(A, B, bias, R, "gelu_tanh"), spec)
