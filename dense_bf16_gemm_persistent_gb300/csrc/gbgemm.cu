@@ -282,6 +282,21 @@ struct Variant {
         int rq = cfg.r_boxes > 0 ? cfg.r_boxes : (short_k ? gb::kMaxBoxes : 3);
         auto r_of = [&](int b) { return r_mode == 2 ? (cfg.r_boxes > 0 ? rq : b) : r_mode == 3 ? rq : (r_mode == 1 ? 2 : 0); };
         const uint32_t rs = r_slot_bytes(flags), ds = d_slot_bytes(flags);
+        if (kEpi == 4) {
+            // Sixteen epilogue warps: per-warp queues must be short to fit.  Wide boxes:
+            // one D box and one R box per warp (the other warps of the SM hide each one's
+            // waits); 32x32 boxes: two D and three R.  A 2-stage ring unless asked.
+            const bool wide = flags & gb::kFlagWide;
+            const int lst = std::max(2, cfg.stages > 0 ? std::min(cfg.stages, STAGES) : 2);
+            int ld = cfg.boxes > 0 ? cfg.boxes : (wide ? 1 : 2);
+            int lr = cfg.r_boxes > 0 ? cfg.r_boxes : (wide ? 1 : 3);
+            const int lmin = wide ? 1 : 2;
+            while (lr > lmin && S::smem_bytes(lst, ld, lr, rs, ds) > smem_optin) --lr;
+            while (ld > lmin && S::smem_bytes(lst, ld, lr, rs, ds) > smem_optin) --ld;
+            int ls = lst;
+            while (ls > 2 && S::smem_bytes(ls, ld, lr, rs, ds) > smem_optin) --ls;
+            return Layout{ls, ld, lr};
+        }
         if (short_k && (flags & gb::kFlagWide) && cfg.stages <= 0 && cfg.boxes <= 0 && cfg.r_boxes <= 0) {
             // Wide boxes on items of 1-4 k-blocks: a 2-stage ring is enough (the MMAs are a
             // few percent of the time) and the room goes to R boxes in flight, whose loads
@@ -426,7 +441,7 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.num_k_blocks = static_cast<int32_t>(cdiv(pr.k, gb::kBK));
     // A multicast between two CTA pairs: on request, for CTA-pair variants without a
     // split, when 4-CTA clusters fit; a work item is then one tile-row x two tile-columns.
-    const bool mc = V::kPair && cfg.mc == 1 && max_units_mc > 0 && !(sr.allowed) && pr.k > 0;
+    const bool mc = V::kPair && V::kEpi != 4 && cfg.mc == 1 && max_units_mc > 0 && !(sr.allowed) && pr.k > 0;
     prm.mc = mc ? 1 : 0;
     prm.sched_n_blocks = mc ? static_cast<int32_t>(cdiv(prm.num_n_blocks, 2)) : prm.num_n_blocks;
     const int64_t tiles = static_cast<int64_t>(prm.num_m_blocks) * prm.sched_n_blocks;
@@ -454,6 +469,13 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.kb_per_split = static_cast<int32_t>(cdiv(prm.num_k_blocks, splits));
     if (prm.kb_per_split > 0) splits = static_cast<int>(cdiv(prm.num_k_blocks, prm.kb_per_split));
     prm.splits = splits;
+    // The lean variant (four epilogue warpgroups) has only the paired epilogue path: a
+    // split plan runs on the two-warpgroup kernel instead.
+    if constexpr (V::kEpi == 4) {
+        if (splits != 1)
+            return plan_and_launch<Variant<V::kBN, 1, 6, true, 2>>(pr, cfg, bn, dev, info, timeout_ns, inject, stream,
+                                                                   sr);
+    }
     const int64_t work = tiles * splits;
     if (work > kMaxDim) return fail(GB_ERR_UNSUPPORTED, "too many work items");
 
@@ -533,7 +555,11 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     const bool paired = r_tma && pr.k > 0 && d_tma && !pr.z;
     const int groups = V::kEpi;
     const bool wide_fits = (V::kBN / gb::kDChunk) % (2 * groups) == 0;
-    if (paired && wide_fits && cfg.wide != 0) flags |= gb::kFlagWide;
+    // (the four-warpgroup kernel defaults to 32x32 boxes: sixteen warps' queues of wide
+    // boxes leave room for one D and one R box each, measured 7 % slower than two and three
+    // 32x32 boxes)
+    const bool wide_default = V::kEpi != 4;
+    if (paired && wide_fits && (cfg.wide == 1 || (cfg.wide < 0 && wide_default))) flags |= gb::kFlagWide;
     const bool z_tma = pr.z && aligned16(pr.z) && pr.ldz % 8 == 0;
     if (!pr.ffn && pr.z) flags |= gb::kFlagZ | (z_tma ? gb::kFlagZTma : 0u);
     prm.z = static_cast<uint16_t*>(pr.z);
@@ -547,6 +573,10 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         prm.r_boxes = lay.r_boxes;
         if (flags & gb::kFlagWide) prm.d_boxes *= 2;  // counted in 32x32 boxes
         prm.r_warp_bytes = static_cast<uint32_t>(lay.r_boxes) * V::r_slot_bytes(flags);
+        const uint32_t smem = V::S::smem_bytes(prm.stages, prm.d_boxes, prm.r_boxes, V::r_slot_bytes(flags));
+        if (smem > info.smem_optin)
+            return fail(GB_ERR_UNSUPPORTED, "shared memory layout (%d stages, %d/%d boxes) needs %u bytes, device allows %zu",
+                        prm.stages, lay.d_boxes, lay.r_boxes, smem, info.smem_optin);
     }
 
     const uint32_t b_rows = static_cast<uint32_t>(V::S::kBBox);
@@ -598,7 +628,8 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     // them (with fewer, one warpgroup would idle); off for long K, where sharing
     // every tile's chunks is 2.5-7.5 % faster.
     const bool pp_auto = prm.kb_per_split <= 4 && work >= 4 * units;
-    prm.pingpong = (V::kEpi == 2 && splits == 1 && (cfg.pingpong == 1 || (cfg.pingpong < 0 && pp_auto))) ? 1 : 0;
+    prm.pingpong = (V::kEpi == 4 || (V::kEpi == 2 && splits == 1 && (cfg.pingpong == 1 || (cfg.pingpong < 0 && pp_auto))))
+                       ? 1 : 0;
 
     char plan[420];
     snprintf(plan, sizeof plan,
@@ -689,7 +720,19 @@ gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitR
                                 !z_rows_aligned || ((pr.r || pr.z) && kb < 64);
     if (cfg.pingpong == 1 && cfg.epi == 1)
         return fail(GB_ERR_INVALID_ARG, "pingpong=1 needs two epilogue warpgroups (epi=2)");
-    const int epi = cfg.pingpong == 1 ? 2 : cfg.epi > 0 ? cfg.epi : (heavy_epilogue ? 2 : 1);
+    // Four epilogue warpgroups (lean kernel: paired path only): linear with an aligned
+    // epilogue input, an aligned D, no second output, 256-wide tiles on CTA pairs.
+    const bool lean_ok = !pr.ffn && !pr.dact && pr.r && !pr.z && r_rows_aligned && d_rows_aligned && kb > 0 &&
+                         pair && bn == 256;
+    // By default for work items of at most 4 k-blocks (the epilogue is the whole cost) over
+    // at least two tiles per CTA pair: measured on GB300, K = 64 residual 8191x12288,
+    // 0.121 -> 0.100 ms against two warpgroups.  Longer K wants the deeper operand ring
+    // that sixteen warps' queues leave no room for (K = 1024: 0.080 against 0.102 ms).
+    const bool lean_auto = lean_ok && kb <= 4 && tiles_est >= info.sms && cfg.pingpong != 0;
+    int epi = cfg.pingpong == 1 ? 2 : cfg.epi > 0 ? cfg.epi : lean_auto ? 4 : (heavy_epilogue ? 2 : 1);
+    if (epi == 4 && !lean_ok) epi = 2;
+    if (epi == 4)
+        return plan_and_launch<Variant<256, 1, 4, true, 4>>(pr, cfg, bn, dev, info, timeout_ns, inject, stream, sr);
     return epi == 2 ? dispatch<2>(pr, cfg, bn, pair, dev, info, timeout_ns, inject, stream, sr)
                     : dispatch<1>(pr, cfg, bn, pair, dev, info, timeout_ns, inject, stream, sr);
 }
@@ -1050,7 +1093,7 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "zigzag" && v >= -1 && v <= 1) c.zigzag = static_cast<int>(v);
             else if (key == "pair" && v >= -1 && v <= 1) c.pair = static_cast<int>(v);
             else if (key == "stages" && v >= 0 && v <= 16) c.stages = static_cast<int>(v);
-            else if (key == "epi" && v >= 0 && v <= 2) c.epi = static_cast<int>(v);
+            else if (key == "epi" && (v == 0 || v == 1 || v == 2 || v == 4)) c.epi = static_cast<int>(v);
             else if (key == "boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.boxes = static_cast<int>(v);
             else if (key == "pingpong" && v >= -1 && v <= 1) c.pingpong = static_cast<int>(v);
             else if (key == "hint_a" && v >= -1 && v <= 2) c.hint_a = static_cast<int>(v);

@@ -69,7 +69,12 @@ struct WarpLayout {
     static constexpr int kRegsEpilogue = 208;
     static_assert(!kRealloc || 128 * kRegsControl + 128 * EPI * kRegsEpilogue <= kThreads * kRegsLaunch,
                   "register budgets exceed the launch pool");
-    static_assert(EPI == 1 || EPI == 2, "one or two epilogue warpgroups");
+    static_assert(EPI == 1 || EPI == 2 || EPI == 4, "one, two or four epilogue warpgroups");
+    // Four epilogue warpgroups (lean variant, short-K residual work): only the paired
+    // epilogue path is compiled in, so the whole kernel fits the 96 registers a thread
+    // of a 640-thread block gets.  Warpgroups 2h and 2h + 1 serve the tiles of parity h
+    // (TMEM buffer h), each taking every other 64-column step.
+    static constexpr bool kLean = EPI == 4;
 };
 constexpr int kTmemCols = 512;    // two accumulator buffers of 256 columns
 constexpr int kAccStride = 256;
@@ -891,24 +896,24 @@ struct KernelShape {
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTxBytes = kCG * kStageBytes;  // bytes the leader's full barrier waits for
     static constexpr uint32_t kBarBytes = 2 * STAGES * 8 + kMaxBoxes * kEpiWarps * 8;  // ring + R barriers
-    // Layout: [barriers][control] in the first 1 KiB (fixed offsets, whatever the queue
-    // sizes), then [ring: stages x stage][D boxes: warps x d_boxes][R boxes: warps x r_boxes].
+    // Layout: [barriers][control] in the first 1 KiB or 2 (fixed offsets, whatever the
+    // queue sizes), then [ring: stages x stage][D boxes: warps x d_boxes][R boxes: warps x r_boxes].
     // `r_slot`, `d_slot`: bytes of one R / D queue entry (a 32x32 or 32x64 TMA box, or a
     // cp.async slot).
-    static constexpr uint32_t kCtlBytes = 1024;
+    static constexpr uint32_t kCtlBytes = (kBarBytes + sizeof(SharedCtl) + 1023) / 1024 * 1024;
     static constexpr uint32_t smem_bytes(int stages, int d_boxes, int r_boxes, uint32_t r_slot = kDStageBytes,
                                          uint32_t d_slot = kDStageBytes) {
         return 1024 /* alignment slack */ + kCtlBytes + stages * kStageBytes +
                static_cast<uint32_t>(kEpiWarps * d_boxes) * d_slot + static_cast<uint32_t>(kEpiWarps * r_boxes) * r_slot;
     }
-    static_assert(kBarBytes + sizeof(SharedCtl) <= kCtlBytes, "barriers and control block fit in their 1 KiB");
+    static_assert(kBarBytes + sizeof(SharedCtl) <= kCtlBytes, "barriers and control block fit in their block");
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kMmaN);
     static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * kCG;  // epilogue warps of every CTA in the pair
     // split-K counters per tile: one per epilogue warp of every CTA of the tile, laid out
     // for the most epilogue warps any variant of this tile shape has (two warpgroups), so
     // the workspace size does not depend on which epilogue layout a call picks
     static constexpr int kSlabs = 8 * kCG;
-    static_assert(kEpiWarps <= 8, "split-K counter layout");
+    static_assert(kEpiWarps <= 8 || W::kLean, "split-K counter layout (the lean variant has no split-K path)");
     static_assert(kMmaN <= kAccStride, "accumulator buffer holds at most 256 columns");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
     static_assert(kBRows % 8 == 0 && kBRows <= 256 && kMmaN % 16 == 0, "B operand rows");
@@ -955,7 +960,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);  // both CTAs of this pair
     const int32_t num_work = p.num_tiles * p.splits;
     // ping-pong takes effect with two epilogue warpgroups and no split only
-    const bool pingpong = kEpiGroups == 2 && p.pingpong != 0 && p.splits == 1;
+    const bool pingpong = W::kLean || (kEpiGroups == 2 && p.pingpong != 0 && p.splits == 1);
+    constexpr int kGroupsPerBuffer = W::kLean ? 2 : 1;  // with ping-pong: warpgroups serving one TMEM buffer
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < stages; ++s) {
@@ -967,7 +973,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             mbar_init(smem_addr(&ctl->acc_full[b]), 1);
             // every epilogue warp of the pair frees a buffer; with ping-pong only the
             // warpgroup that owns it
-            mbar_init(smem_addr(&ctl->acc_empty[b]), pingpong ? S::kAccEmptyArrivals / kEpiGroups
+            mbar_init(smem_addr(&ctl->acc_empty[b]), pingpong ? S::kAccEmptyArrivals / kEpiGroups * kGroupsPerBuffer
                                                               : S::kAccEmptyArrivals);
         }
         mbar_init(smem_addr(&ctl->drain), 1);
@@ -1258,10 +1264,12 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         const int q = e & 3;              // == warp % 4: this warp's TMEM lane quadrant
         const int g = e >> 2;             // this warp's warpgroup among the epilogue warpgroups
         // Chunks of a tile this warp stores: g, g + kEpiGroups, ... when the warpgroups
-        // share every tile; all of them, on every other tile, with ping-pong.
+        // share every tile; all of them, on every other tile, with ping-pong (lean variant:
+        // g % 2, g % 2 + 2, ... on the tiles of parity g / 2).
         const bool pp = pingpong;
-        const int c0 = pp ? 0 : g;
-        const int cstep = pp ? 1 : kEpiGroups;
+        const int owner = W::kLean ? g >> 1 : g;  // with ping-pong: the tile parity this warp serves
+        const int c0 = pp ? (W::kLean ? (g & 1) : 0) : g;
+        const int cstep = pp ? kGroupsPerBuffer : kEpiGroups;
         constexpr int kChunks = BN / kDChunk;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const int32_t slab_row = static_cast<int32_t>(rank) * kBM + q * 32 + lane;  // row within the tile
@@ -1308,7 +1316,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         int32_t r_islot = 0, r_uslot = 0;                 // queue positions of the next load and the next use
         auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
             while (rc_w < num_work) {
-                if (pp && (rc_local & 1) != g) {  // the other warpgroup's work item
+                if (pp && (rc_local & 1) != owner) {  // the other warpgroup's work item
                     rc_w += units;
                     ++rc_local;
                     continue;
@@ -1381,7 +1389,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             for (int i = 0; i < p.r_boxes; ++i) r_issue();
 
         for (int32_t w = unit; w < num_work; w += units, ++local) {
-            if (pp && (local & 1) != g) continue;  // the other warpgroup's tile
+            if (pp && (local & 1) != owner) continue;  // the other warpgroups' tile
             const uint32_t b = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
             bool ok = true;
@@ -1406,87 +1414,89 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             const int32_t m = row0 + lane;
             const bool warp_rows = row0 < p.m;
             const uint32_t tcol = tmem_base + lane_base + b * kAccStride;
-            if (express) {
-                // Express path (no epilogue input, no second output, TMA-stored D, no
-                // split): a compact loop, so the hot epilogue code next to the MMA
-                // issuer stays small.
+            if constexpr (!W::kLean) {
+                if (express) {
+                    // Express path (no epilogue input, no second output, TMA-stored D, no
+                    // split): a compact loop, so the hot epilogue code next to the MMA
+                    // issuer stays small.
 #pragma unroll 1
-                for (int c = c0; c < kChunks; c += cstep) {
-                    const int32_t n0 = nb * BN + c * kDChunk;
-                    const bool chunk_on = warp_rows && n0 < p.n;
-                    float v[32];
-                    GB_TR_T0(tx);
-                    if (chunk_on) {
-                        uint32_t r0[32];
-                        tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
-                        if (NUM_B == 2) {
-                            uint32_t r1[32];
-                            tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
-                            tmem_wait_ld();
+                    for (int c = c0; c < kChunks; c += cstep) {
+                        const int32_t n0 = nb * BN + c * kDChunk;
+                        const bool chunk_on = warp_rows && n0 < p.n;
+                        float v[32];
+                        GB_TR_T0(tx);
+                        if (chunk_on) {
+                            uint32_t r0[32];
+                            tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
+                            if (NUM_B == 2) {
+                                uint32_t r1[32];
+                                tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
+                                tmem_wait_ld();
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
-                        } else {
-                            tmem_wait_ld();
+                                for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                            } else {
+                                tmem_wait_ld();
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                            }
                         }
-                    }
-                    if (c + cstep >= kChunks) {
-                        tc_fence_before_sync();
+                        if (c + cstep >= kChunks) {
+                            tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
+                                else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                            }
+                        }
+                        GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
+                        if (!chunk_on) continue;
+                        if (NUM_B == 1) {
+                            if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
+                            switch (p.act) {
+                                case 1:
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                                    break;
+                                case 2:
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                                    break;
+                                case 3:
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                                    break;
+                                default:
+                                    break;
+                            }
+                        }
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                        GB_TR_ADD(tr_ep, kTrEpMath, tx);
+                        const uint32_t buf = dbox + dslot * kDStageBytes;
+                        if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
+                        __syncwarp();
+                        GB_TR_ADD(tr_ep, kTrEpDBox, tx);
+                        const uint32_t row_addr = buf + lane * 64;
+                        const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
+                                         packed[4 * u + 3]);
+                        fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
-                            else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                            tma_store_op(&p.tm_d, buf, n0, row0, p.hint_d);
+                            bulk_commit_group();
                         }
-                    }
-                    GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
-                    if (!chunk_on) continue;
-                    if (NUM_B == 1) {
-                        if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
-                        switch (p.act) {
-                            case 1:
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
-                                break;
-                            case 2:
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
-                                break;
-                            case 3:
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
-                                break;
-                            default:
-                                break;
-                        }
-                    }
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                    GB_TR_ADD(tr_ep, kTrEpMath, tx);
-                    const uint32_t buf = dbox + dslot * kDStageBytes;
-                    if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
-                    __syncwarp();
-                    GB_TR_ADD(tr_ep, kTrEpDBox, tx);
-                    const uint32_t row_addr = buf + lane * 64;
-                    const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
-                                     packed[4 * u + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_op(&p.tm_d, buf, n0, row0, p.hint_d);
-                        bulk_commit_group();
-                    }
-                    if (++dslot == p.d_boxes) dslot = 0;
-                    GB_TR_ADD(tr_ep, kTrEpStore, tx);
+                        if (++dslot == p.d_boxes) dslot = 0;
+                        GB_TR_ADD(tr_ep, kTrEpStore, tx);
 #ifdef GB_TRACE
-                    if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+                        if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
+                    }
+                    continue;
                 }
-                continue;
             }
             if constexpr (NUM_B == 1) {
                 if (paired) {
@@ -1623,115 +1633,117 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 }
             }
 
-            const bool split_mode = p.splits > 1;
-            // this slab's rows of the tile's fp32 accumulator (split-K only)
-            float* acc_ws = p.ws + static_cast<int64_t>(tile) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
+            if constexpr (!W::kLean) {
+                const bool split_mode = p.splits > 1;
+                // this slab's rows of the tile's fp32 accumulator (split-K only)
+                float* acc_ws = p.ws + static_cast<int64_t>(tile) * NUM_B * kPartFloats + static_cast<int64_t>(slab_row) * BN;
 
 #pragma unroll 1
-            for (int c = c0; c < kChunks; c += cstep) {
-                const int32_t n0 = nb * BN + c * kDChunk;
-                const bool chunk_on = warp_rows && n0 < p.n;
-                float v[32];
-                GB_TR_T0(tg);
+                for (int c = c0; c < kChunks; c += cstep) {
+                    const int32_t n0 = nb * BN + c * kDChunk;
+                    const bool chunk_on = warp_rows && n0 < p.n;
+                    float v[32];
+                    GB_TR_T0(tg);
 #ifdef GB_TRACE
-                if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+                    if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
-                if (chunk_on && p.num_k_blocks > 0) {
-                    uint32_t r0[32];
-                    tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
-                    if (NUM_B == 2) {
-                        uint32_t r1[32];
-                        tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
-                        tmem_wait_ld();
-                        if (split_mode) {
-                            if (m < p.m) {
-                                red_add_f32x32(acc_ws + c * kDChunk, r0);
-                                red_add_f32x32(acc_ws + kPartFloats + c * kDChunk, r1);
+                    if (chunk_on && p.num_k_blocks > 0) {
+                        uint32_t r0[32];
+                        tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
+                        if (NUM_B == 2) {
+                            uint32_t r1[32];
+                            tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
+                            tmem_wait_ld();
+                            if (split_mode) {
+                                if (m < p.m) {
+                                    red_add_f32x32(acc_ws + c * kDChunk, r0);
+                                    red_add_f32x32(acc_ws + kPartFloats + c * kDChunk, r1);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
                             }
                         } else {
+                            tmem_wait_ld();
+                            if (split_mode) {
+                                if (m < p.m) red_add_f32x32(acc_ws + c * kDChunk, r0);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                            }
                         }
                     } else {
-                        tmem_wait_ld();
-                        if (split_mode) {
-                            if (m < p.m) red_add_f32x32(acc_ws + c * kDChunk, r0);
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                    }
+                    if (c + cstep >= kChunks) {
+                        // This warp's TMEM reads of this buffer are done: hand it back to the MMA issuer.
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
+                            else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
                         }
                     }
-                } else {
+                    GB_TR_ADD(tr_ep, kTrEpTmemLd, tg);
+                    if (!chunk_on || split_mode) continue;
+                    uint32_t rbox = 0;
+                    if (r_queue) {
+                        const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
+                        const uint32_t par = (r_phase >> r_uslot) & 1u;
+                        bool rok = true;
+                        if (lane == 0) rok = wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot);
+                        rok = __shfl_sync(0xffffffffu, rok, 0);
+                        if (!rok) break;
+                        while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the slot's data
+                        }
+                        r_phase ^= 1u << r_uslot;
+                        rbox = rbox0 + r_uslot * r_slot;
+                    }
+                    GB_TR_ADD(tr_ep, kTrEpRWait, tg);
+#ifdef GB_TRACE
+                    finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r, tr_ep);
+#else
+                    finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r);
+#endif
+                    if (r_queue) {
+                        __syncwarp();  // every lane has read the box: refill it
+                        if (r_tma) fence_proxy_async_smem();
+                        --r_pending;
+                        if (++r_uslot == p.r_boxes) r_uslot = 0;
+                        r_issue();
+                    }
+                }
+                if (*abort_flag) break;
+                if (!split_mode || !warp_rows) continue;
+
+                // split-K: this partial is in the accumulator; the last split of the slab finishes it.
+                __threadfence();
+                __syncwarp();
+                uint32_t* cnt = p.ws_cnt + tile * S::kSlabs + static_cast<int32_t>(rank) * kEpiWarps + e;
+                uint32_t arrived = 0;
+                if (lane == 0) arrived = atomicAdd(cnt, 1u);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived != static_cast<uint32_t>(p.splits - 1)) continue;
+                __threadfence();
+#pragma unroll 1
+                for (int c = c0; c < kChunks; c += cstep) {
+                    const int32_t n0 = nb * BN + c * kDChunk;
+                    if (n0 >= p.n) break;
+                    float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                }
-                if (c + cstep >= kChunks) {
-                    // This warp's TMEM reads of this buffer are done: hand it back to the MMA issuer.
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
-                        else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                    add_f32x32_cg(v, acc_ws + c * kDChunk);
+                    if (NUM_B == 2) {
+                        float v3[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v3[j] = 0.0f;
+                        add_f32x32_cg(v3, acc_ws + kPartFloats + c * kDChunk);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = silu(v[j]) * v3[j];
                     }
+                    finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, 0u, tbuf_r);
                 }
-                GB_TR_ADD(tr_ep, kTrEpTmemLd, tg);
-                if (!chunk_on || split_mode) continue;
-                uint32_t rbox = 0;
-                if (r_queue) {
-                    const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
-                    const uint32_t par = (r_phase >> r_uslot) & 1u;
-                    bool rok = true;
-                    if (lane == 0) rok = wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot);
-                    rok = __shfl_sync(0xffffffffu, rok, 0);
-                    if (!rok) break;
-                    while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the slot's data
-                    }
-                    r_phase ^= 1u << r_uslot;
-                    rbox = rbox0 + r_uslot * r_slot;
-                }
-                GB_TR_ADD(tr_ep, kTrEpRWait, tg);
-#ifdef GB_TRACE
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r, tr_ep);
-#else
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, rbox, tbuf_r);
-#endif
-                if (r_queue) {
-                    __syncwarp();  // every lane has read the box: refill it
-                    if (r_tma) fence_proxy_async_smem();
-                    --r_pending;
-                    if (++r_uslot == p.r_boxes) r_uslot = 0;
-                    r_issue();
-                }
-            }
-            if (*abort_flag) break;
-            if (!split_mode || !warp_rows) continue;
-
-            // split-K: this partial is in the accumulator; the last split of the slab finishes it.
-            __threadfence();
-            __syncwarp();
-            uint32_t* cnt = p.ws_cnt + tile * S::kSlabs + static_cast<int32_t>(rank) * kEpiWarps + e;
-            uint32_t arrived = 0;
-            if (lane == 0) arrived = atomicAdd(cnt, 1u);
-            arrived = __shfl_sync(0xffffffffu, arrived, 0);
-            if (arrived != static_cast<uint32_t>(p.splits - 1)) continue;
-            __threadfence();
-#pragma unroll 1
-            for (int c = c0; c < kChunks; c += cstep) {
-                const int32_t n0 = nb * BN + c * kDChunk;
-                if (n0 >= p.n) break;
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                add_f32x32_cg(v, acc_ws + c * kDChunk);
-                if (NUM_B == 2) {
-                    float v3[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v3[j] = 0.0f;
-                    add_f32x32_cg(v3, acc_ws + kPartFloats + c * kDChunk);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = silu(v[j]) * v3[j];
-                }
-                finish_chunk<NUM_B>(p, v, m, row0, n0, lane, dbox, dslot, 0u, tbuf_r);
             }
         }
 #ifdef GB_TRACE

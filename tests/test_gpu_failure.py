@@ -53,3 +53,33 @@ def test_wait_timeout_is_reported_and_context_survives(kind, pair, epi, extra):
         gb.device_status()
         assert_close(bits(D), oracle.ffn_gated(bits(A), bits(B), bits(B3)), "after timeout")
     gb.set_config(None)
+
+
+@pytest.mark.parametrize("spec", ["epi=4", "epi=4,wide=0", "epi=2,wide=1", "epi=2,pingpong=1,wide=0"])
+def test_wait_timeout_with_epilogue_input_queues(spec):
+    """A residual launch whose R boxes are in flight when the waits run out (paired
+    path, 32x32 and 32x64 boxes, two and four epilogue warpgroups): the epilogue drains
+    its R loads before it returns and the context stays usable."""
+    M, N, K = 600, 1024, 128
+    A = inputs.randn_bf16((M, K), seed=4).cuda()
+    B = inputs.randn_bf16((N, K), seed=5, std=1.0 / np.sqrt(K)).cuda()
+    R = inputs.randn_bf16((M, N), seed=6).cuda()
+    gb.device_status()
+    gb.set_config(spec)
+    gb.set_wait_timeout_ns(100_000_000)  # 0.1 s
+    gb.set_fault_injection(1)
+    try:
+        gb.linear(A, B, None, R)
+        with pytest.raises(gb.GBError) as ei:
+            gb.device_status()
+        assert ei.value.status == 4, str(ei.value)
+    finally:
+        gb.set_fault_injection(0)
+        gb.set_wait_timeout_ns(0)
+    gb.device_status()
+    D = gb.linear(A, B, None, R)
+    gb.device_status()
+    plan = gb.last_plan()
+    gb.set_config(None)
+    assert f"epi={spec.split('epi=')[1][0]}" in plan, plan
+    assert_close(bits(D), oracle.linear(bits(A), bits(B), None, bits(R)), f"after timeout {spec}")

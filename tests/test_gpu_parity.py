@@ -506,7 +506,8 @@ def test_short_k_plan_takes_deep_queues():
     D = gb.linear(Ab, Bb, None, Rb)
     gb.device_status()
     big = gb.last_plan()
-    assert "pingpong=1" in big and "stages=2" in big and "tma.64x32" in big, big
+    # ... on the lean kernel: four epilogue warpgroups, 32x32 boxes, a 2-stage ring
+    assert "pingpong=1" in big and "epi=4" in big and "stages=2" in big and "boxes=2/3" in big, big
     assert torch.equal(D.view(torch.int16), Rb.view(torch.int16))
 
 
@@ -634,3 +635,53 @@ def test_wide_boxes_identical_bits(spec):
         assert_bitexact(got, base, f"{spec} {M}x{N}x{K}")
         if (M, N, K) == (700, 904, 64):
             assert_close(got, ref_linear(A, B, bias, R, "gelu_tanh"), spec)
+
+
+@pytest.mark.parametrize("spec", ["epi=4", "epi=4,wide=0", "epi=4,grid=4", "epi=4,stages=2,r_boxes=4",
+                                  "epi=4,boxes=2", "epi=4,r_boxes=2,grid=2", "epi=4,hint_r=1,hint_d=1"])
+def test_four_epilogue_warpgroups_identical_bits(spec):
+    """The lean kernel (four epilogue warpgroups, paired path only; warpgroups 2h, 2h + 1
+    serve the tiles of parity h): identical bits to the two-warpgroup kernel on ragged
+    residual shapes with bias and activation, short and long K."""
+    for M, N, K in [(700, 904, 64), (513, 1320, 200), (300, 264, 64), (2100, 2048, 64), (64, 512, 1000)]:
+        A = inputs.randn_bf16((M, K), seed=M + 21)
+        B = inputs.randn_bf16((N, K), seed=N + 22, std=0.1)
+        bias = inputs.randn_bf16((N,), seed=23, std=0.1)
+        R = inputs.randn_bf16((M, N), seed=24)
+        gb.set_config("epi=2")
+        base = run_linear(A, B, bias, R, "silu")
+        gb.set_config(spec)
+        got = run_linear(A, B, bias, R, "silu")
+        plan = gb.last_plan()
+        gb.set_config(None)
+        if M > 128:
+            assert "epi=4" in plan and "pingpong=1" in plan, plan
+        assert_bitexact(got, base, f"{spec} {M}x{N}x{K}")
+        if (M, N, K) == (700, 904, 64):
+            assert_close(got, ref_linear(A, B, bias, R, "silu"), spec)
+
+
+def test_four_epilogue_warpgroups_fall_back():
+    """epi=4 where the lean kernel does not apply runs the two-warpgroup kernel: no
+    epilogue input, an unaligned R, a split-K plan, single CTAs, the FFN."""
+    M, N, K = 300, 512, 512
+    A = inputs.randn_bf16((M, K), seed=31)
+    B = inputs.randn_bf16((N, K), seed=32, std=0.05)
+    R = inputs.randn_bf16((M, N), seed=33)
+    gb.set_config("epi=4")
+    d = run_linear(A, B)
+    assert "epi=2" in gb.last_plan(), gb.last_plan()
+    assert_close(d, ref_linear(A, B), "no R")
+    Rbig = inputs.randn_bf16((M, N + 1), seed=34)
+    d = gb.linear(A.to(DEV), B.to(DEV), None, Rbig.to(DEV)[:, 1:])
+    gb.device_status()
+    assert "epi=2" in gb.last_plan(), gb.last_plan()
+    assert_close(bits(d), ref_linear(A, B, None, Rbig[:, 1:].contiguous()), "unaligned R")
+    d = gb.linear(A.to(DEV), B.to(DEV), None, R.to(DEV), split_k=4)
+    gb.device_status()
+    assert "epi=2" in gb.last_plan() and "splits=4" in gb.last_plan(), gb.last_plan()
+    assert_close(bits(d), ref_linear(A, B, None, R), "split")
+    gb.set_config("epi=4,pair=0")
+    d = run_linear(A, B, None, R)
+    assert "epi=2" in gb.last_plan() and "pair=0" in gb.last_plan(), gb.last_plan()
+    assert_close(d, ref_linear(A, B, None, R), "single CTAs")
