@@ -299,12 +299,14 @@ GB_API gb_status_t gb_last_plan(char* buf, size_t len);
 /*
  * Timing trace, for a library built with -DGB_TRACE (the normal build returns
  * GB_ERR_UNSUPPORTED).  `buf` is device memory of the caller (NULL turns the
- * trace off).  Every later launch whose grid fits (16 unsigned 64-bit words per
+ * trace off).  Every later launch whose grid fits (32 unsigned 64-bit words per
  * CTA) writes one record per CTA: %globaltimer at entry, after set-up, at the
- * first MMA, at the last accumulator commit and at the end of the epilogue, and
- * the SM clock cycles the producer, the MMA issuer and the first epilogue warp
- * spent blocked on their barriers (with the number of blocked waits).  The layout
- * is kTrace* in gemm_kernel.cuh.
+ * first MMA, at the last accumulator commit and at the end of the epilogue; the
+ * SM clock cycles the producer, the MMA issuer and the first epilogue warp spent
+ * blocked on their barriers (with the number of blocked waits); the first
+ * epilogue warp's cycles per phase of its chunk loop (free D boxes, TMEM loads, R
+ * waits, math, stores, R issue) and its step count; and a histogram of the MMA
+ * issuer's k-block-to-k-block intervals.  The layout is kTrace* in gemm_kernel.cuh.
  */
 GB_API gb_status_t gb_set_trace_buffer(void* buf, size_t bytes);
 
