@@ -1571,11 +1571,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                 // this chunk's (step's) R box: the one at the use position of the queue
                                 const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
                                 const uint32_t par = (r_phase >> r_uslot) & 1u;
-                                if (lane == 0) rok = wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot);
-                                rok = __shfl_sync(0xffffffffu, rok, 0);
+                                // every lane waits (and so acquires the TMA data) itself: no lane-0
+                                // branch and broadcast on the per-step path
+                                rok = __all_sync(0xffffffffu,
+                                                 wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot));
                                 if (!rok) break;
-                                while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the TMA data
-                                }
                                 r_phase ^= 1u << r_uslot;
                                 rcur = rbox0 + r_uslot * r_slot;
                                 --r_pending;
@@ -1692,11 +1692,10 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const uint32_t bar = smem_addr(&rbar[e * kMaxBoxes + r_uslot]);
                         const uint32_t par = (r_phase >> r_uslot) & 1u;
                         bool rok = true;
-                        if (lane == 0) rok = wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot);
-                        rok = __shfl_sync(0xffffffffu, rok, 0);
+                        // every lane waits (and so acquires the slot's data) itself
+                        rok = __all_sync(0xffffffffu,
+                                         wait_bar(bar, par, abort_flag, p.timeout_ns, kRoleEpilogue, 0x200u | r_uslot));
                         if (!rok) break;
-                        while (!mbar_try_wait(bar, par)) {  // completed: every lane acquires the slot's data
-                        }
                         r_phase ^= 1u << r_uslot;
                         rbox = rbox0 + r_uslot * r_slot;
                     }
