@@ -66,7 +66,7 @@ struct Config {
     int prod = 0;        // producer threads: 0 auto, 1 or 2 (A and B loads issued by different warps)
     int r_async = -1;    // unaligned R rows (no split): -1 auto, 0 synchronous loads at use, 1 cp.async queue
     int r_boxes = 0;     // R queue depth per epilogue warp: 0 = heuristic, 2..8
-    int wide = -1;       // 32x64 R/D boxes on the paired epilogue path: -1 auto, 0 off, 1 on
+    int wide = -1;       // 32x64 boxes on the paired epilogue path: -1 auto, 0 off, 1 R and D, 2 D only
 };
 
 std::mutex g_cfg_mu;
@@ -272,7 +272,7 @@ struct Variant {
                                                                                           : gb::kDStageBytes;
     }
     static uint32_t d_slot_bytes(uint32_t flags) {
-        return (flags & gb::kFlagWide) ? gb::kWideBoxBytes : gb::kDStageBytes;
+        return (flags & (gb::kFlagWide | gb::kFlagWideD)) ? gb::kWideBoxBytes : gb::kDStageBytes;
     }
     static Layout choose_layout(int kb_per_item, int r_mode, uint32_t flags, const Config& cfg, size_t smem_optin) {
         const bool short_k = kb_per_item <= 4;
@@ -283,18 +283,19 @@ struct Variant {
         auto r_of = [&](int b) { return r_mode == 2 ? (cfg.r_boxes > 0 ? rq : b) : r_mode == 3 ? rq : (r_mode == 1 ? 2 : 0); };
         const uint32_t rs = r_slot_bytes(flags), ds = d_slot_bytes(flags);
         if (kEpi == 4) {
-            // Sixteen epilogue warps: per-warp queues must be short to fit.  Wide boxes:
-            // one D box and one R box per warp (the other warps of the SM hide each one's
-            // waits); 32x32 boxes: two D and three R.  A 2-stage ring unless asked.
-            const bool wide = flags & gb::kFlagWide;
-            const int lst = std::max(2, cfg.stages > 0 ? std::min(cfg.stages, STAGES) : 2);
-            int ld = cfg.boxes > 0 ? cfg.boxes : (wide ? 1 : 2);
-            int lr = cfg.r_boxes > 0 ? cfg.r_boxes : (wide ? 1 : 3);
-            const int lmin = wide ? 1 : 2;
-            while (lr > lmin && S::smem_bytes(lst, ld, lr, rs, ds) > smem_optin) --lr;
-            while (ld > lmin && S::smem_bytes(lst, ld, lr, rs, ds) > smem_optin) --ld;
+            // Sixteen epilogue warps: per-warp queues must be short to fit.  32x64 D and R
+            // boxes: one of each per warp (the other warps of the SM hide each one's waits);
+            // 32x64 D and 32x32 R boxes: one D and three R; 32x32 boxes: two D and three R.
+            // A 2-stage ring unless asked.
+            const bool wide_d = flags & (gb::kFlagWide | gb::kFlagWideD), wide_r = flags & gb::kFlagWide;
+            const int lst = cfg.stages > 0 ? std::min(cfg.stages, STAGES) : 2;
+            int ld = cfg.boxes > 0 ? cfg.boxes : (wide_d ? 1 : 2);
+            int lr = cfg.r_boxes > 0 ? cfg.r_boxes : (wide_r ? 1 : 3);
+            const int dmin = wide_d ? 1 : 2, rmin = wide_r ? 1 : 2;
+            while (lr > rmin && S::smem_bytes(lst, ld, lr, rs, ds) > smem_optin) --lr;
+            while (ld > dmin && S::smem_bytes(lst, ld, lr, rs, ds) > smem_optin) --ld;
             int ls = lst;
-            while (ls > 2 && S::smem_bytes(ls, ld, lr, rs, ds) > smem_optin) --ls;
+            while (ls > 1 && S::smem_bytes(ls, ld, lr, rs, ds) > smem_optin) --ls;
             return Layout{ls, ld, lr};
         }
         if (short_k && (flags & gb::kFlagWide) && cfg.stages <= 0 && cfg.boxes <= 0 && cfg.r_boxes <= 0) {
@@ -555,11 +556,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     const bool paired = r_tma && pr.k > 0 && d_tma && !pr.z;
     const int groups = V::kEpi;
     const bool wide_fits = (V::kBN / gb::kDChunk) % (2 * groups) == 0;
-    // (the four-warpgroup kernel defaults to 32x32 boxes: sixteen warps' queues of wide
-    // boxes leave room for one D and one R box each, measured 7 % slower than two and three
-    // 32x32 boxes)
-    const bool wide_default = V::kEpi != 4;
-    if (paired && wide_fits && (cfg.wide == 1 || (cfg.wide < 0 && wide_default))) flags |= gb::kFlagWide;
+    // The four-warpgroup kernel defaults to 32x64 D boxes with 32x32 R boxes (`wide=2`):
+    // sixteen warps' queues of 32x64 R boxes leave room for one R box each (measured 7 %
+    // slower than three 32x32 R boxes).
+    const int wide_mode = cfg.wide >= 0 ? cfg.wide : (V::kEpi == 4 ? 2 : 1);
+    if (paired && wide_fits && wide_mode == 1) flags |= gb::kFlagWide;
+    if (paired && wide_fits && wide_mode == 2) flags |= gb::kFlagWideD;
     const bool z_tma = pr.z && aligned16(pr.z) && pr.ldz % 8 == 0;
     if (!pr.ffn && pr.z) flags |= gb::kFlagZ | (z_tma ? gb::kFlagZTma : 0u);
     prm.z = static_cast<uint16_t*>(pr.z);
@@ -571,7 +573,7 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         prm.stages = lay.stages;
         prm.d_boxes = lay.d_boxes;
         prm.r_boxes = lay.r_boxes;
-        if (flags & gb::kFlagWide) prm.d_boxes *= 2;  // counted in 32x32 boxes
+        if (flags & (gb::kFlagWide | gb::kFlagWideD)) prm.d_boxes *= 2;  // counted in 32x32 boxes
         prm.r_warp_bytes = static_cast<uint32_t>(lay.r_boxes) * V::r_slot_bytes(flags);
         const uint32_t smem = V::S::smem_bytes(prm.stages, prm.d_boxes, prm.r_boxes, V::r_slot_bytes(flags));
         if (smem > info.smem_optin)
@@ -600,12 +602,12 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
                                       CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
             return st;
     }
-    const bool wide = flags & gb::kFlagWide;
-    const uint32_t box_n = wide ? 2 * gb::kDChunk : gb::kDChunk;
-    const CUtensorMapSwizzle box_sw = wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (d_tma && (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, box_n, 32, box_sw)) != GB_OK)
+    const bool wide = flags & gb::kFlagWide, wide_d = flags & (gb::kFlagWide | gb::kFlagWideD);
+    auto box_n = [](bool w) { return w ? 2 * gb::kDChunk : gb::kDChunk; };
+    auto box_sw = [](bool w) { return w ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B; };
+    if (d_tma && (st = make_tmap(&prm.tm_d, pr.d, pr.n, pr.m, pr.ldd * 2, box_n(wide_d), 32, box_sw(wide_d))) != GB_OK)
         return st;
-    if (r_tma && (st = make_tmap(&prm.tm_r, pr.r, pr.n, pr.m, pr.ldr * 2, box_n, 32, box_sw)) != GB_OK)
+    if (r_tma && (st = make_tmap(&prm.tm_r, pr.r, pr.n, pr.m, pr.ldr * 2, box_n(wide), 32, box_sw(wide))) != GB_OK)
         return st;
     if (z_tma &&
         (st = make_tmap(&prm.tm_z, pr.z, pr.n, pr.m, pr.ldz * 2, gb::kDChunk, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != GB_OK)
@@ -640,10 +642,10 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
              prm.pingpong,
              V::kTileM, bn, gb::kBK,
              prm.stages,
-             (flags & gb::kFlagWide) ? prm.d_boxes / 2 : prm.d_boxes, prm.r_boxes,
+             wide_d ? prm.d_boxes / 2 : prm.d_boxes, prm.r_boxes,
              static_cast<long long>(units * (V::kPair ? (mc ? 4 : 2) : 1)), prm.num_tiles, prm.num_k_blocks, splits,
              prm.group_m, prm.zigzag, prm.prod, prm.hint_a, prm.hint_b, prm.hint_r, prm.hint_d,
-             d_tma ? (wide ? "tma.64x32" : "tma") : "st.transposed",
+             d_tma ? (wide_d ? "tma.64x32" : "tma") : "st.transposed",
              pr.r ? (r_tma ? (wide ? "tma.64x32" : "tma") : r_async ? "cp.async" : (flags & gb::kFlagRVec) ? "ld.v4"
                                                                                                   : "ld.transposed")
                   : "none",
@@ -1106,7 +1108,7 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "prod" && v >= 0 && v <= 3) c.prod = static_cast<int>(v);
             else if (key == "r_async" && v >= -1 && v <= 1) c.r_async = static_cast<int>(v);
             else if (key == "r_boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.r_boxes = static_cast<int>(v);
-            else if (key == "wide" && v >= -1 && v <= 1) c.wide = static_cast<int>(v);
+            else if (key == "wide" && v >= -1 && v <= 2) c.wide = static_cast<int>(v);
             else return fail(GB_ERR_INVALID_ARG, "unknown config key or value: %s=%ld", key.c_str(), v);
             s += len;
             if (*s == ',') ++s;

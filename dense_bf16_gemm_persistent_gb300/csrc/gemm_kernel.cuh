@@ -100,6 +100,8 @@ enum : uint32_t {
                          // shared-memory slots, prefetched ahead of use like the TMA boxes
     kFlagWide = 2048u,   // paired path with 32x64 R and D boxes (128-byte swizzle): one TMA load, one
                          // TMA store, one barrier wait and one fence per 64 columns
+    kFlagWideD = 4096u,  // paired path with 32x64 D boxes and 32x32 R boxes (the two chunks of a
+                         // step adjacent; one TMA store and one fence per 64 columns)
 };
 constexpr uint32_t kWideBoxBytes = 32 * 2 * kDChunk * 2;  // one warp's 32x64 bf16 box
 // One R slot of the cp.async queue: 32 rows x 17 words (a 32-column row segment that
@@ -183,7 +185,7 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
 // Bytes of one D / R queue entry of a launch: a 32x32 box, a 32x64 box (wide), or a
 // cp.async slot (unaligned R rows).
 __host__ __device__ __forceinline__ uint32_t d_slot_bytes(const GemmParams& p) {
-    return (p.flags & kFlagWide) ? kWideBoxBytes : kDStageBytes;
+    return (p.flags & (kFlagWide | kFlagWideD)) ? kWideBoxBytes : kDStageBytes;
 }
 __host__ __device__ __forceinline__ uint32_t r_slot_bytes(const GemmParams& p) {
     return (p.flags & kFlagRAsync) ? kRSlotAsyncBytes : (p.flags & kFlagWide) ? kWideBoxBytes : kDStageBytes;
@@ -1310,8 +1312,13 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
         // the steps starting at chunk 2g, 2g + 2 * groups, ... (all of them with ping-pong),
         // i.e. first chunk 2 * c0 and stride 2 * cstep.  The R cursor walks this warp's R
         // boxes: chunks, or the first chunks of wide steps.
+        // With 32x64 D boxes only (kFlagWideD) the steps are the same adjacent pairs but R
+        // still comes in 32x32 boxes: the cursor walks 2c0, 2c0 + 1, 2c0 + 2 cstep, ...
         const bool wide = (NUM_B == 1) && (p.flags & kFlagWide);
-        int32_t rc_w = unit, rc_local = 0, rc_c = wide ? 2 * c0 : c0, rc_mb = -1, rc_nb = -1;
+        const bool adj = (NUM_B == 1) && (p.flags & (kFlagWide | kFlagWideD));  // steps of adjacent chunks
+        int32_t rc_w = unit, rc_local = 0, rc_c = adj ? 2 * c0 : c0, rc_mb = -1, rc_nb = -1;
+        // the cursor's next R box after rc_c within a tile
+        auto rc_next = [&](int32_t c) { return wide ? c + 2 * cstep : adj ? ((c & 1) ? c + 2 * cstep - 1 : c + 1) : c + cstep; };
         uint32_t r_pending = 0, r_phase = 0;  // R boxes issued and not yet used; one parity bit per box
         int32_t r_islot = 0, r_uslot = 0;                 // queue positions of the next load and the next use
         auto r_find = [&]() -> bool {  // move the cursor to the next chunk this warp will store
@@ -1324,9 +1331,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 if (rc_mb < 0) work_tile(rc_w, p, pairi, rc_mb, rc_nb);
                 const int32_t r0 = rc_mb * S::kTileM + static_cast<int32_t>(rank) * kBM + q * 32;
                 if (rc_c < kChunks && r0 < p.m && rc_nb * BN + rc_c * kDChunk < p.n) return true;
-                rc_c += wide ? 2 * cstep : cstep;
+                rc_c = rc_next(rc_c);
                 if (rc_c >= kChunks) {
-                    rc_c = wide ? 2 * c0 : c0;
+                    rc_c = adj ? 2 * c0 : c0;
                     rc_w += units;
                     ++rc_local;
                     rc_mb = -1;
@@ -1377,9 +1384,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             }
             ++r_pending;
             if (++r_islot == p.r_boxes) r_islot = 0;
-            rc_c += wide ? 2 * cstep : cstep;
+            rc_c = rc_next(rc_c);
             if (rc_c >= kChunks) {
-                rc_c = wide ? 2 * c0 : c0;
+                rc_c = adj ? 2 * c0 : c0;
                 rc_w += units;
                 ++rc_local;
                 rc_mb = -1;
@@ -1508,10 +1515,11 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     // (cs = 1; pairs start at 2 * c0, 2 * c0 + 2 * cstep, ...) that share one
                     // 32x64 R box and one 32x64 D box (one TMA load, one store, one R wait);
                     // a box half past N is loaded as zeros and clipped by the store.
-                    const int cs = wide ? 1 : cstep;
+                    const bool wide_d = adj;  // 32x64 D boxes (with or without 32x64 R boxes)
+                    const int cs = adj ? 1 : cstep;
                     bool rok = true;
 #pragma unroll 1
-                    for (int c = wide ? 2 * c0 : c0; c < kChunks; c += 2 * cstep) {
+                    for (int c = adj ? 2 * c0 : c0; c < kChunks; c += 2 * cstep) {
                         const bool last = c + 2 * cstep >= kChunks;
                         const int nchunks = !(warp_rows && nb * BN + c * kDChunk < p.n) ? 0
                                             : (nb * BN + (c + cs) * kDChunk < p.n ? 2 : 1);
@@ -1519,7 +1527,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         if (nchunks > 0) {
                             // D boxes free (two, or one wide): the stores that last used them
                             // have read them
-                            if (lane == 0) bulk_wait_group_read_at_most(wide ? (p.d_boxes >> 1) - 1 : p.d_boxes - 2);
+                            if (lane == 0) bulk_wait_group_read_at_most(wide_d ? (p.d_boxes >> 1) - 1 : p.d_boxes - 2);
                             __syncwarp();
                         }
                         GB_TR_ADD(tr_ep, kTrEpDBox, tx);
@@ -1583,17 +1591,14 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             }
                             GB_TR_ADD(tr_ep, kTrEpRWait, tx);
                             uint32_t box = box_a;
-                            if (!wide || i == 0) {
+                            if (!wide_d || i == 0) {
                                 box = dbox + dslot * d_slot_bytes(p);
-                                if (++dslot == (wide ? p.d_boxes >> 1 : p.d_boxes)) dslot = 0;
+                                if (++dslot == (wide_d ? p.d_boxes >> 1 : p.d_boxes)) dslot = 0;
                             }
-                            if (wide) {
-                                apply_input_wide(p, v, rcur, i, lane);
-                                stage_wide_half(box, v, i, lane);
-                            } else {
-                                apply_input_box(p, v, rcur, lane);
-                                stage_box_row(box, v, lane);
-                            }
+                            if (wide) apply_input_wide(p, v, rcur, i, lane);
+                            else apply_input_box(p, v, rcur, lane);
+                            if (wide_d) stage_wide_half(box, v, i, lane);
+                            else stage_box_row(box, v, lane);
                             GB_TR_ADD(tr_ep, kTrEpMath, tx);
                             if (i == 0) {
                                 box_a = box;
@@ -1606,7 +1611,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             if (lane == 0) {
                                 tma_store_op(&p.tm_d, box_a, n0 - cs * kDChunk, row0, p.hint_d);
                                 bulk_commit_group();
-                                if (!wide) {
+                                if (!wide_d) {
                                     tma_store_op(&p.tm_d, box, n0, row0, p.hint_d);
                                     bulk_commit_group();
                                 }

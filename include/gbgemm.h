@@ -258,18 +258,28 @@ GB_API const char* gb_last_error(void);
  * group (tile-swizzle group size along M, >= 1), zigzag (0, 1, or -1 = auto),
  * pair (1 = CTA pairs with 256-row tiles, 0 = single CTAs with 128-row tiles,
  * -1 = auto; the 128-wide linear tile always runs on single CTAs), stages
- * (depth of the operand ring, >= 2; 0 = auto: the deepest that fits for
- * long K, 3 for work items of at most 4 k-blocks), boxes (D staging boxes and
- * TMA-loaded R boxes per epilogue warp, 2..8; 0 = auto: 2 for long K, the
- * deepest that fits for short K; boxes shrink before the ring does), epi
- * (epilogue warpgroups: 1 or 2; 0 = auto: two for epilogue-bound shapes),
+ * (depth of the operand ring, >= 2, or 1 on the lean kernel; 0 = auto: the deepest that fits for
+ * long K, 2-3 for work items of at most 4 k-blocks), boxes (D staging boxes
+ * and TMA-loaded R boxes per epilogue warp, 2..8; 0 = auto: 2 for long K, the
+ * deepest that fits for short K; boxes shrink before the ring does), r_boxes
+ * (the R queue's depth alone, 2..8; 0 = auto), epi (epilogue warpgroups: 1, 2
+ * or 4; 0 = auto: four for short-K residual work on CTA pairs with aligned
+ * rows, two for other epilogue-bound shapes, else one; 4 runs the lean kernel,
+ * which has only the paired epilogue path: other plans fall back to 2),
  * pingpong (1 = the two epilogue warpgroups alternate whole tiles, each owning
  * one TMEM accumulator buffer, instead of sharing every tile's chunks; implies
  * epi=2, GB_ERR_INVALID_ARG with epi=1 at the call, no effect with split-K;
- * 0 = never; -1 = auto: on for work items of at most 4 k-blocks), hint_a,
- * hint_b, hint_r, hint_d (L2 eviction policy of the TMA loads of A, of B / W1 /
- * W3, of R, and of the TMA stores of D and Z: 0 = none, 1 = evict first, 2 =
- * evict last, -1 = the built-in choice).
+ * 0 = never; -1 = auto: on for work items of at most 4 k-blocks), wide (the
+ * paired epilogue path's boxes: 0 = 32x32 R and D boxes, 1 = 32x64 R and D
+ * boxes, 2 = 32x64 D and 32x32 R boxes; -1 = auto: 1, or 2 on the lean
+ * kernel), r_async (R rows that are not 16-byte aligned, without split: 1 =
+ * per-lane cp.async word copies into a prefetch queue, 0 or -1 = synchronous
+ * loads at use), mc (1 = A multicast between two CTA pairs in 4-CTA clusters,
+ * without split), issue (MMA issue loop variant 0..3), tmem_ld (TMEM columns
+ * per load on the express path: 32 or 64), prod (producer threads: 1 or 2),
+ * hint_a, hint_b, hint_r, hint_d (L2 eviction policy of the TMA loads of A,
+ * of B / W1 / W3, of R, and of the TMA stores of D and Z: 0 = none, 1 = evict
+ * first, 2 = evict last, -1 = the built-in choice).
  * Process-wide; returns GB_ERR_INVALID_ARG on an unknown key or value.
  */
 GB_API gb_status_t gb_set_config(const char* spec);

@@ -55,7 +55,8 @@ def test_wait_timeout_is_reported_and_context_survives(kind, pair, epi, extra):
     gb.set_config(None)
 
 
-@pytest.mark.parametrize("spec", ["epi=4", "epi=4,wide=0", "epi=2,wide=1", "epi=2,pingpong=1,wide=0"])
+@pytest.mark.parametrize("spec", ["epi=4", "epi=4,wide=0", "epi=4,wide=1", "epi=2,wide=1", "epi=2,wide=2",
+                                  "epi=2,pingpong=1,wide=0"])
 def test_wait_timeout_with_epilogue_input_queues(spec):
     """A residual launch whose R boxes are in flight when the waits run out (paired
     path, 32x32 and 32x64 boxes, two and four epilogue warpgroups): the epilogue drains

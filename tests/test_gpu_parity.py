@@ -506,8 +506,10 @@ def test_short_k_plan_takes_deep_queues():
     D = gb.linear(Ab, Bb, None, Rb)
     gb.device_status()
     big = gb.last_plan()
-    # ... on the lean kernel: four epilogue warpgroups, 32x32 boxes, a 2-stage ring
-    assert "pingpong=1" in big and "epi=4" in big and "stages=2" in big and "boxes=2/3" in big, big
+    # ... on the lean kernel: four epilogue warpgroups, one 32x64 D box and three 32x32 R
+    # boxes per warp, a 2-stage ring
+    assert "pingpong=1" in big and "epi=4" in big and "stages=2" in big and "boxes=1/3" in big, big
+    assert "d_store=tma.64x32" in big and "r_load=tma " in big + " ", big
     assert torch.equal(D.view(torch.int16), Rb.view(torch.int16))
 
 
@@ -637,8 +639,10 @@ def test_wide_boxes_identical_bits(spec):
             assert_close(got, ref_linear(A, B, bias, R, "gelu_tanh"), spec)
 
 
-@pytest.mark.parametrize("spec", ["epi=4", "epi=4,wide=0", "epi=4,grid=4", "epi=4,stages=2,r_boxes=4",
-                                  "epi=4,boxes=2", "epi=4,r_boxes=2,grid=2", "epi=4,hint_r=1,hint_d=1"])
+@pytest.mark.parametrize("spec", ["epi=4", "epi=4,wide=0", "epi=4,wide=1", "epi=4,wide=2,r_boxes=2", "epi=4,grid=4",
+                                  "epi=4,stages=2,r_boxes=4", "epi=4,boxes=2", "epi=4,r_boxes=2,grid=2",
+                                  "epi=4,hint_r=1,hint_d=1", "epi=4,stages=1", "epi=2,wide=2", "epi=2,wide=2,pingpong=0",
+                                  "epi=1,wide=2"])
 def test_four_epilogue_warpgroups_identical_bits(spec):
     """The lean kernel (four epilogue warpgroups, paired path only; warpgroups 2h, 2h + 1
     serve the tiles of parity h): identical bits to the two-warpgroup kernel on ragged
@@ -654,8 +658,11 @@ def test_four_epilogue_warpgroups_identical_bits(spec):
         got = run_linear(A, B, bias, R, "silu")
         plan = gb.last_plan()
         gb.set_config(None)
-        if M > 128:
+        if M > 128 and "epi=4" in spec:
             assert "epi=4" in plan and "pingpong=1" in plan, plan
+        if "wide=0" not in spec:  # 32x64 D boxes; 32x64 R boxes on request, or by default off the lean kernel
+            r_wide = "wide=1" in spec or ("wide=" not in spec and "epi=4" not in plan)
+            assert "d_store=tma.64x32" in plan and ("r_load=tma.64x32" in plan) == r_wide, plan
         assert_bitexact(got, base, f"{spec} {M}x{N}x{K}")
         if (M, N, K) == (700, 904, 64):
             assert_close(got, ref_linear(A, B, bias, R, "silu"), spec)
