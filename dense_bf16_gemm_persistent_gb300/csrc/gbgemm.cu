@@ -259,9 +259,11 @@ struct Variant {
     // for operands) and two boxes per warp; work items of at most 4 k-blocks are
     // bound by the epilogue's global traffic, so they take a 3-stage ring and spend
     // the rest on deeper D/R queues (more bytes in flight per SM).  `r_mode`: 0 no
-    // R boxes, 1 two boxes as the transpose buffer of unaligned R rows, 2 a queue
+    // R boxes, 1 one box as the transpose buffer of unaligned R rows, 2 a queue
     // of R boxes loaded by TMA, 3 a queue of cp.async slots for unaligned R rows
     // (3 deep by default: a long-K tile's next chunks all land during its MMAs).
+    // Unaligned D rows without a TMA-stored second output need one D box (the
+    // transpose buffer), so such launches keep room for a deeper ring.
     // Boxes shrink first, then the ring, down to 2 each.
     struct Layout {
         int stages, d_boxes, r_boxes;
@@ -280,7 +282,11 @@ struct Variant {
         st = std::max(2, st);
         int boxes = cfg.boxes > 0 ? cfg.boxes : (short_k ? gb::kMaxBoxes : 2);
         int rq = cfg.r_boxes > 0 ? cfg.r_boxes : (short_k ? gb::kMaxBoxes : 3);
-        auto r_of = [&](int b) { return r_mode == 2 ? (cfg.r_boxes > 0 ? rq : b) : r_mode == 3 ? rq : (r_mode == 1 ? 2 : 0); };
+        auto r_of = [&](int b) { return r_mode == 2 ? (cfg.r_boxes > 0 ? rq : b) : r_mode == 3 ? rq : (r_mode == 1 ? 1 : 0); };
+        // D rows not 16-byte aligned and no TMA-stored second output: the D queue is only
+        // the transpose buffer, one box
+        const bool d_transpose_only = !(flags & gb::kFlagDTma) && !((flags & gb::kFlagZ) && (flags & gb::kFlagZTma));
+        auto d_of = [&](int b) { return d_transpose_only && cfg.boxes <= 0 ? 1 : b; };
         const uint32_t rs = r_slot_bytes(flags), ds = d_slot_bytes(flags);
         if (kEpi == 4) {
             // Sixteen epilogue warps: per-warp queues must be short to fit.  32x64 D and R
@@ -307,11 +313,12 @@ struct Variant {
             while (r > 2 && S::smem_bytes(2, 2, r, rs, ds) > smem_optin) --r;
             return Layout{2, 2, r};
         }
-        while (r_mode == 3 && rq > 2 && S::smem_bytes(2, 2, rq, rs, ds) > smem_optin) --rq;
-        while (boxes > 2 && S::smem_bytes(st, boxes, r_of(boxes), rs, ds) > smem_optin) --boxes;
-        while (st > 2 && S::smem_bytes(st, boxes, r_of(boxes), rs, ds) > smem_optin) --st;
-        while (rq > 2 && S::smem_bytes(st, boxes, r_of(boxes), rs, ds) > smem_optin) --rq;
-        return Layout{st, boxes, r_of(boxes)};
+        // (a cp.async queue gives up depth, down to 2, before the ring gives up a stage)
+        while (r_mode == 3 && rq > 2 && S::smem_bytes(st, d_of(boxes), rq, rs, ds) > smem_optin) --rq;
+        while (boxes > 2 && S::smem_bytes(st, d_of(boxes), r_of(boxes), rs, ds) > smem_optin) --boxes;
+        while (st > 2 && S::smem_bytes(st, d_of(boxes), r_of(boxes), rs, ds) > smem_optin) --st;
+        while (rq > 2 && S::smem_bytes(st, d_of(boxes), r_of(boxes), rs, ds) > smem_optin) --rq;
+        return Layout{st, d_of(boxes), r_of(boxes)};
     }
 
     static gb_status_t launch(const GemmParams& p, int units, cudaStream_t stream) {

@@ -597,26 +597,40 @@ __device__ __forceinline__ void stage_box_row(uint32_t box, const float (&v)[32]
 }
 
 // Rows of D or R that are not 16-byte aligned (e.g. N = 4099): go through a
-// per-warp shared-memory transpose with a 68-byte row stride (conflict-free), so
-// every global access instruction covers one contiguous 64-byte row segment
-// instead of 32 scattered 2-byte ones.  Warp-collective.
-constexpr uint32_t kTRow = 68;
-static_assert(32 * kTRow <= 2 * kDStageBytes, "transpose buffer fits in a warp's two staging boxes");
+// per-warp shared-memory transpose, so every global access instruction covers one
+// contiguous 64-byte row segment instead of 32 scattered 2-byte ones.  The buffer is
+// one 32x32 staging box in the TMA 64-byte swizzle (16-byte unit u of row r at
+// u ^ ((r / 2) % 4)): a lane's own row moves as four conflict-free 16-byte accesses,
+// and column r (element `lane` of row r) is 64 contiguous bytes of the box.
+// Warp-collective.
+struct TransposeCols {  // this lane's element of a row, for the four swizzle phases of a row
+    uint32_t at[4];
+    __device__ __forceinline__ TransposeCols(uint32_t buf, int lane) {
+#pragma unroll
+        for (uint32_t k = 0; k < 4; ++k)
+            at[k] = buf + ((((static_cast<uint32_t>(lane) >> 3) ^ k) << 4) | ((static_cast<uint32_t>(lane) & 7u) << 1));
+    }
+    // shared address of element `lane` of row r (r a compile-time constant after unrolling)
+    __device__ __forceinline__ uint32_t row(int r) const { return at[(r >> 1) & 3] + static_cast<uint32_t>(r) * 64u; }
+};
 
 __device__ __forceinline__ void store_rows_transposed(const GemmParams& p, uint16_t* out, int64_t ld,
                                                       const uint32_t (&packed)[16], int32_t row0, int32_t n0,
-                                                      int valid, int lane, uint8_t* tbuf) {
-    if (lane == 0) bulk_wait_group_read<0>();  // TMA stores of this warp no longer read the buffers
+                                                      int valid, int lane, uint32_t tbuf) {
+    if (lane == 0) bulk_wait_group_read<0>();  // TMA stores of this warp no longer read the buffer
     __syncwarp();
-    uint32_t* mine = reinterpret_cast<uint32_t*>(tbuf + lane * kTRow);
+    const uint32_t row_addr = tbuf + lane * 64;
+    const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) mine[j] = packed[j];
+    for (int u = 0; u < 4; ++u)
+        st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
     __syncwarp();
     const int rows = min(32, p.m - row0);
-    const uint16_t* col = reinterpret_cast<const uint16_t*>(tbuf) + lane;
+    const TransposeCols col(tbuf, lane);
     uint16_t h[32];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) h[r] = col[r * (kTRow / 2)];  // all reads first...
+    for (int r = 0; r < 32; ++r)  // all reads first...
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h[r]) : "r"(col.row(r)));
     uint16_t* dst = out + static_cast<int64_t>(row0) * ld + n0 + lane;
     if (lane < valid) {
 #pragma unroll
@@ -627,38 +641,18 @@ __device__ __forceinline__ void store_rows_transposed(const GemmParams& p, uint1
 }
 
 __device__ __forceinline__ void add_rows_transposed(const GemmParams& p, float (&v)[32], int32_t row0, int32_t n0,
-                                                    int valid, int lane, uint8_t* tbuf) {
+                                                    int valid, int lane, uint32_t tbuf) {
     const int rows = min(32, p.m - row0);
     const uint16_t* src = p.r + static_cast<int64_t>(row0) * p.ldr + n0 + lane;
     uint16_t h[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r)  // all 32 coalesced row-segment loads in flight together
         h[r] = (r < rows && lane < valid) ? __ldg(src + static_cast<int64_t>(r) * p.ldr) : uint16_t(0);
-    uint16_t* col = reinterpret_cast<uint16_t*>(tbuf) + lane;
+    const TransposeCols col(tbuf, lane);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) col[r * (kTRow / 2)] = h[r];
+    for (int r = 0; r < 32; ++r) asm volatile("st.shared.u16 [%0], %1;" ::"r"(col.row(r)), "h"(h[r]) : "memory");
     __syncwarp();
-    const uint32_t* mine = reinterpret_cast<const uint32_t*>(tbuf + lane * kTRow);
-    switch (input_op(p.flags, p.act)) {
-        case 0:
-#pragma unroll
-            for (int j = 0; j < 16; ++j) combine2<0>(v[2 * j], v[2 * j + 1], mine[j]);
-            break;
-        case 1:
-#pragma unroll
-            for (int j = 0; j < 16; ++j) combine2<1>(v[2 * j], v[2 * j + 1], mine[j]);
-            break;
-        case 2:
-#pragma unroll
-            for (int j = 0; j < 16; ++j) combine2<2>(v[2 * j], v[2 * j + 1], mine[j]);
-            break;
-        case 3:
-#pragma unroll
-            for (int j = 0; j < 16; ++j) combine2<3>(v[2 * j], v[2 * j + 1], mine[j]);
-            break;
-        default:
-            break;
-    }
+    apply_input_box(p, v, tbuf, lane);  // this lane's row, as from a TMA box
     __syncwarp();
 }
 
@@ -689,7 +683,7 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorM
         }
         if (++dslot == p.d_boxes) dslot = 0;
     } else {
-        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, shared_ptr(dbox));
+        store_rows_transposed(p, out, ld, packed, row0, n0, valid, lane, dbox);
     }
 }
 
@@ -763,7 +757,7 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, float (&v)[32]
                 }
             } else {
                 GB_TR_ADD(tr_ep, kTrEpMath, tx);
-                add_rows_transposed(p, v, row0, n0, valid, lane, shared_ptr(tbuf_r));
+                add_rows_transposed(p, v, row0, n0, valid, lane, tbuf_r);
                 GB_TR_ADD(tr_ep, kTrEpRWait, tx);
             }
         }
