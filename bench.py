@@ -61,12 +61,15 @@ WORKLOADS = {
     # the MLP layer's backward activation-gradient product D[M,K] = (dY[M,N] . W[N,K]) * gelu'(Z[M,K])
     "mlp_dact": dict(M=8192, N=14336, K=4096, kind="dact", act="gelu_tanh", bias=False, residual=False,
                      name="mlp_dact_8192x14336x4096"),
+    # the MLP linear in the MatmulOp form: X[8192,4096] . W[4096,14336] (the weight stored [K,N])
+    "mlp_matmul": dict(M=8192, N=14336, K=4096, kind="matmul", act="gelu_tanh", bias=True, residual=False,
+                       name="mlp_matmul_8192x14336x4096"),
 }
 
 # Every configuration, timed after the main workload: plain matmul (latency), MLP linear,
 # Llama FFN, 64-bit indexing, the MLP with its stored pre-activation, the backward
 # activation-gradient product, and ragged rows (skinny and long K, short K, unaligned N).
-PER_SHAPE = ["plain", "mlp_gelu", "llama_ffn", "int64", "mlp_preact", "mlp_dact",
+PER_SHAPE = ["plain", "mlp_gelu", "llama_ffn", "int64", "mlp_preact", "mlp_dact", "mlp_matmul",
              "ragged:127,96,65536", "ragged:8191,96,65536", "ragged:8191,12288,64",
              "ragged:1000,4099,4096", "ragged:3001,4099,4096", "ragged:8191,4099,4096"]
 
@@ -271,6 +274,11 @@ def make_inputs(wl: dict, device):
         return inputs.llama_ffn(device=device, M=M, N=N, K=K)
     if wl["kind"] == "dact":
         return inputs.mlp_dact(device=device, M=M, N=N, K=K)
+    if wl["kind"] == "matmul":  # the MLP recipe with W laid out [K, N]
+        t = inputs.mlp_gelu(device=device, M=M, N=N, K=K)
+        t["B"] = t["B"].t().contiguous()
+        t.setdefault("R", None)
+        return t
     if wl["name"].startswith("ragged"):
         t = inputs.ragged(M, N, K, device=device)
     elif wl["name"].startswith("int64"):
@@ -314,6 +322,8 @@ def step_fn(wl: dict, t: dict, out, workspace=None, stream=None):
         z = torch.empty_like(out)
         return lambda: gb.linear_preact(t["A"], t["B"], t.get("bias"), t.get("R"), act=t["act"], out=out,
                                         preact=z, stream=stream)
+    if wl["kind"] == "matmul":
+        return lambda: gb.matmul(t["A"], t["B"], t.get("bias"), t.get("R"), act=t["act"], out=out, stream=stream)
     split = wl.get("split_k")
     return lambda: gb.linear(t["A"], t["B"], t.get("bias"), t.get("R"), act=t["act"], out=out, split_k=split,
                              workspace=workspace, stream=stream)
@@ -343,7 +353,7 @@ def oracle_sample_run(wl: dict, h: dict, rows: int):
         return time.perf_counter() - t0, 2.0 * rows * N * K, oracle.num_threads()
     R = h.get("R")
     t0 = time.perf_counter()
-    run = oracle.linear_preact if wl.get("preact") else oracle.linear
+    run = oracle.linear_preact if wl.get("preact") else oracle.matmul if wl["kind"] == "matmul" else oracle.linear
     run(h["A"][:rows], h["B"], h.get("bias"), None if R is None else R[:rows], h["act"])
     return time.perf_counter() - t0, 2.0 * rows * N * K, oracle.num_threads()
 
@@ -475,7 +485,9 @@ def sampled_accuracy(wl: dict, t: dict, out, n: int, seed: int) -> dict:
         else:
             bias = _bits(t["bias"][cj]) if t.get("bias") is not None else None
             R = _bits(t["R"][ci, cj]) if t.get("R") is not None else None
-            A, B = _bits(t["A"][ci]), _bits(t["B"][cj])
+            # B rows [N, K]; for the matmul form, columns of B [K, N]
+            B = _bits(t["B"][:, cj].t().contiguous()) if wl["kind"] == "matmul" else _bits(t["B"][cj])
+            A = _bits(t["A"][ci])
             ref[sl] = oracle.linear_entries(A, B, bias, R, t["act"])
             ref64[sl] = oracle.linear_entries(A, B, bias, R, t["act"], f64=True)
     g = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         L.gb_gemm_linear_preact.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, p, i64, i64, i64, i64,
                                             p]
         L.gb_gemm_linear_dact.argtypes = [p, i64, p, i64, p, i64, ctypes.c_int, p, i64, i64, i64, i64, p]
+        L.gb_gemm_matmul.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64, p]
         L.gb_gemm_linear_splitk.argtypes = [p, i64, p, i64, p, p, i64, ctypes.c_int, p, i64, i64, i64, i64,
                                              ctypes.c_int, p, ctypes.c_size_t, p]
         L.gb_gemm_ffn_gated_splitk.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, ctypes.c_int, p,
@@ -80,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.gb_version.argtypes = []
         L.gb_version.restype = ctypes.c_char_p
         for name in ("gb_gemm_linear", "gb_gemm_ffn_gated", "gb_gemm_linear_preact", "gb_gemm_linear_dact",
+                     "gb_gemm_matmul",
                      "gb_gemm_linear_splitk",
                      "gb_gemm_ffn_gated_splitk",
                      "gb_splitk_workspace_bytes", "gb_gemm_linear_splitk_noalloc", "gb_static_scratch_bytes",
@@ -186,6 +188,28 @@ def linear_preact(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = 
     _check(lib().gb_gemm_linear_preact(pa, lda, pb, ldb, bias.data_ptr() if bias is not None else None, pr, ldr,
                                        ACT[act], pd, ldd, pz, ldz, M, N, K, _stream(stream)))
     return out, preact
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, bias: torch.Tensor | None = None, R: torch.Tensor | None = None,
+           act: str = "none", out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = bf16(act(A @ B + bias) + R) on the GPU with B in its [K,N] layout (A [M,K], B [K,N],
+    bias [N], R [M,N])."""
+    M, K = A.shape
+    N = B.shape[1]
+    if act not in ACT:
+        raise ValueError(f"act must be one of {sorted(ACT)}")
+    pa, lda = _mat(A, "A", M, K)
+    pb, ldb = _mat(B, "B", K, N)
+    pr, ldr = _mat(R, "R", M, N)
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.shape != (N,) or (N > 1 and bias.stride(0) != 1):
+            raise ValueError("bias: expected a contiguous CUDA bfloat16 tensor of shape (N,)")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    pd, ldd = _mat(out, "out", M, N)
+    _check(lib().gb_gemm_matmul(pa, lda, pb, ldb, bias.data_ptr() if bias is not None else None, pr, ldr, ACT[act],
+                                pd, ldd, M, N, K, _stream(stream)))
+    return out
 
 
 def linear_dact(dY: torch.Tensor, W: torch.Tensor, Z: torch.Tensor, act: str = "none",

@@ -368,8 +368,11 @@ struct Problem {
     bool ffn;
     void* z = nullptr;  // optional second output (linear): the pre-activation
     int64_t ldz = 0;
-    // activation gradient: B is a row-major [k, n] matrix (MN-major operand) and the
-    // epilogue input r (the stored pre-activation) multiplies by act'(r)
+    // B is a row-major [k, n] matrix (MN-major operand): the matmul form, and the
+    // activation gradient
+    bool b_mn = false;
+    // activation gradient: the epilogue input r (the stored pre-activation) multiplies
+    // by act'(r)
     bool dact = false;
 };
 
@@ -399,9 +402,9 @@ gb_status_t validate(const Problem& pr) {
         if (pr.lda < pr.k)
             return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < %s=%" PRId64, pr.ffn ? "x" : pr.dact ? "dy" : "a",
                         pr.lda, kn, pr.k);
-        if (pr.dact && pr.ldb0 < pr.n)
-            return fail(GB_ERR_INVALID_ARG, "ldw=%" PRId64 " < K=%" PRId64, pr.ldb0, pr.n);
-        if (!pr.dact && pr.ldb0 < pr.k)
+        if (pr.b_mn && pr.ldb0 < pr.n)
+            return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < %s=%" PRId64, pr.dact ? "w" : "b", pr.ldb0, nn, pr.n);
+        if (!pr.b_mn && pr.ldb0 < pr.k)
             return fail(GB_ERR_INVALID_ARG, "ld%s=%" PRId64 " < K=%" PRId64, pr.ffn ? "w1" : "b", pr.ldb0, pr.k);
         if (pr.ffn && pr.ldb1 < pr.k) return fail(GB_ERR_INVALID_ARG, "ldw3=%" PRId64 " < K=%" PRId64, pr.ldb1, pr.k);
         if (!aligned16(pr.a) || !aligned16(pr.b0) || (pr.ffn && !aligned16(pr.b1)))
@@ -542,7 +545,8 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     uint32_t flags = 0;
     if (!pr.ffn && pr.bias) flags |= gb::kFlagBias | (aligned16(pr.bias) ? gb::kFlagBiasVec : 0u);
     if (!pr.ffn && pr.r) flags |= gb::kFlagResidual | ((aligned16(pr.r) && pr.ldr % 8 == 0) ? gb::kFlagRVec : 0u);
-    if (pr.dact) flags |= gb::kFlagBMn | gb::kFlagDact;
+    if (pr.b_mn) flags |= gb::kFlagBMn;
+    if (pr.dact) flags |= gb::kFlagDact;
     const bool d_tma = aligned16(pr.d) && pr.ldd % 8 == 0;
     if (d_tma) flags |= gb::kFlagDTma;
     const bool r_tma = !pr.ffn && pr.r && aligned16(pr.r) && pr.ldr % 8 == 0 && splits == 1;
@@ -596,8 +600,8 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
         if ((mc || prm.prod == 3) && (st = make_tmap(&prm.tm_a_half, pr.a, pr.k, pr.m, pr.lda * 2, gb::kBK, gb::kBM / 2,
                                                     CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
             return st;
-        if (pr.dact) {
-            // B = W [k rows (contraction), n columns]: boxes of 64 columns x 64 rows
+        if (pr.b_mn) {
+            // B [k rows (contraction), n columns]: boxes of 64 columns x 64 rows
             if ((st = make_tmap(&prm.tm_b0, pr.b0, pr.n, pr.k, pr.ldb0 * 2, 64, gb::kBK,
                                 CU_TENSOR_MAP_SWIZZLE_128B)) != GB_OK)
                 return st;
@@ -645,7 +649,8 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
              "kernel=%s pair=%d mc=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
              "k_blocks=%d splits=%d group=%d zigzag=%d prod=%d hints=%u%u%u%u "
              "d_store=%s r_load=%s z_store=%s",
-             pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : "linear", V::kPair ? 1 : 0, prm.mc, V::kEpi,
+             pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : pr.b_mn ? "matmul" : "linear", V::kPair ? 1 : 0, prm.mc,
+             V::kEpi,
              prm.pingpong,
              V::kTileM, bn, gb::kBK,
              prm.stages,
@@ -737,7 +742,7 @@ gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitR
         return fail(GB_ERR_INVALID_ARG, "pingpong=1 needs two epilogue warpgroups (epi=2)");
     // Four epilogue warpgroups (lean kernel: paired path only): linear with an aligned
     // epilogue input, an aligned D, no second output, 256-wide tiles on CTA pairs.
-    const bool lean_ok = !pr.ffn && !pr.dact && pr.r && !pr.z && r_rows_aligned && d_rows_aligned && kb > 0 &&
+    const bool lean_ok = !pr.ffn && !pr.b_mn && pr.r && !pr.z && r_rows_aligned && d_rows_aligned && kb > 0 &&
                          pair && bn == 256;
     // By default for work items of at most 4 k-blocks (the epilogue is the whole cost) over
     // at least two tiles per CTA pair: measured on GB300, K = 64 residual 8191x12288,
@@ -970,7 +975,17 @@ gb_status_t gb_gemm_linear_dact(const void* dY, int64_t lddy, const void* W, int
     t_error.clear();
     // output [M, K], contraction over N: in the plan's terms n = K and k = N
     Problem pr{dY, lddy, W, ldw, nullptr, 0, nullptr, Z, ldz, act, D, ldd, M, K, N, false};
+    pr.b_mn = true;
     pr.dact = true;
+    return run(pr, stream);
+}
+
+gb_status_t gb_gemm_matmul(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, const void* R,
+                           int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                           void* stream) {
+    t_error.clear();
+    Problem pr{A, lda, B, ldb, nullptr, 0, bias, R, ldr, act, D, ldd, M, N, K, false};
+    pr.b_mn = true;
     return run(pr, stream);
 }
 

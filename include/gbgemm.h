@@ -169,6 +169,24 @@ GB_API gb_status_t gb_gemm_ffn_gated_splitk(const void* X, int64_t ldx, const vo
                                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Matrix product with B in its natural [K, N] layout (the MatmulOp form, A.B,
+ * beside the LinearOp form A.B^T of gb_gemm_linear):
+ *
+ *   D[m,n] = bf16( act( sum_k A[m,k] B[k,n] + bias[n] ) + R[m,n] )
+ *
+ * B is a row-major [K, N] matrix (ldb >= N): the contraction runs over its rows,
+ * so the tensor cores read it as an MN-major operand straight from its layout
+ * (TMA boxes of 64 columns x 64 rows), with no transposed copy.  "Translate MmaOp
+ * patterns properly on Hopper" (NVIDIA/Fuser PR #4072, description: MatmulOp and
+ * LinearOp) names both forms.  A and B: base 16-byte aligned, lda and ldb
+ * multiples of 8 (TMA), lda >= K, ldb >= N.  bias, R, D, act, the epilogue
+ * order, the store and load paths, errors and limits as gb_gemm_linear.
+ */
+GB_API gb_status_t gb_gemm_matmul(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                                  const void* R, int64_t ldr, int act, void* D, int64_t ldd, int64_t M, int64_t N,
+                                  int64_t K, void* stream);
+
+/*
  * Activation gradient of a linear layer's input (the backward-pass consumer of
  * the pre-activation that gb_gemm_linear_preact stores):
  *

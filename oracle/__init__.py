@@ -120,6 +120,14 @@ class Oracle:
         self.lib.oracle_linear_f32(pa, lda, pb, ldb, pbias, pr, ldr, ACT[act], D.ctypes.data, N, M, N, K)
         return D
 
+    def matmul(self, A, B, bias=None, R=None, act: str = "none"):
+        """D[M,N] = bf16( act(A.B + bias) + R ) with B given as [K,N] (the MatmulOp form of
+        "Translate MmaOp patterns properly on Hopper", description).  By definition A.B =
+        A.(B^T)^T: the same sum over k in the same order as linear() on B^T, so B is
+        transposed (a copy) and linear() evaluates it."""
+        Bt = np.ascontiguousarray(np.asarray(B).T)
+        return self.linear(A, Bt, bias, R, act)
+
     def linear_preact(self, A, B, bias=None, R=None, act: str = "none"):
         """(D, Z): D as in linear(), Z[M,N] = bf16(A.B^T + bias), the pre-activation."""
         M, N, K = self._dims(A, B)
@@ -307,6 +315,10 @@ def default() -> Oracle:
 
 def linear(A, B, bias=None, R=None, act: str = "none"):
     return default().linear(A, B, bias, R, act)
+
+
+def matmul(A, B, bias=None, R=None, act: str = "none"):
+    return default().matmul(A, B, bias, R, act)
 
 
 def linear_f64(A, B, bias=None, R=None, act: str = "none"):

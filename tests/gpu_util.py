@@ -75,7 +75,8 @@ def check_pairs(kind: str, D: torch.Tensor, ops: dict, i: np.ndarray, j: np.ndar
 
     kind "linear": ops A [M,K], B [N,K], optional bias [N], R [M,N];
     kind "ffn":    ops X, W1, W3;
-    kind "dact":   ops dY [M,N'], W [N',K] (entry (m, k) uses column k of W), Z [M,K].
+    kind "dact":   ops dY [M,N'], W [N',K] (entry (m, k) uses column k of W), Z [M,K];
+    kind "matmul": ops A [M,K], B [K,N] (entry (m, n) uses column n of B), optional bias, R.
     Operand rows are gathered on the device in chunks, so K may be large.  Checks the
     tolerance on every entry and, when ulp_gate is set, that at least that fraction of
     entries lies within one bf16 ulp of the float64 result.  Returns a small report."""
@@ -93,6 +94,15 @@ def check_pairs(kind: str, D: torch.Tensor, ops: dict, i: np.ndarray, j: np.ndar
             rv = _gather_pairs(R, ii, jj) if R is not None else None
             ref[s:s + ii.size] = oracle.linear_entries(Ar, Br, bv, rv, act)
             ref64[s:s + ii.size] = oracle.linear_entries(Ar, Br, bv, rv, act, f64=True)
+        elif kind == "matmul":  # ops A [M,K], B [K,N] (entry (m, n) uses column n of B), bias, R
+            Ar = _gather(ops["A"], ii)
+            Bc = bits(ops["B"][:, torch.from_numpy(jj).to(ops["B"].device)].t().contiguous())
+            bias = ops.get("bias")
+            R = ops.get("R")
+            bv = bits(bias)[jj] if bias is not None else None
+            rv = _gather_pairs(R, ii, jj) if R is not None else None
+            ref[s:s + ii.size] = oracle.linear_entries(Ar, Bc, bv, rv, act)
+            ref64[s:s + ii.size] = oracle.linear_entries(Ar, Bc, bv, rv, act, f64=True)
         elif kind == "ffn":
             Xr, W1r, W3r = _gather(ops["X"], ii), _gather(ops["W1"], jj), _gather(ops["W3"], jj)
             ref[s:s + ii.size] = oracle.ffn_entries(Xr, W1r, W3r)

@@ -492,10 +492,37 @@ def check_entries(o) -> None:
                                rtol=1e-12, atol=1e-13)
 
 
+def check_matmul_form(o) -> None:
+    """The MatmulOp form (B given as [K,N]): integer operands against numpy's exact integer
+    product, an index pattern that a transposed or misread B cannot reproduce (D[m,n] =
+    m + 16 n with B[0,n] = 1, B[1,n] = 16 n), and the identity B = I_K returning A."""
+    rng = np.random.default_rng(31)
+    for M, N, K in [(1, 1, 1), (6, 9, 40), (13, 5, 64)]:
+        A, a = int_bf16(rng, (M, K))
+        B, b = int_bf16(rng, (K, N))
+        bias, bv = int_bf16(rng, (N,), -3, 3)
+        R, rv = int_bf16(rng, (M, N), -3, 3)
+        exact = a @ b
+        np.testing.assert_array_equal(o.matmul(A, B), lib_round_bf16(exact.astype(np.float32)))
+        relu = np.maximum(exact + bv[None, :], 0) + rv
+        np.testing.assert_array_equal(o.matmul(A, B, bias=bias, R=R, act="relu"), lib_round_bf16(relu.astype(np.float32)))
+    M, N, K = 9, 7, 24
+    a = np.zeros((M, K), np.float32)
+    b = np.zeros((K, N), np.float32)
+    a[:, 0] = np.arange(M)
+    a[:, 1] = 1.0
+    b[0, :] = 1.0
+    b[1, :] = 16.0 * np.arange(N)
+    want = np.arange(M)[:, None] + 16 * np.arange(N)[None, :]
+    np.testing.assert_array_equal(o.matmul(lib_round_bf16(a), lib_round_bf16(b)), lib_round_bf16(want.astype(np.float32)))
+    A = rand_bf16(rng, (11, 16))
+    np.testing.assert_array_equal(o.matmul(A, lib_round_bf16(np.eye(16, dtype=np.float32))), A)
+
+
 ALL_CHECKS = [check_f32_to_bf16, check_f64_to_bf16, check_acc_error_bound, check_fp32_sequential_sum,
               check_integer_exact,
               check_transpose_and_index, check_identity_b, check_zero_bias_and_linearity,
               check_bias_broadcast_and_residual, check_k_zero, check_activation_closed_forms,
               check_activation_vs_library, check_epilogue_order, check_ffn, check_leading_dims,
               check_preact_output, check_dact_closed_forms, check_dact_vs_autograd, check_dact_integer_exact,
-              check_dact_index_and_transpose, check_dact_identity_and_order, check_entries]
+              check_dact_index_and_transpose, check_dact_identity_and_order, check_entries, check_matmul_form]

@@ -177,6 +177,30 @@ def test_dact_rejects(L, kwargs, status, needle):
     assert needle in L.gb_last_error().decode()
 
 
+def matmul(L, A=P16, lda=64, B=P16, ldb=32, bias=None, R=None, ldr=0, act=1, D=P16, ldd=32, M=16, N=32, K=64):
+    return L.gb_gemm_matmul(A, lda, B, ldb, bias, R, ldr, act, D, ldd, M, N, K, None)
+
+
+@pytest.mark.parametrize("kwargs,status,needle", [
+    (dict(A=None), GB_ERR_INVALID_ARG, "A is null"),
+    (dict(B=None), GB_ERR_INVALID_ARG, "B is null"),
+    (dict(lda=32), GB_ERR_INVALID_ARG, "lda"),
+    (dict(ldb=16), GB_ERR_INVALID_ARG, "ldb"),
+    (dict(ldd=16), GB_ERR_INVALID_ARG, "ldd"),
+    (dict(R=P16, ldr=16), GB_ERR_INVALID_ARG, "ldr"),
+    (dict(act=9), GB_ERR_INVALID_ARG, "activation"),
+    (dict(B=P2), GB_ERR_UNSUPPORTED, "16-byte"),
+    (dict(ldb=36), GB_ERR_UNSUPPORTED, "multiples of 8"),
+    (dict(D=P1), GB_ERR_UNSUPPORTED, "2-byte"),
+])
+def test_matmul_rejects(L, kwargs, status, needle):
+    """The MatmulOp entry point (B given as [K,N]): ldb is checked against N, not K."""
+    assert matmul(L, **kwargs) == status
+    assert needle in L.gb_last_error().decode()
+    # M = 0 or N = 0: nothing to do, no pointer is needed
+    assert L.gb_gemm_matmul(None, 0, None, 0, None, None, 0, 0, None, 0, 0, 4, 4, None) == GB_OK
+
+
 def test_probe_rejects_bad_arguments(L):
     import ctypes
     r, c = ctypes.c_double(0), ctypes.c_double(0)
