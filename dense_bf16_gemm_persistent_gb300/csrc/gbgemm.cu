@@ -878,6 +878,7 @@ gb_status_t probe_run(int mode, int units, int num_mma, int alternate, int alu, 
         case gb::kProbeTmaStore: return probe_launch<CG, N, gb::kProbeTmaStore>(units, num_mma, alternate, alu, stream);
         case gb::kProbeSmspMath: return probe_launch<CG, N, gb::kProbeSmspMath>(units, num_mma, alternate, alu, stream);
         case gb::kProbeSmspPoll: return probe_launch<CG, N, gb::kProbeSmspPoll>(units, num_mma, alternate, alu, stream);
+        case gb::kProbeMnMajor: return probe_launch<CG, N, gb::kProbeMnMajor>(units, num_mma, alternate, alu, stream);
         default: return probe_launch<CG, N, gb::kProbePipeline>(units, num_mma, alternate, alu, stream);
     }
     }

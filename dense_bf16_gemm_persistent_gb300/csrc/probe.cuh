@@ -66,7 +66,10 @@ enum : int {
     // empty barriers of both CTAs; producers are warp 0 (A, and the byte count) and warp 2
     // (B) of every CTA, the MMA issuer is warp 1 of the leader
     kProbePipeline = 20,
-    kProbeModes = 21,
+    // as kProbePlain with B MN-major (the layout of a row-major [K, N] operand: 64-column
+    // blocks of 128-byte rows, one row per K index)
+    kProbeMnMajor = 21,
+    kProbeModes = 22,
 };
 
 // Source of the bulk copies of probe mode 11 (read only; its contents do not matter).
@@ -288,16 +291,19 @@ __global__ void __launch_bounds__(256, 1) mma_rate_kernel(int num_mma, int alter
     if (threadIdx.x == 0) {
         bool ok = true;
         if (rank == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128 * CG, N);
+            constexpr bool mn = MODE == kProbeMnMajor;
+            constexpr uint32_t idesc = idesc_bf16_f32(128 * CG, N) | (mn ? kIdescBMnMajor : 0u);
             const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(a_tile));
-            const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(b_tile));
+            // MN-major: 64-column blocks 8 KiB apart, a 16-row K slice is 2 KiB (>> 4: 128)
+            const uint64_t bdesc = mn ? sdesc_mnmajor_sw128(smem_addr(b_tile), 64 * 64 * 2) : sdesc_kmajor_sw128(smem_addr(b_tile));
+            constexpr uint64_t bstep = mn ? 128u : 2u;
             uint32_t x = static_cast<uint32_t>(num_mma);  // the ALU chain's value (kept live)
             const long long c0 = clock64();
-            if constexpr (MODE == kProbePlain || MODE == kProbeAlu) {
+            if constexpr (MODE == kProbePlain || MODE == kProbeAlu || MODE == kProbeMnMajor) {
                 for (int i = 0; i < num_mma; ++i) {
                     const uint32_t acc_col = (alternate & 1) ? static_cast<uint32_t>(i & 1) * 256u : 0u;
                     const int j = i & 3;  // walk the four 16-wide K slices of the tile
-                    mma_bf16<CG>(tmem + acc_col, adesc + 2 * j, bdesc + 2 * j, idesc, i >= 2 ? 1u : 0u);
+                    mma_bf16<CG>(tmem + acc_col, adesc + 2 * j, bdesc + bstep * j, idesc, i >= 2 ? 1u : 0u);
                     if constexpr (MODE == kProbeAlu) {
                         for (int a = 0; a < alu; ++a) asm volatile("mad.lo.u32 %0, %0, 3, 1;" : "+r"(x));
                     }

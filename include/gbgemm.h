@@ -374,7 +374,9 @@ GB_API gb_status_t gb_measure_mma_rate(int cta_group, int n, int alternate, int 
  * (one on each SM sub-partition, warp 4 beside the issuing thread) running FMA
  * math (18) or polling an mbarrier that never completes (19); 20 a GEMM mainloop
  * without epilogue (TMA into a 6-stage ring, full/empty barriers, two producer
- * threads, the MMAs of each stage, a commit per stage).  Writes the median
+ * threads, the MMAs of each stage, a commit per stage); 21 as 0 with the B operand
+ * MN-major (a row-major [K, N] matrix's layout, as gb_gemm_matmul and
+ * gb_gemm_linear_dact read it).  Writes the median
  * cycles per MMA and, when tmem_loads_per_mma is not NULL, the TMEM loads (modes
  * 7-9), 16 KiB copies (modes 11, 13, 14) or warp-wide 16-byte stores (mode 12) the leader
  * CTA completed per MMA (0 otherwise).  mode | 256: the operand tiles hold random
