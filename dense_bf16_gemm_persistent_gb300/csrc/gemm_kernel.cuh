@@ -1007,7 +1007,13 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
     // epilogue the large one; only the short teardown after the branches is shared.
     if (warp < kEpiWarp0) {
         if constexpr (W::kRealloc) setmaxnreg_dec<W::kRegsControl>();
-        if (warp == 0 || (warp == 2 && p.prod >= 2) || (warp == 3 && p.prod == 3)) {
+        // An MN-major B tile is two TMA boxes per stage: with two producer threads, warps 2
+        // and 3 take the B loads of alternate stages, so no thread issues more than one
+        // stage's worth of boxes per stage time (one thread issuing two boxes per stage
+        // falls behind the MMAs: measured on GB300, the MatmulOp MLP 0.731 -> 0.663 ms with
+        // the split; the same split costs the one-box K-major B 4 %, so it is MN-major only)
+        const bool b_par = (p.flags & kFlagBMn) && p.prod == 2;
+        if (warp == 0 || (warp == 2 && p.prod >= 2) || (warp == 3 && (p.prod == 3 || b_par))) {
             // ------------------------------------------------------------ producer (every CTA)
             // One thread issues every stage's loads, or two split them: warp 0 the A tile (and
             // the leader's expected byte count), warp 2 the B tile.  Both wait for the stage
@@ -1015,7 +1021,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             // prod == 3: warps 0 and 2 load the upper and lower halves of the A tile, warp 3 B
             const bool split_a = p.prod == 3 && !mc;
             const bool do_a = warp == 0 || (split_a && warp == 2);
-            const bool do_b = p.prod == 1 || (p.prod == 2 && warp == 2) || (p.prod == 3 && warp == 3);
+            const bool do_b = p.prod == 1 || (p.prod == 2 && (warp == 2 || (b_par && warp == 3))) ||
+                              (p.prod == 3 && warp == 3);
             if (lane == 0) {
                 uint32_t it = 0;
                 uint32_t s = 0, ph = 0;  // ring slot and phase of k-block `it`
@@ -1041,6 +1048,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                                 ph ^= 1u;
                             }
                         }
+                        // the other B thread's stage (MN-major B with two producer threads)
+                        if (b_par && warp != 0 && (it & 1u) != (warp == 3 ? 1u : 0u)) continue;
                         if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
                             ok = false;
                             break;

@@ -84,3 +84,39 @@ def test_wait_timeout_with_epilogue_input_queues(spec):
     gb.set_config(None)
     assert f"epi={spec.split('epi=')[1][0]}" in plan, plan
     assert_close(bits(D), oracle.linear(bits(A), bits(B), None, bits(R)), f"after timeout {spec}")
+
+
+@pytest.mark.parametrize("kind", ["matmul", "dact"])
+@pytest.mark.parametrize("pair", [0, 1])
+def test_wait_timeout_with_mn_major_b(kind, pair):
+    """The MN-major B path (B stored [K, N]; two producer threads take the B boxes of
+    alternate stages): a wait that runs out is reported and the context survives."""
+    M, N, K = 512, 768, 1024
+    A = inputs.randn_bf16((M, K), seed=11).cuda()
+    B = inputs.randn_bf16((K, N), seed=12, std=1.0 / np.sqrt(K)).cuda()
+    Z = inputs.randn_bf16((M, N), seed=13).cuda()
+    gb.device_status()
+    gb.set_config(f"pair={pair}")
+    gb.set_wait_timeout_ns(100_000_000)  # 0.1 s
+    gb.set_fault_injection(1)
+    try:
+        if kind == "matmul":
+            gb.matmul(A, B)
+        else:  # dY [M, K] . W [K, N] with the gradient of Z [M, N]
+            gb.linear_dact(A, B, Z, act="gelu_tanh")
+        with pytest.raises(gb.GBError) as ei:
+            gb.device_status()
+        assert ei.value.status == 4, str(ei.value)
+    finally:
+        gb.set_fault_injection(0)
+        gb.set_wait_timeout_ns(0)
+    gb.device_status()
+    if kind == "matmul":
+        D = gb.matmul(A, B)
+        gb.device_status()
+        assert_close(bits(D), oracle.matmul(bits(A), bits(B)), "after timeout")
+    else:
+        D = gb.linear_dact(A, B, Z, act="gelu_tanh")
+        gb.device_status()
+        assert_close(bits(D), oracle.dact(bits(A), bits(B), bits(Z), "gelu_tanh"), "after timeout")
+    gb.set_config(None)
