@@ -804,6 +804,40 @@ __device__ __forceinline__ void stage_descs(uint32_t ring0, uint32_t slot, uint3
     bd = b_mn ? sdesc_mnmajor_sw128(a_addr + a_bytes, kMnBoxBytes) : sdesc_kmajor_sw128(a_addr + a_bytes);
 }
 
+// The MMA issuer's loop over one item's k-blocks for the common operand forms: the
+// descriptor steps, the instruction descriptor and the commit mask are compile-time
+// constants, and nothing but the stage wait runs between k-blocks.  `s`, `ph` and `it`
+// carry the ring position across items (it == 0: nothing consumed yet).  Without A
+// multicast the cluster is the CTA pair itself, so the stage is freed in ranks 0 and 1.
+// Returns false if a wait gave up.
+template <int CG, uint32_t kStageBytes, uint32_t kABytes, uint32_t kIdescK, bool BMN>
+__device__ __forceinline__ bool issue_kblocks(uint32_t d_tmem, int32_t nkb, uint64_t* full, uint64_t* empty,
+                                              uint8_t* ring, uint32_t stages, uint32_t& s, uint32_t& ph,
+                                              uint32_t& it, volatile int32_t* abort_flag, uint64_t tmo,
+                                              TraceAcc& tr_full, bool& issued) {
+    constexpr uint32_t kIdesc = kIdescK | (BMN ? kIdescBMnMajor : 0u);
+    // per 16-element K slice: +32 bytes in a K-major tile (+2 encoded), +16 rows of 128 bytes
+    // in an MN-major one (+128 encoded)
+    constexpr uint64_t kBStep = BMN ? (16u * 128u) >> 4 : 2u;
+    for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
+        if (it > 0 && ++s == stages) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s, &tr_full)) return false;
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_addr(ring + s * kStageBytes);
+        const uint64_t ad = sdesc_kmajor_sw128(a_addr);
+        const uint64_t bd = BMN ? sdesc_mnmajor_sw128(a_addr + kABytes, kMnBoxBytes) : sdesc_kmajor_sw128(a_addr + kABytes);
+        mma_bf16_x4<CG>(d_tmem, ad, ad + 2, ad + 4, ad + 6, bd, bd + kBStep, bd + 2 * kBStep, bd + 3 * kBStep, kIdesc,
+                        kk > 0 ? 1u : 0u);
+        issued = true;
+        if constexpr (CG == 2) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
+        else mma_commit<1>(smem_addr(&empty[s]));
+    }
+    return true;
+}
+
 // One work item's k-blocks on the lean issue path.  The ring position (s, ph) and the
 // k-block counter `it` describe the k-block consumed last (it == 0: none yet), as in
 // the rebuild path, so both paths can follow each other.  Returns false if a wait gave up.
@@ -1038,6 +1072,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 // branches per k-block on those options, leave the tensor pipe idle longer (MLP
                 // launch 0.678 -> 0.601 ms with this loop alone, one CTA pair 1.69 -> 1.44 ms).
                 const bool lean_loads = !mc && !(p.flags & kFlagBMn) && p.prod == 2 && p.inject == 0;
+                // the same for an MN-major B (two boxes per stage; warps 2 and 3 take the B
+                // boxes of alternate stages)
+                const bool lean_mn = !mc && b_par && NUM_B == 1 && p.inject == 0;
                 const bool is_a = warp == 0;
                 for (int32_t w = unit; lean_loads && ok && w < num_work; w += units, ++local) {
                     const int32_t tile = w / p.splits;
@@ -1075,7 +1112,42 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         }
                     }
                 }
-                for (int32_t w = unit; !lean_loads && ok && w < num_work; w += units, ++local) {
+                for (int32_t w = unit; lean_mn && ok && w < num_work; w += units, ++local) {
+                    const int32_t tile = w / p.splits;
+                    const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
+                    const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
+                    int32_t mb, nb;
+                    work_tile(tile, p, pairi, mb, nb);
+                    const bool reverse = p.zigzag && (local & 1);
+                    const int32_t a_row = mb * S::kTileM + static_cast<int32_t>(rank) * kBM;
+                    const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * S::kBRows;
+                    const uint32_t my_parity = warp == 3 ? 1u : 0u;
+                    for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
+                        const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
+                        if (it > 0 && ++s == stages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        if (!is_a && (it & 1u) != my_parity) continue;  // the other B thread's stage
+                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t own_full = smem_addr(&full[s]);
+                        if (leader && is_a) mbar_arrive_expect_tx(own_full, S::kTxBytes);
+                        const uint32_t fb = PAIR ? mapa_shared(own_full, lead) : own_full;
+                        const uint32_t dst = smem_addr(ring + s * S::kStageBytes);
+                        if (is_a) {
+                            tma_load_op<PAIR>(dst, &p.tm_a, fb, kb * kBK, a_row, pol_a);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < S::kBRows / 64; ++h)
+                                tma_load_op<PAIR>(dst + S::kABytes + h * kMnBoxBytes, &p.tm_b0, fb, b_row + h * 64, kb * kBK,
+                                                  pol_b);
+                        }
+                    }
+                }
+                for (int32_t w = unit; !lean_loads && !lean_mn && ok && w < num_work; w += units, ++local) {
                     const int32_t tile = w / p.splits;
                     const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
                     const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
@@ -1196,9 +1268,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 const bool b_mn = NUM_B == 1 && (p.flags & kFlagBMn);
                 const uint32_t idesc = S::kIdesc | (b_mn ? kIdescBMnMajor : 0u);
                 const uint32_t bstep = b_mn ? (16u * 128u) >> 4 : 2u;
-                // the common form's loop (measured on GB300 with the lean load loop: MLP launch
+                // the common forms' loop (measured on GB300 with the lean load loop: MLP launch
                 // 0.601 -> 0.590 ms, one CTA pair 1.44 -> 1.31 ms)
-                const bool lean_issue = p.issue == 0 && !b_mn && !mc;
+                const bool lean_issue = p.issue == 0 && !mc;
 #ifdef GB_TRACE
                 const long long mma_c0 = clock64();
                 if (trace) trace[kTrMmaFirstNs] = 0;
@@ -1217,32 +1289,18 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + b * kAccStride;
                     if (lean_issue) {
-                        // Common form: the descriptor steps, the instruction descriptor and the
-                        // commit mask are constants (without A multicast the cluster is the pair
-                        // itself, ranks 0 and 1), and nothing else runs between k-blocks.
-                        for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
-                            if (it > 0 && ++s == stages) {
-                                s = 0;
-                                ph ^= 1u;
-                            }
-                            if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, p.timeout_ns, kRoleMma, s, &tr_full)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after_sync();
 #ifdef GB_TRACE
-                            if (trace && !issued) trace[kTrMmaFirstNs] = global_timer_ns();
+                        if (trace && !issued) trace[kTrMmaFirstNs] = global_timer_ns();
 #endif
-                            const uint32_t a_addr = smem_addr(ring + s * S::kStageBytes);
-                            const uint64_t ad = sdesc_kmajor_sw128(a_addr);
-                            const uint64_t bd = sdesc_kmajor_sw128(a_addr + S::kABytes);
-                            mma_bf16_x4<CG>(d_tmem, ad, ad + 2, ad + 4, ad + 6, bd, bd + 2, bd + 4, bd + 6, S::kIdesc,
-                                            kk > 0 ? 1u : 0u);
-                            issued = true;
-                            if constexpr (PAIR) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
-                            else mma_commit<1>(smem_addr(&empty[s]));
+                        const bool kb_ok =
+                            b_mn ? issue_kblocks<CG, S::kStageBytes, S::kABytes, S::kIdesc, true>(
+                                       d_tmem, nkb, full, empty, ring, stages, s, ph, it, abort_flag, p.timeout_ns, tr_full, issued)
+                                 : issue_kblocks<CG, S::kStageBytes, S::kABytes, S::kIdesc, false>(
+                                       d_tmem, nkb, full, empty, ring, stages, s, ph, it, abort_flag, p.timeout_ns, tr_full, issued);
+                        if (!kb_ok) {
+                            ok = false;
+                            break;
                         }
-                        if (!ok) break;
                         if constexpr (PAIR) mma_commit_multicast2(smem_addr(&ctl->acc_full[b]), pair_mask);
                         else mma_commit<1>(smem_addr(&ctl->acc_full[b]));
                         continue;
