@@ -266,18 +266,29 @@ __device__ __forceinline__ void record_timeout(uint32_t role, uint32_t where, vo
     *abort = 1;
 }
 
+// Suspend-time bound (ns) of the pipeline's ring and accumulator waits (see mbar_try_wait_for).
+constexpr uint32_t kRingSuspendNs = 64;
+
+// One try of a wait: with a suspend-time bound when kSuspendNs > 0.
+template <uint32_t kSuspendNs>
+__device__ __forceinline__ bool try_bar(uint32_t bar, uint32_t parity) {
+    if constexpr (kSuspendNs > 0) return mbar_try_wait_for<kSuspendNs>(bar, parity);
+    else return mbar_try_wait(bar, parity);
+}
+
 // Bounded wait for the phase of `bar` with the given parity.  Returns false if
 // the CTA is aborting or the time limit ran out (then it records the timeout).
+template <uint32_t kSuspendNs = 0>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort,
                                          uint64_t timeout_ns, uint32_t role, uint32_t where,
                                          TraceAcc* acc = nullptr) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_bar<kSuspendNs>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
 #ifdef GB_TRACE
     const long long c0 = clock64();
 #endif
     while (true) {
-        if (mbar_try_wait(bar, parity)) {
+        if (try_bar<kSuspendNs>(bar, parity)) {
 #ifdef GB_TRACE
             if (acc) {
                 acc->cyc += static_cast<unsigned long long>(clock64() - c0);
@@ -824,7 +835,7 @@ __device__ __forceinline__ bool issue_kblocks(uint32_t d_tmem, int32_t nkb, uint
             s = 0;
             ph ^= 1u;
         }
-        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s, &tr_full)) return false;
+        if (!wait_bar<kRingSuspendNs>(smem_addr(&full[s]), ph, abort_flag, tmo, kRoleMma, s, &tr_full)) return false;
         tc_fence_after_sync();
         const uint32_t a_addr = smem_addr(ring + s * kStageBytes);
         const uint64_t ad = sdesc_kmajor_sw128(a_addr);
@@ -858,7 +869,7 @@ __device__ __forceinline__ bool issue_tile_lean(const GemmParams& p, uint32_t d_
     }
     uint64_t ad, bd;
     stage_descs(ring0, cs, kStageBytes, kABytes, b_mn, ad, bd);
-    if (!wait_bar(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
+    if (!wait_bar<kRingSuspendNs>(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
     tc_fence_after_sync();
     const bool lookahead = p.issue == 2;
     for (int32_t kk = 0; kk < nkb; ++kk) {
@@ -880,7 +891,7 @@ __device__ __forceinline__ bool issue_tile_lean(const GemmParams& p, uint32_t d_
                 bd += kStageBytes >> 4;
             }
             if (lookahead) {
-                if (!wait_bar(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
+                if (!wait_bar<kRingSuspendNs>(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
                 tc_fence_after_sync();
             }
         }
@@ -888,7 +899,7 @@ __device__ __forceinline__ bool issue_tile_lean(const GemmParams& p, uint32_t d_
         if constexpr (CG == 2) mma_commit_multicast2(empty0 + 8 * done, empty_mask);
         else mma_commit<1>(empty0 + 8 * done);
         if (more && !lookahead) {
-            if (!wait_bar(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
+            if (!wait_bar<kRingSuspendNs>(full0 + 8 * cs, cph, abort_flag, tmo, kRoleMma, cs, &tr_full)) return false;
             tc_fence_after_sync();
         }
     }
@@ -1096,7 +1107,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             s = 0;
                             ph ^= 1u;
                         }
-                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
+                        if (!wait_bar<kRingSuspendNs>(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
                             ok = false;
                             break;
                         }
@@ -1129,7 +1140,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                             ph ^= 1u;
                         }
                         if (!is_a && (it & 1u) != my_parity) continue;  // the other B thread's stage
-                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
+                        if (!wait_bar<kRingSuspendNs>(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
                             ok = false;
                             break;
                         }
@@ -1166,7 +1177,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         }
                         // the other B thread's stage (MN-major B with two producer threads)
                         if (b_par && warp != 0 && (it & 1u) != (warp == 3 ? 1u : 0u)) continue;
-                        if (!wait_bar(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
+                        if (!wait_bar<kRingSuspendNs>(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s, &tr_empty)) {
                             ok = false;
                             break;
                         }
@@ -1281,7 +1292,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                     const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
                     const uint32_t b = local & 1;
                     const uint32_t aph = (local >> 1) & 1u;
-                    if (!wait_bar(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, p.timeout_ns, kRoleMma, 0x100u | b,
+                    if (!wait_bar<kRingSuspendNs>(smem_addr(&ctl->acc_empty[b]), aph ^ 1u, abort_flag, p.timeout_ns, kRoleMma, 0x100u | b,
                                   &tr_acc)) {
                         ok = false;
                         break;
@@ -1328,7 +1339,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         const unsigned long long blocked_before = tr_full.n;
                         const long long wait_c0 = clock64();
 #endif
-                        if (!wait_bar(smem_addr(&full[s]), ph, abort_flag, p.timeout_ns, kRoleMma, s, &tr_full)) {
+                        if (!wait_bar<kRingSuspendNs>(smem_addr(&full[s]), ph, abort_flag, p.timeout_ns, kRoleMma, s, &tr_full)) {
                             ok = false;
                             break;
                         }
@@ -1540,7 +1551,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
             const uint32_t aph = (local >> 1) & 1u;
             bool ok = true;
             if (lane == 0)
-                ok = wait_bar(smem_addr(&ctl->acc_full[b]), aph, abort_flag, p.timeout_ns, kRoleEpilogue, b, &tr_accfull);
+                ok = wait_bar<kRingSuspendNs>(smem_addr(&ctl->acc_full[b]), aph, abort_flag, p.timeout_ns, kRoleEpilogue, b, &tr_accfull);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
