@@ -819,9 +819,10 @@ __device__ __forceinline__ void stage_descs(uint32_t ring0, uint32_t slot, uint3
 // descriptor steps, the instruction descriptor and the commit mask are compile-time
 // constants, and nothing but the stage wait runs between k-blocks.  `s`, `ph` and `it`
 // carry the ring position across items (it == 0: nothing consumed yet).  Without A
-// multicast the cluster is the CTA pair itself, so the stage is freed in ranks 0 and 1.
+// multicast the cluster is the CTA pair itself, so the stage is freed in ranks 0 and 1
+// (kMask 0x3); with A multicast between two pairs, in all four CTAs (0xF).
 // Returns false if a wait gave up.
-template <int CG, uint32_t kStageBytes, uint32_t kABytes, uint32_t kIdescK, bool BMN>
+template <int CG, uint32_t kStageBytes, uint32_t kABytes, uint32_t kIdescK, bool BMN, uint16_t kMask = 0x3>
 __device__ __forceinline__ bool issue_kblocks(uint32_t d_tmem, int32_t nkb, uint64_t* full, uint64_t* empty,
                                               uint8_t* ring, uint32_t stages, uint32_t& s, uint32_t& ph,
                                               uint32_t& it, volatile int32_t* abort_flag, uint64_t tmo,
@@ -843,7 +844,7 @@ __device__ __forceinline__ bool issue_kblocks(uint32_t d_tmem, int32_t nkb, uint
         mma_bf16_x4<CG>(d_tmem, ad, ad + 2, ad + 4, ad + 6, bd, bd + kBStep, bd + 2 * kBStep, bd + 3 * kBStep, kIdesc,
                         kk > 0 ? 1u : 0u);
         issued = true;
-        if constexpr (CG == 2) mma_commit_multicast2(smem_addr(&empty[s]), 0x3);
+        if constexpr (CG == 2) mma_commit_multicast2(smem_addr(&empty[s]), kMask);
         else mma_commit<1>(smem_addr(&empty[s]));
     }
     return true;
@@ -1086,6 +1087,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 // the same for an MN-major B (two boxes per stage; warps 2 and 3 take the B
                 // boxes of alternate stages)
                 const bool lean_mn = !mc && b_par && NUM_B == 1 && p.inject == 0;
+                // and with A multicast between two pairs (4-CTA clusters): warp 0 loads its
+                // 64-row half of the A tile into its own and the other pair's same-rank CTA
+                const bool lean_mc = mc && !(p.flags & kFlagBMn) && p.prod == 2 && p.inject == 0;
                 const bool is_a = warp == 0;
                 for (int32_t w = unit; lean_loads && ok && w < num_work; w += units, ++local) {
                     const int32_t tile = w / p.splits;
@@ -1158,7 +1162,41 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                         }
                     }
                 }
-                for (int32_t w = unit; !lean_loads && !lean_mn && ok && w < num_work; w += units, ++local) {
+                if constexpr (PAIR) {
+                    const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
+                    for (int32_t w = unit; lean_mc && ok && w < num_work; w += units, ++local) {
+                        const int32_t tile = w / p.splits;
+                        const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
+                        const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
+                        int32_t mb, nb;
+                        work_tile(tile, p, pairi, mb, nb);
+                        const bool reverse = p.zigzag && (local & 1);
+                        const CUtensorMap* map = is_a ? &p.tm_a_half : (NUM_B == 2 && !leader) ? &p.tm_b1 : &p.tm_b0;
+                        const int32_t row = is_a ? mb * S::kTileM + static_cast<int32_t>(rank) * kBM +
+                                                       static_cast<int32_t>(pairi) * (kBM / 2)
+                                                 : nb * BN + (NUM_B == 1 ? static_cast<int32_t>(rank) * S::kBRows : 0);
+                        const uint32_t off = is_a ? pairi * (S::kABytes / 2) : static_cast<uint32_t>(S::kABytes);
+                        for (int32_t kk = 0; kk < nkb; ++kk, ++it) {
+                            const int32_t kb = kb0 + (reverse ? nkb - 1 - kk : kk);
+                            if (it > 0 && ++s == stages) {
+                                s = 0;
+                                ph ^= 1u;
+                            }
+                            if (!wait_bar<kRingSuspendNs>(smem_addr(&empty[s]), ph ^ 1u, abort_flag, p.timeout_ns, kRoleProducer, s,
+                                                          &tr_empty)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t own_full = smem_addr(&full[s]);
+                            if (leader && is_a) mbar_arrive_expect_tx(own_full, S::kTxBytes);
+                            const uint32_t dst = smem_addr(ring + s * S::kStageBytes) + off;
+                            const uint32_t fb = mapa_shared(own_full, lead);
+                            if (is_a) tma_load_2d_pair_multicast(dst, map, fb, kb * kBK, row, mc_mask);
+                            else tma_load_op<true>(dst, map, fb, kb * kBK, row, pol_b);
+                        }
+                    }
+                }
+                for (int32_t w = unit; !lean_loads && !lean_mn && !lean_mc && ok && w < num_work; w += units, ++local) {
                     const int32_t tile = w / p.splits;
                     const int32_t kb0 = (w - tile * p.splits) * p.kb_per_split;
                     const int32_t nkb = min(p.num_k_blocks - kb0, p.kb_per_split);
@@ -1281,7 +1319,7 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 const uint32_t bstep = b_mn ? (16u * 128u) >> 4 : 2u;
                 // the common forms' loop (measured on GB300 with the lean load loop: MLP launch
                 // 0.601 -> 0.590 ms, one CTA pair 1.44 -> 1.31 ms)
-                const bool lean_issue = p.issue == 0 && !mc;
+                const bool lean_issue = p.issue == 0 && !(mc && b_mn);
 #ifdef GB_TRACE
                 const long long mma_c0 = clock64();
                 if (trace) trace[kTrMmaFirstNs] = 0;
@@ -1305,6 +1343,8 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
 #endif
                         const bool kb_ok =
                             b_mn ? issue_kblocks<CG, S::kStageBytes, S::kABytes, S::kIdesc, true>(
+                                       d_tmem, nkb, full, empty, ring, stages, s, ph, it, abort_flag, p.timeout_ns, tr_full, issued)
+                            : mc ? issue_kblocks<CG, S::kStageBytes, S::kABytes, S::kIdesc, false, 0xF>(
                                        d_tmem, nkb, full, empty, ring, stages, s, ph, it, abort_flag, p.timeout_ns, tr_full, issued)
                                  : issue_kblocks<CG, S::kStageBytes, S::kABytes, S::kIdesc, false>(
                                        d_tmem, nkb, full, empty, ring, stages, s, ph, it, abort_flag, p.timeout_ns, tr_full, issued);
