@@ -27,7 +27,22 @@ constexpr int64_t kMaxLd = (int64_t(1) << 39) - 1;   // TMA strides are below 2^
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
 
 thread_local std::string t_error;
-thread_local std::string t_plan;
+thread_local std::string t_plan;  // a plan without a launch ("empty (no launch)")
+
+// The last launch's plan, kept as values and formatted only when gb_last_plan asks
+// (formatting it on every call cost host time on latency-bound launches).
+struct PlanRec {
+    bool valid = false;
+    const char* kernel = "";
+    int pair = 0, mc = 0, epi = 0, pingpong = 0, tile_m = 0, bn = 0, stages = 0, d_boxes = 0, r_boxes = 0;
+    long long grid = 0;
+    int tiles = 0, k_blocks = 0, splits = 0, group = 0, zigzag = 0, prod = 0;
+    unsigned hint_a = 0, hint_b = 0, hint_r = 0, hint_d = 0;
+    const char* d_store = "";
+    const char* r_load = "";
+    const char* z_store = "";
+};
+thread_local PlanRec t_plan_rec;
 
 gb_status_t fail(gb_status_t s, const char* fmt, ...) {
     char buf[512];
@@ -644,25 +659,34 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.pingpong = (V::kEpi == 4 || (V::kEpi == 2 && splits == 1 && (cfg.pingpong == 1 || (cfg.pingpong < 0 && pp_auto))))
                        ? 1 : 0;
 
-    char plan[420];
-    snprintf(plan, sizeof plan,
-             "kernel=%s pair=%d mc=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
-             "k_blocks=%d splits=%d group=%d zigzag=%d prod=%d hints=%u%u%u%u "
-             "d_store=%s r_load=%s z_store=%s",
-             pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : pr.b_mn ? "matmul" : "linear", V::kPair ? 1 : 0, prm.mc,
-             V::kEpi,
-             prm.pingpong,
-             V::kTileM, bn, gb::kBK,
-             prm.stages,
-             wide_d ? prm.d_boxes / 2 : prm.d_boxes, prm.r_boxes,
-             static_cast<long long>(units * (V::kPair ? (mc ? 4 : 2) : 1)), prm.num_tiles, prm.num_k_blocks, splits,
-             prm.group_m, prm.zigzag, prm.prod, prm.hint_a, prm.hint_b, prm.hint_r, prm.hint_d,
-             d_tma ? (wide_d ? "tma.64x32" : "tma") : "st.transposed",
-             pr.r ? (r_tma ? (wide ? "tma.64x32" : "tma") : r_async ? "cp.async" : (flags & gb::kFlagRVec) ? "ld.v4"
-                                                                                                  : "ld.transposed")
-                  : "none",
-             pr.z ? (z_tma ? "tma" : "st.transposed") : "none");
-    t_plan = plan;
+    PlanRec& rec = t_plan_rec;
+    rec.valid = true;
+    rec.kernel = pr.ffn ? "ffn_gated" : pr.dact ? "linear_dact" : pr.b_mn ? "matmul" : "linear";
+    rec.pair = V::kPair ? 1 : 0;
+    rec.mc = prm.mc;
+    rec.epi = V::kEpi;
+    rec.pingpong = prm.pingpong;
+    rec.tile_m = V::kTileM;
+    rec.bn = bn;
+    rec.stages = prm.stages;
+    rec.d_boxes = wide_d ? prm.d_boxes / 2 : prm.d_boxes;
+    rec.r_boxes = prm.r_boxes;
+    rec.grid = static_cast<long long>(units * (V::kPair ? (mc ? 4 : 2) : 1));
+    rec.tiles = prm.num_tiles;
+    rec.k_blocks = prm.num_k_blocks;
+    rec.splits = splits;
+    rec.group = prm.group_m;
+    rec.zigzag = prm.zigzag;
+    rec.prod = prm.prod;
+    rec.hint_a = prm.hint_a;
+    rec.hint_b = prm.hint_b;
+    rec.hint_r = prm.hint_r;
+    rec.hint_d = prm.hint_d;
+    rec.d_store = d_tma ? (wide_d ? "tma.64x32" : "tma") : "st.transposed";
+    rec.r_load = pr.r ? (r_tma ? (wide ? "tma.64x32" : "tma") : r_async ? "cp.async" : (flags & gb::kFlagRVec) ? "ld.v4"
+                                                                                                      : "ld.transposed")
+                      : "none";
+    rec.z_store = pr.z ? (z_tma ? "tma" : "st.transposed") : "none";
     {
         std::lock_guard<std::mutex> lk(g_cfg_mu);
         const size_t need = static_cast<size_t>(units) * (V::kPair ? (mc ? 4 : 2) : 1) * gb::kTraceWords * 8;
@@ -697,6 +721,7 @@ gb_status_t run(const Problem& pr, void* stream_ptr, const SplitReq& sr = SplitR
     if (st != GB_OK) return st;
     if (pr.m == 0 || pr.n == 0) {
         t_plan = "empty (no launch)";
+        t_plan_rec.valid = false;
         if (sr.query_only) *sr.ws_needed = 0;
         return GB_OK;
     }
@@ -1050,6 +1075,7 @@ gb_status_t gb_gemm_linear_splitk_noalloc(const void* A, int64_t lda, const void
     if (st != GB_OK) return st;
     if (pr.m == 0 || pr.n == 0) {
         t_plan = "empty (no launch)";
+        t_plan_rec.valid = false;
         return GB_OK;
     }
     int dev = 0;
@@ -1157,7 +1183,18 @@ gb_status_t gb_set_wait_timeout_ns(uint64_t ns) {
 gb_status_t gb_last_plan(char* buf, size_t len) {
     if (!buf) return fail(GB_ERR_INVALID_ARG, "buf is null");
     if (len == 0) return GB_OK;
-    snprintf(buf, len, "%s", t_plan.c_str());
+    const PlanRec& r = t_plan_rec;
+    if (!r.valid) {
+        snprintf(buf, len, "%s", t_plan.c_str());
+        return GB_OK;
+    }
+    snprintf(buf, len,
+             "kernel=%s pair=%d mc=%d epi=%d pingpong=%d tile=%dx%dx%d stages=%d boxes=%d/%d grid=%lld tiles=%d "
+             "k_blocks=%d splits=%d group=%d zigzag=%d prod=%d hints=%u%u%u%u "
+             "d_store=%s r_load=%s z_store=%s",
+             r.kernel, r.pair, r.mc, r.epi, r.pingpong, r.tile_m, r.bn, gb::kBK, r.stages, r.d_boxes, r.r_boxes, r.grid,
+             r.tiles, r.k_blocks, r.splits, r.group, r.zigzag, r.prod, r.hint_a, r.hint_b, r.hint_r, r.hint_d, r.d_store,
+             r.r_load, r.z_store);
     return GB_OK;
 }
 

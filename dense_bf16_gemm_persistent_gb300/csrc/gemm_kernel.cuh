@@ -1957,7 +1957,9 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 drain_bar(smem_addr(&rbar[e * kMaxBoxes + slot]), (r_phase >> slot) & 1u, p.timeout_ns);
                 if (++slot == p.r_boxes) slot = 0;
             }
-            bulk_wait_group<0>();
+            // the staging boxes must outlive the TMA stores' reads of them; the stores'
+            // global writes complete with the grid
+            bulk_wait_group_read<0>();
         }
         __syncwarp();
 
