@@ -108,8 +108,10 @@ def _mat(t: torch.Tensor | None, name: str, rows: int | None = None, cols: int |
         raise ValueError(f"{name}: expected a 2-D tensor with a contiguous last dimension")
     if rows is not None and t.shape[0] != rows or cols is not None and t.shape[1] != cols:
         raise ValueError(f"{name}: shape {tuple(t.shape)} does not match ({rows}, {cols})")
-    ld = t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
-    return t.data_ptr(), ld
+    # one row: its stride is arbitrary; keep a real row pitch (e.g. of a padded buffer's
+    # view) when there is one, else the width
+    ld = t.stride(0) if t.shape[0] > 1 or t.stride(0) >= t.shape[1] else max(t.shape[1], 1)
+    return t.data_ptr(), max(ld, 1)
 
 
 def _stream(stream) -> int:
