@@ -588,6 +588,10 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     const int wide_mode = cfg.wide >= 0 ? cfg.wide : (V::kEpi == 4 ? 2 : 1);
     if (paired && wide_fits && wide_mode == 1) flags |= gb::kFlagWide;
     if (paired && wide_fits && wide_mode == 2) flags |= gb::kFlagWideD;
+    // The express path (no epilogue input, no second output, TMA-stored D, no split) of the
+    // one-warpgroup kernel stages two adjacent chunks into one 32x64 D box per step as well.
+    const bool express = splits == 1 && pr.k > 0 && d_tma && !pr.r && !pr.z;
+    if (express && V::kEpi == 1 && wide_fits && wide_mode >= 1) flags |= gb::kFlagWideD;
     const bool z_tma = pr.z && aligned16(pr.z) && pr.ldz % 8 == 0;
     if (!pr.ffn && pr.z) flags |= gb::kFlagZ | (z_tma ? gb::kFlagZTma : 0u);
     prm.z = static_cast<uint16_t*>(pr.z);

@@ -1615,82 +1615,189 @@ __global__ void __launch_bounds__(128 * (1 + EPI), 1) gemm_persistent_kernel(con
                 if (express) {
                     // Express path (no epilogue input, no second output, TMA-stored D, no
                     // split): a compact loop, so the hot epilogue code next to the MMA
-                    // issuer stays small.
+                    // issuer stays small.  With 32x64 D boxes (kFlagWideD) a step is two
+                    // adjacent chunks (2 c0 + 2 i cstep and the next) staged into one box:
+                    // one box wait, one proxy fence and one TMA store per 64 columns; a box
+                    // half past N is clipped by the store.
+                    if constexpr (EPI == 1) {
+                        const bool wide_e = p.flags & kFlagWideD;
+                        const int halves = wide_e ? 2 : 1;
+                        const int adv = wide_e ? 2 * cstep : cstep;
+                        const int nbox = wide_e ? p.d_boxes >> 1 : p.d_boxes;
 #pragma unroll 1
-                    for (int c = c0; c < kChunks; c += cstep) {
-                        const int32_t n0 = nb * BN + c * kDChunk;
-                        const bool chunk_on = warp_rows && n0 < p.n;
-                        float v[32];
-                        GB_TR_T0(tx);
-                        if (chunk_on) {
-                            uint32_t r0[32];
-                            tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
-                            if (NUM_B == 2) {
-                                uint32_t r1[32];
-                                tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
-                                tmem_wait_ld();
+                        for (int c = wide_e ? 2 * c0 : c0; c < kChunks; c += adv) {
+                            const bool last_step = c + adv >= kChunks;
+                            uint32_t buf = 0;
+                            bool staged = false;
+#pragma unroll 1
+                            for (int i = 0; i < halves; ++i) {
+                                const int ci = c + i;
+                                const int32_t n0 = nb * BN + ci * kDChunk;
+                                const bool chunk_on = warp_rows && n0 < p.n;
+                                float v[32];
+                                GB_TR_T0(tx);
+                                if (chunk_on) {
+                                    uint32_t r0[32];
+                                    tmem_ld_32x32b_x32(tcol + ci * kDChunk, r0);
+                                    if (NUM_B == 2) {
+                                        uint32_t r1[32];
+                                        tmem_ld_32x32b_x32(tcol + BN + ci * kDChunk, r1);
+                                        tmem_wait_ld();
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
-                            } else {
-                                tmem_wait_ld();
+                                        for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                                    } else {
+                                        tmem_wait_ld();
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                                    }
+                                }
+                                if (last_step && i == halves - 1) {  // this warp's last TMEM reads of the buffer
+                                    tc_fence_before_sync();
+                                    __syncwarp();
+                                    if (lane == 0) {
+                                        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
+                                        else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                                    }
+                                }
+                                GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
+                                if (!chunk_on) continue;
+                                if (NUM_B == 1) {
+                                    if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
+                                    switch (p.act) {
+                                        case 1:
+#pragma unroll
+                                            for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                                            break;
+                                        case 2:
+#pragma unroll
+                                            for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                                            break;
+                                        case 3:
+#pragma unroll
+                                            for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                                            break;
+                                        default:
+                                            break;
+                                    }
+                                }
+                                uint32_t packed[16];  // (packed before the box wait: v's registers are free by then)
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                                GB_TR_ADD(tr_ep, kTrEpMath, tx);
+                                if (!staged) {
+                                    buf = dbox + dslot * d_slot_bytes(p);
+                                    // the store that last used this box has read it
+                                    if (lane == 0) bulk_wait_group_read_at_most(nbox - 1);
+                                    __syncwarp();
+                                    if (++dslot == nbox) dslot = 0;
+                                    staged = true;
+                                }
+                                GB_TR_ADD(tr_ep, kTrEpDBox, tx);
+                                {
+                                    // 32x64 box, 128-byte swizzle: unit u of row r at u ^ (r % 8); 32x32
+                                    // box, 64-byte swizzle: unit u at u ^ ((r / 2) % 4)
+                                    const uint32_t row_addr = buf + lane * (wide_e ? 128 : 64);
+                                    const uint32_t sw = wide_e ? (lane & 7u) : ((lane >> 1) & 3u);
+                                    const uint32_t u0 = wide_e ? 4u * static_cast<uint32_t>(i) : 0u;
+#pragma unroll
+                                    for (uint32_t u = 0; u < 4; ++u)
+                                        st_shared_v4(row_addr + (((u0 + u) ^ sw) << 4), packed[4 * u], packed[4 * u + 1],
+                                                     packed[4 * u + 2], packed[4 * u + 3]);
+                                }
+                                GB_TR_ADD(tr_ep, kTrEpMath, tx);
                             }
-                        }
-                        if (c + cstep >= kChunks) {
-                            tc_fence_before_sync();
+                            if (!staged) continue;
+                            GB_TR_T0(ts);
+                            fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
-                                else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                                tma_store_op(&p.tm_d, buf, nb * BN + c * kDChunk, row0, p.hint_d);
+                                bulk_commit_group();
                             }
-                        }
-                        GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
-                        if (!chunk_on) continue;
-                        if (NUM_B == 1) {
-                            if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
-                            switch (p.act) {
-                                case 1:
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
-                                    break;
-                                case 2:
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
-                                    break;
-                                case 3:
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
-                                    break;
-                                default:
-                                    break;
-                            }
-                        }
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                        GB_TR_ADD(tr_ep, kTrEpMath, tx);
-                        const uint32_t buf = dbox + dslot * kDStageBytes;
-                        if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
-                        __syncwarp();
-                        GB_TR_ADD(tr_ep, kTrEpDBox, tx);
-                        const uint32_t row_addr = buf + lane * 64;
-                        const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
-                                         packed[4 * u + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_op(&p.tm_d, buf, n0, row0, p.hint_d);
-                            bulk_commit_group();
-                        }
-                        if (++dslot == p.d_boxes) dslot = 0;
-                        GB_TR_ADD(tr_ep, kTrEpStore, tx);
+                            GB_TR_ADD(tr_ep, kTrEpStore, ts);
 #ifdef GB_TRACE
-                        if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+                            if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
 #endif
+                        }
+                    } else {
+                        // (two epilogue warpgroups: 32x32 boxes only -- the 32x64 step's extra live
+                        // state does not fit the 168 registers of the 384-thread launch)
+#pragma unroll 1
+                        for (int c = c0; c < kChunks; c += cstep) {
+                            const int32_t n0 = nb * BN + c * kDChunk;
+                            const bool chunk_on = warp_rows && n0 < p.n;
+                            float v[32];
+                            GB_TR_T0(tx);
+                            if (chunk_on) {
+                                uint32_t r0[32];
+                                tmem_ld_32x32b_x32(tcol + c * kDChunk, r0);
+                                if (NUM_B == 2) {
+                                    uint32_t r1[32];
+                                    tmem_ld_32x32b_x32(tcol + BN + c * kDChunk, r1);
+                                    tmem_wait_ld();
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                                } else {
+                                    tmem_wait_ld();
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+                                }
+                            }
+                            if (c + cstep >= kChunks) {
+                                tc_fence_before_sync();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[b]), lead));
+                                    else mbar_arrive(smem_addr(&ctl->acc_empty[b]));
+                                }
+                            }
+                            GB_TR_ADD(tr_ep, kTrEpTmemLd, tx);
+                            if (!chunk_on) continue;
+                            if (NUM_B == 1) {
+                                if (p.flags & kFlagBias) add_bf16_row(v, p.bias + n0, min(32, p.n - n0), p.flags & kFlagBiasVec);
+                                switch (p.act) {
+                                    case 1:
+#pragma unroll
+                                        for (int j = 0; j < 32; ++j) v[j] = act_apply(1, v[j]);
+                                        break;
+                                    case 2:
+#pragma unroll
+                                        for (int j = 0; j < 32; ++j) v[j] = act_apply(2, v[j]);
+                                        break;
+                                    case 3:
+#pragma unroll
+                                        for (int j = 0; j < 32; ++j) v[j] = act_apply(3, v[j]);
+                                        break;
+                                    default:
+                                        break;
+                                }
+                            }
+                            uint32_t packed[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                            GB_TR_ADD(tr_ep, kTrEpMath, tx);
+                            const uint32_t buf = dbox + dslot * kDStageBytes;
+                            if (lane == 0) bulk_wait_group_read_at_most(p.d_boxes - 1);  // the store that last used this box has read it
+                            __syncwarp();
+                            GB_TR_ADD(tr_ep, kTrEpDBox, tx);
+                            const uint32_t row_addr = buf + lane * 64;
+                            const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                st_shared_v4(row_addr + ((u ^ sw) << 4), packed[4 * u], packed[4 * u + 1], packed[4 * u + 2],
+                                             packed[4 * u + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_op(&p.tm_d, buf, n0, row0, p.hint_d);
+                                bulk_commit_group();
+                            }
+                            if (++dslot == p.d_boxes) dslot = 0;
+                            GB_TR_ADD(tr_ep, kTrEpStore, tx);
+#ifdef GB_TRACE
+                            if (tr_ep) tr_ep[kTrEpSteps - kTrEpDBox] += 1;
+#endif
+                        }
                     }
                     continue;
                 }
