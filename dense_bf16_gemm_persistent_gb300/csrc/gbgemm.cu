@@ -77,7 +77,6 @@ struct Config {
     int hint_a = -1, hint_b = -1, hint_r = -1, hint_d = -1;
     int mc = -1;         // A multicast between two CTA pairs (4-CTA clusters): -1 auto, 0 off, 1 on
     int issue = -1;      // MMA issue loop: -1 auto, 0 rebuild, 1 lean, 2 lean with look-ahead wait
-    int tmem_ld = 0;     // TMEM columns per load on the express path: 0 auto, 32 or 64
     int prod = 0;        // producer threads: 0 auto, 1 or 2 (A and B loads issued by different warps)
     int r_async = -1;    // unaligned R rows (no split): -1 auto, 0 synchronous loads at use, 1 cp.async queue
     int r_boxes = 0;     // R queue depth per epilogue warp: 0 = heuristic, 2..8
@@ -552,7 +551,6 @@ gb_status_t plan_and_launch(const Problem& pr, const Config& cfg, int bn, int de
     prm.hint_r = hint(cfg.hint_r, 0);
     prm.hint_d = hint(cfg.hint_d, long_k ? 1 : 0);
     prm.issue = cfg.issue >= 0 ? cfg.issue : 0;
-    prm.tmem_ld = cfg.tmem_ld > 0 ? cfg.tmem_ld : 32;
     // two producer threads by default: measured 7-12 % faster than one on the MLP, FFN,
     // activation-gradient, 64-bit and unaligned shapes (one thread issuing both loads of
     // every stage falls behind the MMAs)
@@ -1163,7 +1161,6 @@ gb_status_t gb_set_config(const char* spec) {
             else if (key == "hint_d" && v >= -1 && v <= 2) c.hint_d = static_cast<int>(v);
             else if (key == "mc" && v >= -1 && v <= 1) c.mc = static_cast<int>(v);
             else if (key == "issue" && v >= -1 && v <= 3) c.issue = static_cast<int>(v);
-            else if (key == "tmem_ld" && (v == 0 || v == 32 || v == 64)) c.tmem_ld = static_cast<int>(v);
             else if (key == "prod" && v >= 0 && v <= 3) c.prod = static_cast<int>(v);
             else if (key == "r_async" && v >= -1 && v <= 1) c.r_async = static_cast<int>(v);
             else if (key == "r_boxes" && (v == 0 || (v >= 2 && v <= gb::kMaxBoxes))) c.r_boxes = static_cast<int>(v);

@@ -173,7 +173,6 @@ struct GemmParams {  // the CUtensorMap members give it their 64-byte alignment
     // third MMA runs, before its fourth is issued
     int32_t issue;
     // TMEM columns per tcgen05.ld on the express path (32, or 64: two chunks per load)
-    int32_t tmem_ld;
     // producer threads: 1 (warp 0 issues the A and B loads of every stage) or 2 (warp 0
     // the A loads and the expected byte count, warp 2 the B loads)
     int32_t prod;

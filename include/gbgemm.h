@@ -293,8 +293,8 @@ GB_API const char* gb_last_error(void);
  * kernel), r_async (R rows that are not 16-byte aligned, without split: 1 =
  * per-lane cp.async word copies into a prefetch queue, 0 or -1 = synchronous
  * loads at use), mc (1 = A multicast between two CTA pairs in 4-CTA clusters,
- * without split), issue (MMA issue loop variant 0..3), tmem_ld (TMEM columns
- * per load on the express path: 32 or 64), prod (producer threads: 1 or 2),
+ * without split), issue (MMA issue loop variant 0..3), prod (producer threads:
+ * 1, 2 or 3; the lean loads need 2),
  * hint_a, hint_b, hint_r, hint_d (L2 eviction policy of the TMA loads of A,
  * of B / W1 / W3, of R, and of the TMA stores of D and Z: 0 = none, 1 = evict
  * first, 2 = evict last, -1 = the built-in choice).
