@@ -42,6 +42,8 @@ class GBError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """Load libgbgemm.so (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -104,13 +106,15 @@ def _mat(t: torch.Tensor | None, name: str, rows: int | None = None, cols: int |
         return None, 0
     if t.dtype != torch.bfloat16 or not t.is_cuda:
         raise TypeError(f"{name}: expected a CUDA bfloat16 tensor, got {t.dtype} on {t.device}")
-    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+    shape, stride = t.shape, t.stride()  # (each attribute read costs host time on small calls)
+    if len(shape) != 2 or (shape[1] > 1 and stride[1] != 1):
         raise ValueError(f"{name}: expected a 2-D tensor with a contiguous last dimension")
-    if rows is not None and t.shape[0] != rows or cols is not None and t.shape[1] != cols:
-        raise ValueError(f"{name}: shape {tuple(t.shape)} does not match ({rows}, {cols})")
+    r, c = shape
+    if rows is not None and r != rows or cols is not None and c != cols:
+        raise ValueError(f"{name}: shape {tuple(shape)} does not match ({rows}, {cols})")
     # one row: its stride is arbitrary; keep a real row pitch (e.g. of a padded buffer's
     # view) when there is one, else the width
-    ld = t.stride(0) if t.shape[0] > 1 or t.stride(0) >= t.shape[1] else max(t.shape[1], 1)
+    ld = stride[0] if r > 1 or stride[0] >= c else max(c, 1)
     return t.data_ptr(), max(ld, 1)
 
 
