@@ -359,10 +359,14 @@ def oracle_sample_run(wl: dict, h: dict, rows: int):
 
 
 def calibrate_rows(wl: dict, target_s: float) -> tuple[int, dict]:
-    """Rows of output the oracle computes in about target_s seconds, and their inputs."""
-    h = oracle_sample_inputs(wl, 4)
-    dt, _, _ = oracle_sample_run(wl, h, 4)
-    rows = min(max(4, int(4 * target_s / max(dt, 1e-3))), wl["M"])
+    """Rows of output the oracle computes in about target_s seconds, and their inputs.  The
+    timing probe has two rows per host thread, so the estimate sees the oracle's parallel
+    rate (it parallelises over rows)."""
+    import oracle
+    probe = min(max(4, 2 * oracle.num_threads()), wl["M"])
+    h = oracle_sample_inputs(wl, probe)
+    dt, _, _ = oracle_sample_run(wl, h, probe)
+    rows = min(max(probe, int(probe * target_s / max(dt, 1e-3))), wl["M"])
     return rows, oracle_sample_inputs(wl, rows)
 
 
