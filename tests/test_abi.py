@@ -106,6 +106,22 @@ def test_config_parser(L):
     assert L.gb_set_config(None) == GB_OK
 
 
+def test_every_config_key_is_documented_and_accepted(L):
+    """Each key gb_set_config takes is described in the header, and accepted alone."""
+    header = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                               "gbgemm.h")).read()
+    decl = header.index("gb_status_t gb_set_config(")
+    doc = header[header.rindex("/*", 0, decl):decl]  # the comment block above the declaration
+    keys = {"bn": 256, "grid": 8, "persistent": 1, "group": 16, "zigzag": 0, "pair": 0, "stages": 4, "epi": 2,
+            "boxes": 2, "r_boxes": 3, "pingpong": 0, "hint_a": 2, "hint_b": 1, "hint_r": 0, "hint_d": 1, "mc": 1,
+            "issue": 3, "prod": 1, "r_async": 1, "wide": 2}
+    for k, v in keys.items():
+        assert re.search(r"\b" + k + r"\b", doc), f"{k} is not described in gbgemm.h"
+        assert L.gb_set_config(f"{k}={v}".encode()) == GB_OK, k
+    assert L.gb_set_config(b"tmem_ld=64") == GB_ERR_INVALID_ARG  # (a key the planner never read; removed)
+    assert L.gb_set_config(None) == GB_OK
+
+
 def test_misc_entry_points(L):
     assert L.gb_set_wait_timeout_ns(1000) == GB_OK
     assert L.gb_set_wait_timeout_ns(0) == GB_OK
